@@ -1,0 +1,460 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Nothing here compares the oracle with itself: each pin checks a hand-derived
+closed form (tests/golden/hand_cases.json), an invariant the pages state, a
+brute-force enumeration on tiny inputs, or a special case that reduces to a
+library routine (torch float64 on the CPU, scipy).  The planted-mistake test
+at the end applies plausible mistakes to the oracle, on the CPU, and checks
+that at least one pin catches each.
+"""
+
+import itertools
+import json
+import math
+import os
+import types
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_mixture_experts_67_b300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
+
+
+def _golden():
+    with open(GOLDEN) as fh:
+        return json.load(fh)
+
+
+def _log_entry(v):
+    return 0.0 if v == 0 else math.log(v)
+
+
+def _frac(a):
+    return np.vectorize(lambda s: float(Fraction(s)))(np.asarray(a, dtype=object)).astype(np.float64)
+
+
+def _rand_experts(rng, E, d, F, scale=0.3):
+    return [(rng.normal(0, scale, (F, d)), rng.normal(0, scale, (F, d)), rng.normal(0, scale, (d, F)))
+            for _ in range(E)]
+
+
+# --------------------------------------------------------------------------- pins
+
+
+def pin_golden_route(orc):
+    g = _golden()
+    for name in ("route_two_tokens", "route_three_experts_top2"):
+        case = g[name]
+        x = np.asarray(case["x"], np.float64)
+        w_g = np.vectorize(_log_entry)(np.asarray(case["w_g_log"], np.float64))
+        s = orc.router_logits(x, w_g)
+        idx, w, probs = orc.topk_route(s, case["k"])
+        assert idx.tolist() == case["idx"], name
+        np.testing.assert_allclose(w, _frac(case["w"]), rtol=0, atol=1e-15)
+        np.testing.assert_allclose(probs, _frac(case["g"]), rtol=0, atol=1e-15)
+        counts, f, p, loss = orc.aux_stats(probs, idx, w_g.shape[0])
+        assert counts.tolist() == case["counts"], name
+        np.testing.assert_allclose(f, _frac(case["f"]), rtol=0, atol=1e-15)
+        np.testing.assert_allclose(p, _frac(case["p"]), rtol=0, atol=1e-15)
+        assert abs(loss - float(Fraction(case["loss"]))) < 1e-14, name
+
+
+def pin_golden_dispatch(orc):
+    case = _golden()["dispatch_three_tokens"]
+    counts, offsets, perm, inv_perm = orc.dispatch(np.asarray(case["idx"]), case["E"])
+    assert counts.tolist() == case["counts"]
+    assert offsets.tolist() == case["offsets"]
+    assert perm.tolist() == case["perm"]
+    assert inv_perm.tolist() == case["inv_perm"]
+
+
+def pin_golden_expert_choice(orc):
+    case = _golden()["expert_choice_four_tokens"]
+    s = np.vectorize(_log_entry)(np.asarray(case["s_log"], np.float64))
+    C, ec_idx, ec_score, pos = orc.expert_choice_route(s, case["capacity_factor"])
+    assert C == case["C"]
+    assert ec_idx.tolist() == case["ec_idx"]
+    np.testing.assert_allclose(ec_score, _frac(case["ec_score"]), rtol=0, atol=1e-15)
+    assert pos.tolist() == case["pos"]
+
+
+def pin_golden_silu(orc):
+    case = _golden()["silu_values"]
+    np.testing.assert_allclose(orc.silu(np.asarray(case["a"])), case["silu"], rtol=1e-15, atol=0)
+    scalar = _golden()["swiglu_scalar"]
+    y = orc.swiglu_expert(np.array([[scalar["x"]]]), np.array([[scalar["w_gate"]]]),
+                          np.array([[scalar["w_up"]]]), np.array([[scalar["w_down"]]]))
+    assert abs(y[0, 0] - scalar["y"]) < 1e-14
+
+
+def pin_silu_vs_scipy(orc):
+    from scipy.special import expit
+
+    a = np.linspace(-30, 30, 1001)
+    np.testing.assert_allclose(orc.silu(a), a * expit(a), rtol=1e-13, atol=1e-300)
+
+
+def pin_weights_sum_to_one(orc):
+    rng = np.random.default_rng(1)
+    for E in (2, 5, 8, 64):
+        s = rng.normal(0, 2.0, (37, E))
+        for k in sorted({1, 2, min(4, E), E}):
+            idx, w, _ = orc.topk_route(s, k)
+            np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+            if k == 1:
+                assert np.all(w == 1.0)
+
+
+def pin_topk_on_logits_form(orc):
+    """[zh-moe] torch MoELayer: top-k of the logits, then softmax over those k logits."""
+    rng = np.random.default_rng(2)
+    s = rng.normal(0, 1.5, (50, 8))
+    idx, w, _ = orc.topk_route(s, 3)
+    top = np.take_along_axis(s, idx, axis=1)
+    z = np.exp(top - top.max(axis=1, keepdims=True))
+    np.testing.assert_allclose(w, z / z.sum(axis=1, keepdims=True), rtol=0, atol=1e-15)
+
+
+def pin_topk_brute_force(orc):
+    rng = np.random.default_rng(3)
+    for E in (3, 5, 8):
+        for k in range(1, E + 1):
+            s = rng.normal(0, 1.0, (6, E))
+            idx, w, g = orc.topk_route(s, k)
+            for t in range(s.shape[0]):
+                best = max(itertools.combinations(range(E), k), key=lambda c: sum(g[t, list(c)]))
+                assert sorted(idx[t].tolist()) == sorted(best)
+                assert all(g[t, idx[t, j]] > g[t, idx[t, j + 1]] for j in range(k - 1))
+
+
+def pin_all_ties(orc):
+    """W_g = 0: every logit ties, so the lower-index rule fixes everything in closed form."""
+    T, d = 10, 6
+    x = np.random.default_rng(4).normal(size=(T, d))
+    for E, k in ((8, 2), (5, 5), (64, 4)):
+        s = orc.router_logits(x, np.zeros((E, d)))
+        idx, w, g = orc.topk_route(s, k)
+        assert np.all(idx == np.arange(k)[None, :])
+        np.testing.assert_allclose(w, 1.0 / k, rtol=0, atol=1e-15)
+        counts, f, p, loss = orc.aux_stats(g, idx, E)
+        assert counts.tolist() == [T] * k + [0] * (E - k)
+        np.testing.assert_allclose(f, [1.0] * k + [0.0] * (E - k), rtol=0, atol=0)
+        np.testing.assert_allclose(p, 1.0 / E, rtol=0, atol=1e-15)
+        assert abs(loss - k) < 1e-12
+
+
+def pin_bias_only(orc):
+    """x = 0: the logits are the bias ([zh-moe] GatingNetwork adds b)."""
+    b = np.array([1.5 * math.log(1.0 / (e + 1)) for e in range(6)])
+    s = orc.router_logits(np.zeros((3, 4)), np.ones((6, 4)), b)
+    np.testing.assert_array_equal(s, np.broadcast_to(b, (3, 6)))
+    idx, w, _ = orc.topk_route(s, 2)
+    assert idx.tolist() == [[0, 1]] * 3
+    # b_0 = 0, b_1 = 1.5 ln(1/2): weights 1 : 2^-1.5
+    r = 2.0 ** -1.5
+    np.testing.assert_allclose(w[0], [1 / (1 + r), r / (1 + r)], rtol=1e-15)
+
+
+def pin_aux_invariants(orc):
+    rng = np.random.default_rng(5)
+    for E, k in ((8, 2), (64, 4), (16, 1)):
+        s = rng.normal(0, 1.0, (200, E))
+        idx, w, g = orc.topk_route(s, k)
+        counts, f, p, loss = orc.aux_stats(g, idx, E)
+        assert counts.sum() == 200 * k
+        assert abs(f.sum() - k) < 1e-12
+        assert abs(p.sum() - 1) < 1e-12
+        assert loss > 0
+
+
+def pin_uniform_loss_is_k(orc):
+    """Perfectly balanced routing with uniform probabilities gives loss = k ([moe-theory] demo's ideal)."""
+    E, k = 8, 2
+    T = 8 * 5
+    idx = np.array([[(t + j) % E for j in range(k)] for t in range(T)])
+    g = np.full((T, E), 1.0 / E)
+    counts, f, p, loss = orc.aux_stats(g, idx, E)
+    assert counts.tolist() == [T * k // E] * E
+    assert abs(loss - k) < 1e-12
+
+
+def pin_dispatch_brute_force(orc):
+    rng = np.random.default_rng(6)
+    for T, E, k in ((1, 1, 1), (13, 5, 2), (40, 8, 3), (7, 64, 4)):
+        idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)])
+        counts, offsets, perm, inv_perm = orc.dispatch(idx, E)
+        rows = []
+        for e in range(E):
+            for t in range(T):
+                for j in range(k):
+                    if idx[t, j] == e:
+                        rows.append(t * k + j)
+        assert perm.tolist() == rows
+        assert sorted(perm.tolist()) == list(range(T * k))
+        assert np.all(inv_perm[perm] == np.arange(T * k))
+        assert offsets[0] == 0 and np.all(np.diff(offsets) == counts)
+        for e in range(E):
+            seg = perm[offsets[e]:offsets[e + 1]]
+            assert np.all(np.diff(seg) > 0)
+            assert np.all(idx.reshape(-1)[seg] == e)
+
+
+def pin_swiglu_vs_torch(orc):
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as tf
+
+    rng = np.random.default_rng(7)
+    n, d, F = 9, 6, 11
+    x = rng.normal(size=(n, d))
+    wg, wu, wd = rng.normal(size=(F, d)), rng.normal(size=(F, d)), rng.normal(size=(d, F))
+    tx = torch.from_numpy(x)
+    ref = (tf.silu(tf.linear(tx, torch.from_numpy(wg))) * tf.linear(tx, torch.from_numpy(wu)))
+    ref = tf.linear(ref, torch.from_numpy(wd)).numpy()
+    np.testing.assert_allclose(orc.swiglu_expert(x, wg, wu, wd), ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_zero_input(orc):
+    rng = np.random.default_rng(8)
+    experts = _rand_experts(rng, 4, 5, 7)
+    idx = np.array([[0, 3], [2, 1]])
+    w = np.array([[0.6, 0.4], [0.3, 0.7]])
+    y = orc.moe_forward(np.zeros((2, 5)), idx, w, experts)
+    assert np.all(y == 0)
+
+
+def pin_dense_limit(orc):
+    """k = E: the renormalised weights are the full softmax, so the layer is the dense mixture."""
+    rng = np.random.default_rng(9)
+    T, d, F, E = 12, 5, 7, 4
+    x = rng.normal(size=(T, d))
+    experts = _rand_experts(rng, E, d, F)
+    s = orc.router_logits(x, rng.normal(0, 0.5, (E, d)))
+    idx, w, g = orc.topk_route(s, E)
+    np.testing.assert_allclose(orc.moe_forward(x, idx, w, experts), orc.dense_mixture(x, g, experts),
+                               rtol=1e-12, atol=1e-12)
+    # the dense mixture itself against a direct torch evaluation
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as tf
+
+    tx = torch.from_numpy(x)
+    ref = torch.zeros_like(tx)
+    for e, (wg, wu, wd) in enumerate(experts):
+        h = tf.silu(tf.linear(tx, torch.from_numpy(wg))) * tf.linear(tx, torch.from_numpy(wu))
+        ref += torch.from_numpy(g[:, e:e + 1]) * tf.linear(h, torch.from_numpy(wd))
+    np.testing.assert_allclose(orc.dense_mixture(x, g, experts), ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def pin_identical_experts(orc):
+    """All experts equal: weights sum to 1, so y = E_0(x) for any k."""
+    rng = np.random.default_rng(10)
+    T, d, F, E = 15, 6, 9, 8
+    x = rng.normal(size=(T, d))
+    one = _rand_experts(rng, 1, d, F)[0]
+    s = orc.router_logits(x, rng.normal(0, 1.0, (E, d)))
+    for k in (1, 2, 5):
+        idx, w, _ = orc.topk_route(s, k)
+        np.testing.assert_allclose(orc.moe_forward(x, idx, w, [one] * E), orc.swiglu_expert(x, *one),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def pin_single_slot_selects_expert(orc):
+    """k = 1: y_t is exactly the output of the selected expert on x_t."""
+    rng = np.random.default_rng(11)
+    T, d, F, E = 10, 4, 6, 3
+    x = rng.normal(size=(T, d))
+    experts = _rand_experts(rng, E, d, F)
+    s = orc.router_logits(x, rng.normal(0, 1.0, (E, d)))
+    idx, w, _ = orc.topk_route(s, 1)
+    y = orc.moe_forward(x, idx, w, experts)
+    for t in range(T):
+        np.testing.assert_allclose(y[t], orc.swiglu_expert(x[t:t + 1], *experts[idx[t, 0]])[0],
+                                   rtol=1e-13, atol=1e-13)
+
+
+def pin_expert_choice_invariants(orc):
+    rng = np.random.default_rng(12)
+    for T, E, cf in ((30, 4, 1.0), (64, 16, 2.0), (9, 3, 0.25), (16, 4, 4.0)):
+        s = rng.normal(0, 1.0, (T, E))
+        C, ec_idx, ec_score, pos = orc.expert_choice_route(s, cf)
+        assert C == int(T * cf // E)
+        assert ec_idx.shape == (E, C)
+        for e in range(E):
+            assert len(set(ec_idx[e].tolist())) == C
+            col = np.exp(s[:, e] - s[:, e].max())
+            col /= col.sum()
+            assert abs(col.sum() - 1) < 1e-12
+            np.testing.assert_allclose(ec_score[e], col[ec_idx[e]], rtol=1e-14)
+            assert np.all(np.diff(ec_score[e]) <= 0)
+        assert int((pos >= 0).sum()) == E * C
+        for e in range(E):
+            for c in range(C):
+                assert pos[e, ec_idx[e, c]] == e * C + c
+
+
+def pin_expert_choice_brute_force(orc):
+    rng = np.random.default_rng(13)
+    for T, E, cf in ((8, 2, 1.0), (12, 3, 1.0), (10, 5, 2.0)):
+        s = rng.normal(0, 1.0, (T, E))
+        C, ec_idx, ec_score, _ = orc.expert_choice_route(s, cf)
+        for e in range(E):
+            best = max(itertools.combinations(range(T), C), key=lambda c: sum(np.exp(s[list(c), e])))
+            assert sorted(ec_idx[e].tolist()) == sorted(best)
+
+
+def pin_expert_choice_ties_and_empty(orc):
+    s = np.zeros((10, 4))
+    C, ec_idx, ec_score, pos = orc.expert_choice_route(s, 2.0)
+    assert C == 5
+    assert np.all(ec_idx == np.arange(5)[None, :])
+    np.testing.assert_allclose(ec_score, 0.1, rtol=0, atol=1e-16)
+    C0, idx0, sc0, pos0 = orc.expert_choice_route(s, 0.3)
+    assert C0 == 0 and idx0.shape == (4, 0) and np.all(pos0 == -1)
+    y = orc.expert_choice_forward(np.ones((10, 3)), idx0, sc0, _rand_experts(np.random.default_rng(0), 4, 3, 2))
+    assert np.all(y == 0)
+
+
+def pin_expert_choice_forward(orc):
+    """Only tokens chosen by an expert receive its output, weighted by the raw score."""
+    rng = np.random.default_rng(14)
+    T, d, F, E = 12, 4, 5, 3
+    x = rng.normal(size=(T, d))
+    experts = _rand_experts(rng, E, d, F)
+    s = rng.normal(size=(T, E))
+    C, ec_idx, ec_score, pos = orc.expert_choice_route(s, 1.0)
+    y = orc.expert_choice_forward(x, ec_idx, ec_score, experts)
+    for t in range(T):
+        ref = np.zeros(d)
+        for e in range(E):
+            if pos[e, t] >= 0:
+                c = pos[e, t] - e * C
+                ref += ec_score[e, c] * orc.swiglu_expert(x[t:t + 1], *experts[e])[0]
+        np.testing.assert_allclose(y[t], ref, rtol=1e-13, atol=1e-15)
+
+
+def pin_bf16_round(orc):
+    rng = np.random.default_rng(15)
+    a = (rng.normal(0, 3.0, 100000) * np.exp(rng.uniform(-20, 20, 100000))).astype(np.float32)
+    # exact halfway cases between bf16 neighbours exercise the ties-to-even rule
+    halfway = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(2.0 + 2.0 ** -7)], np.float32)
+    a = np.concatenate([a, halfway])
+    np.testing.assert_array_equal(orc.bf16_round(a.astype(np.float64)),
+                                  synth.to_f64(synth.round_to_bf16_bits(a)))
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(pin):
+    pin(oracle)
+
+
+# ------------------------------------------------------------- planted mistakes
+
+
+def _mutant(**overrides):
+    ns = types.SimpleNamespace(**{k: getattr(oracle, k) for k in dir(oracle) if not k.startswith("__")})
+    for k, v in overrides.items():
+        setattr(ns, k, v)
+    return ns
+
+
+def _no_renorm(s, k):
+    g = oracle.softmax(s, axis=1)
+    idx = oracle.topk_select(s, k)
+    return idx, np.take_along_axis(g, idx, axis=1), g
+
+
+def _smallest(s, k):
+    g = oracle.softmax(s, axis=1)
+    idx = np.argsort(s, axis=1, kind="stable")[:, :k]
+    sel = np.take_along_axis(g, idx, axis=1)
+    return idx, sel / sel.sum(axis=1, keepdims=True), g
+
+
+def _ties_high(s, k):
+    g = oracle.softmax(s, axis=1)
+    idx = (s.shape[1] - 1 - np.argsort(-s[:, ::-1], axis=1, kind="stable"))[:, :k]
+    sel = np.take_along_axis(g, idx, axis=1)
+    return idx, sel / sel.sum(axis=1, keepdims=True), g
+
+
+def _swap_gate_up(x, wg, wu, wd, round_h=None):
+    return oracle.swiglu_expert(x, wu, wg, wd, round_h)
+
+
+def _down_transposed(x, wg, wu, wd, round_h=None):
+    h = oracle.silu(x @ wg.T) * (x @ wu.T)
+    return h @ wd
+
+
+def _f_over_tk(g, idx, E):
+    counts, f, p, loss = oracle.aux_stats(g, idx, E)
+    f2 = f / idx.shape[1]
+    return counts, f2, p, float(E * np.sum(f2 * p))
+
+
+def _loss_no_E(g, idx, E):
+    counts, f, p, loss = oracle.aux_stats(g, idx, E)
+    return counts, f, p, loss / E
+
+
+def _dispatch_desc(idx, E):
+    counts, offsets, perm, inv_perm = oracle.dispatch(idx, E)
+    perm = perm.copy()
+    for e in range(E):
+        perm[offsets[e]:offsets[e + 1]] = perm[offsets[e]:offsets[e + 1]][::-1]
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(perm.size)
+    return counts, offsets, perm, inv
+
+
+def _ec_softmax_over_experts(s, cf):
+    T, E = s.shape
+    C, ec_idx, _, pos = oracle.expert_choice_route(s, cf)
+    g = oracle.softmax(s, axis=1)
+    return C, ec_idx, np.stack([g[ec_idx[e], e] for e in range(E)]), pos
+
+
+def _forward_unweighted(x, idx, w, experts, round_h=None):
+    return oracle.moe_forward(x, idx, np.ones_like(w), experts, round_h)
+
+
+def _silu_sign(a):
+    return a / (1.0 + np.exp(a))
+
+
+def _no_bias(x, w_g, bias=None):
+    return oracle.router_logits(x, w_g, None)
+
+
+MUTANTS = {
+    "no_renormalisation": dict(topk_route=_no_renorm),
+    "select_smallest": dict(topk_route=_smallest),
+    "ties_to_higher_index": dict(topk_route=_ties_high),
+    "gate_up_swapped": dict(swiglu_expert=_swap_gate_up),
+    "down_transposed": dict(swiglu_expert=_down_transposed),
+    "f_over_T_times_k": dict(aux_stats=_f_over_tk),
+    "loss_without_E": dict(aux_stats=_loss_no_E),
+    "dispatch_unstable": dict(dispatch=_dispatch_desc),
+    "ec_softmax_over_experts": dict(expert_choice_route=_ec_softmax_over_experts),
+    "forward_ignores_weights": dict(moe_forward=_forward_unweighted),
+    "silu_sign": dict(silu=_silu_sign),
+    "bias_dropped": dict(router_logits=_no_bias),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name):
+    orc = _mutant(**MUTANTS[name])
+    caught = []
+    for pin in PINS:
+        try:
+            pin(orc)
+        except Exception:  # noqa: BLE001 - any failure of a pin counts as caught
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake {name}"
