@@ -1,0 +1,437 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse MoE SwiGLU layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl {moe,reference}]
+
+One step = one full layer forward (router, dispatch, gate/up GEMM + SwiGLU,
+down GEMM, combine, aux statistics) over one batch of synthetic tokens of the
+workload, inputs resident in HBM.  L2 is flushed (a 256 MiB write) between
+timed steps; each step is timed with CUDA events on the launching stream.
+Prints one JSON line.  Under torchrun every rank runs its own replica of the
+workload (tokens are independent, no collective on the data path); the time
+is the max over ranks and the value counts the tokens of all ranks.
+
+--impl reference times the fp64 CPU oracle on bounded samples of the same
+workload on the host cores (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_mixture_experts_67_b300 import synth  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s and active TFLOP/s (% of B300 BF16 peak), 1 GPU"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+KERNEL_SOURCES = {"gateup": "sparse_mixture_experts_67_b300/csrc/grouped_tc.cuh"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="top2_d1024")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (large_d4096 sweep)")
+    ap.add_argument("--impl", default="moe", choices=["moe", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args(argv)
+
+
+def workload_config(args) -> synth.LayerConfig:
+    cfg = synth.CONFIGS[args.workload]
+    if args.tokens:
+        cfg = cfg.with_tokens(args.tokens)
+    return cfg
+
+
+def describe(cfg: synth.LayerConfig) -> str:
+    if cfg.routing == "expert_choice":
+        return (f"{cfg.name}: expert-choice T={cfg.T} d={cfg.d} F={cfg.F} E={cfg.E} "
+                f"cf={cfg.capacity_factor} C={cfg.C} {cfg.dtype}")
+    return f"{cfg.name}: top-{cfg.k} T={cfg.T} d={cfg.d} F={cfg.F} E={cfg.E} {cfg.dtype}"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)[kernel]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as fh:
+            sha = hashlib.sha256(fh.read()).hexdigest()
+        return rec if sha == rec["source_sha256"] else None
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+# ---------------------------------------------------------------- distributed
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(local_seconds: float, local_units: float, world_size: int, dist=None, device=None):
+    """Whole-job throughput: units of all ranks / max over ranks of the timed seconds."""
+    if world_size == 1 or dist is None:
+        return local_units / local_seconds, local_seconds, local_units
+    import torch
+
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([local_units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(u.item()) / float(t.item()), float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which: str):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[5 + i].strip().lower() == "active":
+                    reasons.add(n)
+        loaded = [v for v in sm if mx and v > 0.3 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+
+def run_gpu(args, cfg):
+    import torch
+
+    import sparse_mixture_experts_67_b300 as moe
+
+    ws, rank, local_rank = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    inp = synth.make_inputs(cfg)
+
+    def up(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    w = {"w_g": up(inp.w_g), "bias": None if inp.bias is None else up(inp.bias),
+         "w_gate": up(inp.w_gate), "w_up": up(inp.w_up), "w_down": up(inp.w_down)}
+    x = up(inp.x)
+    ec = cfg.routing == "expert_choice"
+    layer = moe.MoELayer(w, k=cfg.k, routing=1 if ec else 0, capacity_factor=cfg.capacity_factor)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(3, args.warmup)):
+        layer(x, y=y)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        layer(x, y=y)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    local_s = sum(step_ms) / 1e3
+
+    # per-stage breakdown through the individual entry points (same kernels)
+    stages = stage_breakdown(moe, torch, cfg, x, w, flush, stream, min(K, 50)) if not ec else {}
+    # end to end through the public API with host buffers
+    e2e = run_e2e(moe, torch, layer, inp.x, cfg, dev, min(K, 50))
+    clk = clocks.stop()
+
+    value, max_s, units = aggregate(local_s, float(cfg.T * K), ws, dist, dev)
+    if dist:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    ms = max_s * 1e3 / K
+    flops = cfg.active_flops()
+    peaks, peak_src = load_peaks()
+    tflops = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded normal x and weights of the workload's shape; no dataset)",
+        "config": {"workload": describe(cfg), "T_per_gpu": cfg.T, "d_model": cfg.d, "d_ff": cfg.F,
+                   "experts": cfg.E, "k": cfg.k, "routing": cfg.routing,
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "active_tflops": tflops,
+        "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
+                              "sustained": tflops / peaks["bf16_tflops_sustained"],
+                              "source": peak_src},
+        "stages_ms": stages,
+        "gpu_launches": launches_per_step(cfg) * K,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if stages:
+        gu_ms = stages.get("gateup_ms")
+        gu_flops = 4.0 * cfg.R * cfg.d * cfg.F
+        achieved = gu_flops / (gu_ms / 1e3) / 1e12
+        traffic = recorded_traffic("gateup")
+        line["roofline"] = {
+            "kernel": "grouped gate/up GEMM + SwiGLU", "bound": "tensor", "achieved": achieved,
+            "peak": peaks["bf16_tflops_sustained"], "peak_kind": f"bf16 sustained ({peak_src})",
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops_sustained"],
+            "frac_of_burst": achieved / peaks["bf16_tflops"],
+            "traffic": None if traffic is None else traffic["bytes_per_launch"],
+            "algorithmic_flops_per_launch": gu_flops,
+        }
+    if not args.no_cpu_baseline and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+    return line
+
+
+def launches_per_step(cfg) -> int:
+    if cfg.routing == "expert_choice":
+        return 7  # logits, EC select, offsets, gather, gate/up, down, EC combine
+    return 9  # router, hist, scan, scatter, gather, gate/up, down, combine, aux
+
+
+def stage_breakdown(moe, torch, cfg, x, w, flush, stream, steps):
+    """Average device ms per stage, timed with events between the entry points."""
+    names = ["route_ms", "permute_ms", "gateup_ms", "down_ms", "combine_ms", "aux_ms"]
+    acc = {n: 0.0 for n in names}
+    for i in range(steps + 3):
+        flush.fill_(i & 0xFF)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        evs[0].record(stream)
+        r = moe.moe_route(x, w["w_g"], w["bias"], cfg.k)
+        evs[1].record(stream)
+        p = moe.moe_permute(x, r["topk_idx"], cfg.E)
+        evs[2].record(stream)
+        h = moe.moe_grouped_gateup_swiglu(p["x_perm"], p["offsets"], w["w_gate"], w["w_up"])
+        evs[3].record(stream)
+        yp = moe.moe_grouped_down(h, p["offsets"], w["w_down"])
+        evs[4].record(stream)
+        moe.moe_combine(yp, p["inv_perm"], r["topk_w"])
+        evs[5].record(stream)
+        moe.moe_aux_loss(p["counts"], cfg.T, cfg.k, aux_partials=r["aux_partials"])
+        evs[6].record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            for j, n in enumerate(names):
+                acc[n] += evs[j].elapsed_time(evs[j + 1])
+    return {n: v / steps for n, v in acc.items()}
+
+
+def run_e2e(moe, torch, layer, x_host_np, cfg, dev, steps):
+    """Same metric with host buffers: pinned H2D of x, forward, D2H of y inside the timed region."""
+    if x_host_np.dtype == np.uint16:
+        xh = torch.from_numpy(x_host_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    else:
+        xh = torch.from_numpy(x_host_np).pin_memory()
+    xd = torch.empty_like(xh, device=dev)
+    yd = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
+    yh = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    total = 0.0
+    for i in range(steps + 3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        xd.copy_(xh, non_blocking=True)
+        layer(xd, y=yd)
+        yh.copy_(yd, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            total += a.elapsed_time(b)
+    ms = total / steps
+    return {"value": cfg.T / (ms / 1e3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
+            "d2h_bytes_per_step": int(yh.numel() * yh.element_size())}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+
+def _oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:  # noqa: BLE001
+        return os.cpu_count() or 1
+
+
+def _oracle_step(oracle, cfg, x64, wg64, experts, tokens):
+    xs = x64[tokens]
+    if cfg.routing == "expert_choice":
+        # expert choice needs every token's logits; the experts run on this sample's picks
+        s = oracle.router_logits(x64, wg64, cfg_bias(cfg))
+        C, idx, sc, pos = oracle.expert_choice_route(s, cfg.capacity_factor)
+        keep = np.isin(idx, tokens)
+        for e in range(cfg.E):
+            rows = idx[e][keep[e]]
+            if rows.size:
+                oracle.swiglu_expert(x64[rows], *experts[e])
+        return
+    s = oracle.router_logits(xs, wg64, cfg_bias(cfg))
+    idx, w, g = oracle.topk_route(s, cfg.k)
+    oracle.aux_stats(g, idx, cfg.E)
+    oracle.dispatch(idx, cfg.E)
+    oracle.moe_forward(xs, idx, w, experts)
+
+
+def cfg_bias(cfg):
+    return synth.router_bias(cfg)
+
+
+class _Pre:
+    """fp64 copies of the stored weights (input preparation, outside the timing)."""
+
+    def __init__(self, inp):
+        self.items = [tuple(synth.to_f64(w[e]) for w in (inp.w_gate, inp.w_up, inp.w_down))
+                      for e in range(inp.cfg.E)]
+
+    def __len__(self):
+        return len(self.items)
+
+    def __getitem__(self, e):
+        return self.items[e]
+
+
+def cpu_baseline(cfg, seconds: float, sample_tokens: int = 256):
+    import oracle
+
+    inp = synth.make_inputs(cfg)
+    x64, wg64 = synth.to_f64(inp.x), synth.to_f64(inp.w_g)
+    experts = _Pre(inp)
+    rng = np.random.default_rng(7)
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        tokens = np.sort(rng.choice(cfg.T, size=min(sample_tokens, cfg.T), replace=False))
+        _oracle_step(oracle, cfg, x64, wg64, experts, tokens)
+        done += tokens.size
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": UNIT, "cores": _oracle_threads(), "kind": "oracle",
+            "sample": f"{done} tokens of {cfg.name} in chunks of {sample_tokens} (routing, aux, "
+                      f"dispatch and fp64 SwiGLU experts per chunk), {dt:.1f} s"}
+
+
+def run_reference(args, cfg):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+
+    inp = synth.make_inputs(cfg)
+    x64, wg64 = synth.to_f64(inp.x), synth.to_f64(inp.w_g)
+    experts = _Pre(inp)
+    rng = np.random.default_rng(11)
+    per_step = 128
+    for _ in range(args.warmup):
+        _oracle_step(oracle, cfg, x64, wg64, experts, np.sort(rng.choice(cfg.T, per_step, replace=False)))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(oracle, cfg, x64, wg64, experts, np.sort(rng.choice(cfg.T, per_step, replace=False)))
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    cores = _oracle_threads()
+    sample = f"{per_step} random tokens of {cfg.name} per step"
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(cfg), "T_per_gpu": cfg.T}, "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    cfg = workload_config(args)
+    line = run_reference(args, cfg) if args.impl == "reference" else run_gpu(args, cfg)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

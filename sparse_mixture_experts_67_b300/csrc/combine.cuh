@@ -1,0 +1,138 @@
+// Weighted combine and load-balancing statistics.
+//
+// Combine: y_t = sum_j w[t,j] * E_{idx[t,j]}(x_t), the accumulation of
+// MoELayer.forward in "Mixture of Experts（MoE）の理論と実装" and of
+// MoELayerWithAuxLoss.forward in "Sparse Mixture of Experts(MoE) 아키텍처 심층
+// 분석".  One warp per token, float4 columns, slots summed in order j = 0..k-1
+// (deterministic).  Expert choice sums the experts that picked the token in
+// ascending expert order, weighted by the raw dispatch-mask score.
+//
+// Aux: f_e = count_e / T, p_e = mean_t g[t,e], loss = E * sum_e f_e p_e, the
+// load_balancing_loss of the first page.  p is reduced from per-block partial
+// sums in a fixed order, so the result does not depend on scheduling.
+#pragma once
+
+#include "common.cuh"
+#include "router.cuh"
+
+namespace moe {
+
+constexpr int kCombineThreads = 256;
+
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const float4* __restrict__ y_perm, const int32_t* __restrict__ inv_perm,
+                   const float* __restrict__ w, int T, int d4, int k, float4* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (kCombineThreads / 32);
+  for (int t = blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5); t < T; t += warps) {
+    for (int c0 = 0; c0 < d4; c0 += 32 * 8) {
+      float4 acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < k; ++j) {
+        const int row = inv_perm[(size_t)t * k + j];
+        const float wj = w[(size_t)t * k + j];
+        const float4* src = y_perm + (size_t)row * d4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + lane + 32 * i;
+          if (c < d4) {
+            const float4 v = __ldg(src + c);
+            acc[i].x = fmaf(wj, v.x, acc[i].x);
+            acc[i].y = fmaf(wj, v.y, acc[i].y);
+            acc[i].z = fmaf(wj, v.z, acc[i].z);
+            acc[i].w = fmaf(wj, v.w, acc[i].w);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < d4) y[(size_t)t * d4 + c] = acc[i];
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kCombineThreads)
+    ec_combine_kernel(const float4* __restrict__ y_perm, const int32_t* __restrict__ pos,
+                      const float* __restrict__ score, int T, int d4, int E,
+                      float4* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (kCombineThreads / 32);
+  for (int t = blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5); t < T; t += warps) {
+    for (int c0 = 0; c0 < d4; c0 += 32 * 8) {
+      float4 acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const int p = (e < E) ? pos[(size_t)e * T + t] : -1;
+        unsigned hit = __ballot_sync(kFullMask, p >= 0);
+        while (hit) {  // ascending expert order
+          const int src_lane = __ffs(hit) - 1;
+          hit &= hit - 1;
+          const int row = __shfl_sync(kFullMask, p, src_lane);
+          const float s = score[row];
+          const float4* src = y_perm + (size_t)row * d4;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c = c0 + lane + 32 * i;
+            if (c < d4) {
+              const float4 v = __ldg(src + c);
+              acc[i].x = fmaf(s, v.x, acc[i].x);
+              acc[i].y = fmaf(s, v.y, acc[i].y);
+              acc[i].z = fmaf(s, v.z, acc[i].z);
+              acc[i].w = fmaf(s, v.w, acc[i].w);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int c = c0 + lane + 32 * i;
+        if (c < d4) y[(size_t)t * d4 + c] = acc[i];
+      }
+    }
+  }
+}
+
+// Per-block partial column sums of probs [T,E] in the router's block layout.
+__global__ void probs_partials_kernel(const float* __restrict__ probs, int T, int E,
+                                      float* __restrict__ partials) {
+  const int t0 = blockIdx.x * kRouterTokens;
+  const int t1 = min(T, t0 + kRouterTokens);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+    for (int t = t0; t < t1; ++t) s += probs[(size_t)t * E + e];
+    partials[(size_t)blockIdx.x * E + e] = s;
+  }
+}
+
+// One CTA of MOE_MAX_EXPERTS threads.
+__global__ void __launch_bounds__(MOE_MAX_EXPERTS)
+    aux_finalize_kernel(const float* __restrict__ partials, int rows, const int32_t* __restrict__ counts,
+                        int T, int E, float* __restrict__ f, float* __restrict__ p,
+                        float* __restrict__ loss) {
+  __shared__ float s[MOE_MAX_EXPERTS];
+  const int e = threadIdx.x;
+  float fp = 0.f;
+  if (e < E) {
+    float acc = 0.f;
+    for (int r = 0; r < rows; ++r) acc += partials[(size_t)r * E + e];
+    const float pe = acc / (float)T;
+    const float fe = (float)counts[e] / (float)T;
+    if (p) p[e] = pe;
+    if (f) f[e] = fe;
+    fp = fe * pe;
+  }
+  s[e] = fp;
+  __syncthreads();
+  for (int off = MOE_MAX_EXPERTS / 2; off > 0; off >>= 1) {
+    if (e < off) s[e] += s[e + off];
+    __syncthreads();
+  }
+  if (e == 0 && loss) *loss = (float)E * s[0];
+}
+
+}  // namespace moe

@@ -1,0 +1,398 @@
+// C ABI of the MoE layer forward: argument checks, workspace carving and the
+// launch sequence.  Every entry point only enqueues on the caller's stream.
+#include <math.h>
+#include <string.h>
+
+#include "combine.cuh"
+#include "common.cuh"
+#include "dispatch.cuh"
+#include "ec_route.cuh"
+#include "grouped_simt.cuh"
+#include "grouped_tc.cuh"
+#include "router.cuh"
+
+using namespace moe;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool valid_dtype(moe_dtype dt) { return dt == MOE_F32 || dt == MOE_BF16; }
+size_t elt_size(moe_dtype dt) { return dt == MOE_BF16 ? 2 : 4; }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Shape rule shared by every call that reads rows of x / weights.
+moe_status check_dims(int d, moe_dtype dt) {
+  if (!valid_dtype(dt)) return MOE_ERR_UNSUPPORTED;
+  if (d <= 0) return MOE_ERR_INVALID_ARG;
+  if (dt == MOE_BF16 && d % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (dt == MOE_F32 && d % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct Carver {
+  char* base;
+  size_t used = 0;
+  template <typename T>
+  T* take(size_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + used) : nullptr;
+    used += align256(count * sizeof(T));
+    return p;
+  }
+  void* take_bytes(size_t bytes) {
+    void* p = base ? base + used : nullptr;
+    used += align256(bytes);
+    return p;
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status moe_device_error(uint32_t* word, int clear) {
+  if (!word) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_error_word, sizeof(uint32_t));
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(uint32_t));
+  }
+  return cuda_status(e);
+}
+
+size_t moe_route_aux_rows(int T) { return T <= 0 ? 0 : (size_t)ceil_div(T, kRouterTokens); }
+
+moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, int d, int E, int k,
+                     moe_dtype dt, int32_t* topk_idx, float* topk_w, float* logits, float* probs,
+                     float* aux_partials, moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_dims(d, dt);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_g || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (dt == MOE_BF16 && (!aligned16(x) || !aligned16(w_g))) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_router(x, w_g, bias, T, d, E, k, dt == MOE_BF16, topk_idx, topk_w,
+                                   logits, probs, aux_partials, (cudaStream_t)stream));
+}
+
+int moe_expert_choice_capacity(int T, int E, float capacity_factor) {
+  if (T < 0 || E < 1 || !(capacity_factor > 0.f)) return -1;
+  return (int)floor((double)T * (double)capacity_factor / (double)E);
+}
+
+moe_status moe_expert_choice_route(const void* x, const void* w_g, const float* bias, int T, int d,
+                                   int E, float capacity_factor, moe_dtype dt, int32_t* ec_idx,
+                                   float* ec_score, int32_t* pos, float* logits,
+                                   moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || !(capacity_factor > 0.f)) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_dims(d, dt);
+  if (st != MOE_OK) return st;
+  const int C = moe_expert_choice_capacity(T, E, capacity_factor);
+  if (C > T) return MOE_ERR_INVALID_ARG;
+  if (T > kEcMaxTokens) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_g || !pos || !logits || (C > 0 && (!ec_idx || !ec_score))) return MOE_ERR_INVALID_ARG;
+  if (dt == MOE_BF16 && (!aligned16(x) || !aligned16(w_g))) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_router(x, w_g, bias, T, d, E, /*k=*/0, dt == MOE_BF16, nullptr, nullptr,
+                                logits, nullptr, nullptr, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const int n2 = next_pow2(T);
+  const size_t sm = (size_t)n2 * sizeof(unsigned long long);
+  e = cudaFuncSetAttribute(ec_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  ec_route_kernel<<<E, kEcThreads, sm, s>>>(logits, T, E, C, n2, ec_idx, ec_score, pos);
+  return cuda_status(cudaGetLastError());
+}
+
+size_t moe_permute_workspace_size(int T, int E, int k) {
+  if (T < 0 || E < 1 || k < 1) return 0;
+  const int tiles = dispatch_tiles((long long)T * k);
+  return 2 * align256((size_t)tiles * E * sizeof(int32_t)) + 256;
+}
+
+moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, int T, int d,
+                           moe_dtype dt, void* x_perm, moe_stream_t stream) {
+  if (R < 0 || div < 1 || T < 0) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_dims(d, dt);
+  if (st != MOE_OK) return st;
+  if (R == 0) return MOE_OK;
+  if (!x || !src || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
+  const int vec = (int)(d * elt_size(dt) / 16);
+  const int grid = min(ceil_div(R, kGatherThreads / 32), 148 * 16);
+  gather_rows_kernel<<<grid, kGatherThreads, 0, (cudaStream_t)stream>>>(
+      static_cast<const uint4*>(x), src, R, div, vec, static_cast<uint4*>(x_perm));
+  return cuda_status(cudaGetLastError());
+}
+
+moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
+                       moe_dtype dt, void* x_perm, int32_t* counts, int32_t* offsets, int32_t* perm,
+                       int32_t* inv_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_dims(d, dt);
+  if (st != MOE_OK) return st;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const long long A = (long long)T * k;
+  if (A > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) {  // empty: counts = 0, offsets = 0
+    cudaError_t e = cudaMemsetAsync(counts, 0, E * sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, (E + 1) * sizeof(int32_t), s);
+    return cuda_status(e);
+  }
+  if (!x || !topk_idx || !x_perm || !perm || !inv_perm) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < moe_permute_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
+  const int tiles = dispatch_tiles(A);
+  Carver cv{static_cast<char*>(ws)};
+  cv.used = (256 - (reinterpret_cast<uintptr_t>(ws) & 255)) & 255;
+  int32_t* tile_counts = cv.take<int32_t>((size_t)tiles * E);
+  int32_t* tile_base = cv.take<int32_t>((size_t)tiles * E);
+  dispatch_hist_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile_counts);
+  dispatch_scan_kernel<<<1, MOE_MAX_EXPERTS, 0, s>>>(tile_counts, tiles, E, (int)A, tile_base,
+                                                     counts, offsets);
+  dispatch_scatter_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile_base, perm,
+                                                             inv_perm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return moe_gather_rows(x, perm, (int)A, k, T, d, dt, x_perm, stream);
+}
+
+static moe_status check_experts(int R, int d, int F, int E, moe_dtype dt) {
+  if (R < 0 || E < 1 || E > MOE_MAX_EXPERTS || F <= 0) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_dims(d, dt);
+  if (st != MOE_OK) return st;
+  return check_dims(F, dt);
+}
+
+moe_status moe_grouped_gateup_swiglu(const void* x_perm, const int32_t* offsets, const void* w_gate,
+                                     const void* w_up, int R, int d, int F, int E, moe_dtype dt,
+                                     void* h, moe_stream_t stream) {
+  moe_status st = check_experts(R, d, F, E, dt);
+  if (st != MOE_OK) return st;
+  if (R == 0) return MOE_OK;
+  if (!x_perm || !offsets || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(h))
+    return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (dt == MOE_BF16)
+    return cuda_status(launch_gateup_tc(static_cast<const __nv_bfloat16*>(x_perm), offsets,
+                                        static_cast<const __nv_bfloat16*>(w_gate),
+                                        static_cast<const __nv_bfloat16*>(w_up), R, d, F, E,
+                                        static_cast<__nv_bfloat16*>(h), s));
+  return cuda_status(launch_grouped_simt<float, true>(
+      static_cast<const float*>(x_perm), offsets, static_cast<const float*>(w_gate),
+      static_cast<const float*>(w_up), R, F, d, E, h, s));
+}
+
+moe_status moe_grouped_down(const void* h, const int32_t* offsets, const void* w_down, int R, int d,
+                            int F, int E, moe_dtype dt, float* y_perm, moe_stream_t stream) {
+  moe_status st = check_experts(R, d, F, E, dt);
+  if (st != MOE_OK) return st;
+  if (R == 0) return MOE_OK;
+  if (!h || !offsets || !w_down || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w_down) || !aligned16(y_perm)) return MOE_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (dt == MOE_BF16)
+    return cuda_status(launch_down_tc(static_cast<const __nv_bfloat16*>(h), offsets,
+                                      static_cast<const __nv_bfloat16*>(w_down), R, d, F, E,
+                                      y_perm, s));
+  return cuda_status(launch_grouped_simt<float, false>(static_cast<const float*>(h), offsets,
+                                                       static_cast<const float*>(w_down), nullptr,
+                                                       R, d, F, E, y_perm, s));
+}
+
+moe_status moe_experts_swiglu(const void* x_perm, const int32_t* offsets, const void* w_gate,
+                              const void* w_up, const void* w_down, int R, int d, int F, int E,
+                              moe_dtype dt, void* h, float* y_perm, moe_stream_t stream) {
+  moe_status st = moe_grouped_gateup_swiglu(x_perm, offsets, w_gate, w_up, R, d, F, E, dt, h, stream);
+  if (st != MOE_OK) return st;
+  return moe_grouped_down(h, offsets, w_down, R, d, F, E, dt, y_perm, stream);
+}
+
+moe_status moe_combine(const float* y_perm, const int32_t* inv_perm, const float* topk_w, int T,
+                       int d, int k, float* y, moe_stream_t stream) {
+  if (T < 0 || k < 1 || d <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !inv_perm || !topk_w || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
+  const int grid = min(ceil_div(T, kCombineThreads / 32), 148 * 8);
+  combine_kernel<<<grid, kCombineThreads, 0, (cudaStream_t)stream>>>(
+      reinterpret_cast<const float4*>(y_perm), inv_perm, topk_w, T, d / 4, k,
+      reinterpret_cast<float4*>(y));
+  return cuda_status(cudaGetLastError());
+}
+
+moe_status moe_ec_combine(const float* y_perm, const int32_t* pos, const float* ec_score, int T,
+                          int d, int E, int C, float* y, moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || C < 0 || C > T || d <= 0) return MOE_ERR_INVALID_ARG;
+  if (d % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!pos || !y || (C > 0 && (!y_perm || !ec_score))) return MOE_ERR_INVALID_ARG;
+  if ((y_perm && !aligned16(y_perm)) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
+  const int grid = min(ceil_div(T, kCombineThreads / 32), 148 * 8);
+  ec_combine_kernel<<<grid, kCombineThreads, 0, (cudaStream_t)stream>>>(
+      reinterpret_cast<const float4*>(y_perm), pos, ec_score, T, d / 4, E,
+      reinterpret_cast<float4*>(y));
+  return cuda_status(cudaGetLastError());
+}
+
+moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int32_t* counts, int T,
+                        int E, int k, float* f, float* p, float* loss, moe_stream_t stream) {
+  if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!counts || (!probs && !aux_partials)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int rows = (int)moe_route_aux_rows(T);
+  if (probs) {
+    // probs given: rebuild the per-block partial sums in place of the router's
+    if (!aux_partials) return MOE_ERR_INVALID_ARG;
+    probs_partials_kernel<<<rows, 256, 0, s>>>(probs, T, E, const_cast<float*>(aux_partials));
+  }
+  aux_finalize_kernel<<<1, MOE_MAX_EXPERTS, 0, s>>>(aux_partials, rows, counts, T, E, f, p, loss);
+  return cuda_status(cudaGetLastError());
+}
+
+size_t moe_layer_workspace_size(const moe_layer_desc* desc) {
+  if (!desc) return 0;
+  const moe_layer_desc& D = *desc;
+  if (D.T < 0 || D.E < 1 || D.E > MOE_MAX_EXPERTS || D.d <= 0 || D.F <= 0 || !valid_dtype(D.dtype))
+    return 0;
+  Carver cv{nullptr};
+  const size_t es = elt_size(D.dtype);
+  if (D.routing == MOE_ROUTING_EXPERT_CHOICE) {
+    const int C = moe_expert_choice_capacity(D.T, D.E, D.capacity_factor);
+    if (C < 0) return 0;
+    const size_t R = (size_t)D.E * C;
+    cv.take<float>((size_t)D.T * D.E);  // logits
+    cv.take<int32_t>(R);                // ec_idx
+    cv.take<float>(R);                  // ec_score
+    cv.take<int32_t>((size_t)D.E * D.T);  // pos
+    cv.take<int32_t>(D.E + 1);          // offsets
+    cv.take_bytes(R * D.d * es);        // x_perm
+    cv.take_bytes(R * D.F * es);        // h
+    cv.take<float>(R * D.d);            // y_perm
+  } else {
+    if (D.k < 1 || D.k > D.E) return 0;
+    const size_t A = (size_t)D.T * D.k;
+    cv.take<int32_t>(A);                                   // topk_idx
+    cv.take<float>(A);                                     // topk_w
+    cv.take<float>(moe_route_aux_rows(D.T) * D.E);          // aux partials
+    cv.take<int32_t>(D.E);                                 // counts
+    cv.take<int32_t>(D.E + 1);                             // offsets
+    cv.take<float>(2 * D.E + 1);                           // f, p, loss
+    cv.take_bytes(moe_permute_workspace_size(D.T, D.E, D.k));
+    cv.take<int32_t>(A);                                   // perm
+    cv.take<int32_t>(A);                                   // inv_perm
+    cv.take_bytes(A * D.d * es);                           // x_perm
+    cv.take_bytes(A * D.F * es);                           // h
+    cv.take<float>(A * D.d);                               // y_perm
+  }
+  return cv.used + 256;
+}
+
+moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights* w, const void* x,
+                             float* y, const moe_layer_outputs* out, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+  if (!desc || !w) return MOE_ERR_INVALID_ARG;
+  const moe_layer_desc& D = *desc;
+  const bool ec = D.routing == MOE_ROUTING_EXPERT_CHOICE;
+  if (D.routing != MOE_ROUTING_TOPK && !ec) return MOE_ERR_INVALID_ARG;
+  if (D.T < 0 || D.E < 1 || D.E > MOE_MAX_EXPERTS || D.F <= 0) return MOE_ERR_INVALID_ARG;
+  if (!ec && (D.k < 1 || D.k > D.E)) return MOE_ERR_INVALID_ARG;
+  if (ec && !(D.capacity_factor > 0.f)) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_experts(0, D.d, D.F, D.E, D.dtype);
+  if (st != MOE_OK) return st;
+  if (D.T == 0) return MOE_OK;
+  if (!x || !y || !w->w_g || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_layer_workspace_size(desc);
+  if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  moe_layer_outputs none;
+  memset(&none, 0, sizeof(none));
+  const moe_layer_outputs& O = out ? *out : none;
+  Carver cv{static_cast<char*>(ws)};
+  cv.used = (256 - (reinterpret_cast<uintptr_t>(ws) & 255)) & 255;
+  const size_t es = elt_size(D.dtype);
+  cudaStream_t s = (cudaStream_t)stream;
+
+  if (ec) {
+    const int C = moe_expert_choice_capacity(D.T, D.E, D.capacity_factor);
+    const size_t R = (size_t)D.E * C;
+    float* logits = cv.take<float>((size_t)D.T * D.E);
+    int32_t* ec_idx = cv.take<int32_t>(R);
+    float* ec_score = cv.take<float>(R);
+    int32_t* pos = cv.take<int32_t>((size_t)D.E * D.T);
+    int32_t* offsets = cv.take<int32_t>(D.E + 1);
+    void* x_perm = cv.take_bytes(R * D.d * es);
+    void* h = cv.take_bytes(R * D.F * es);
+    float* y_perm = cv.take<float>(R * D.d);
+    if (O.logits) logits = O.logits;
+    if (O.ec_idx) ec_idx = O.ec_idx;
+    if (O.ec_score) ec_score = O.ec_score;
+    if (O.pos) pos = O.pos;
+    st = moe_expert_choice_route(x, w->w_g, w->bias, D.T, D.d, D.E, D.capacity_factor, D.dtype,
+                                 ec_idx, ec_score, pos, logits, stream);
+    if (st != MOE_OK) return st;
+    if (R > 0) {
+      // expert e owns dispatch rows [e*C, (e+1)*C)
+      uniform_offsets_kernel<<<1, MOE_MAX_EXPERTS + 1, 0, s>>>(offsets, D.E, C);
+      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+      st = moe_gather_rows(x, ec_idx, (int)R, 1, D.T, D.d, D.dtype, x_perm, stream);
+      if (st != MOE_OK) return st;
+      st = moe_experts_swiglu(x_perm, offsets, w->w_gate, w->w_up, w->w_down, (int)R, D.d, D.F,
+                              D.E, D.dtype, h, y_perm, stream);
+      if (st != MOE_OK) return st;
+    }
+    return moe_ec_combine(y_perm, pos, ec_score, D.T, D.d, D.E, C, y, stream);
+  }
+
+  const int k = D.k;
+  const size_t A = (size_t)D.T * k;
+  int32_t* idx = cv.take<int32_t>(A);
+  float* tw = cv.take<float>(A);
+  float* aux = cv.take<float>(moe_route_aux_rows(D.T) * D.E);
+  int32_t* counts = cv.take<int32_t>(D.E);
+  int32_t* offsets = cv.take<int32_t>(D.E + 1);
+  float* fpl = cv.take<float>(2 * D.E + 1);
+  const size_t pws = moe_permute_workspace_size(D.T, D.E, k);
+  void* pw = cv.take_bytes(pws);
+  int32_t* perm = cv.take<int32_t>(A);
+  int32_t* inv_perm = cv.take<int32_t>(A);
+  void* x_perm = cv.take_bytes(A * D.d * es);
+  void* h = cv.take_bytes(A * D.F * es);
+  float* y_perm = cv.take<float>(A * D.d);
+  if (O.topk_idx) idx = O.topk_idx;
+  if (O.topk_w) tw = O.topk_w;
+  if (O.counts) counts = O.counts;
+  if (O.offsets) offsets = O.offsets;
+  st = moe_route(x, w->w_g, w->bias, D.T, D.d, D.E, k, D.dtype, idx, tw, O.logits, nullptr, aux,
+                 stream);
+  if (st != MOE_OK) return st;
+  st = moe_permute(x, idx, D.T, D.d, D.E, k, D.dtype, x_perm, counts, offsets, perm, inv_perm, pw,
+                   pws, stream);
+  if (st != MOE_OK) return st;
+  st = moe_experts_swiglu(x_perm, offsets, w->w_gate, w->w_up, w->w_down, (int)A, D.d, D.F, D.E,
+                          D.dtype, h, y_perm, stream);
+  if (st != MOE_OK) return st;
+  st = moe_combine(y_perm, inv_perm, tw, D.T, D.d, k, y, stream);
+  if (st != MOE_OK) return st;
+  return moe_aux_loss(nullptr, aux, counts, D.T, D.E, k, O.f ? O.f : fpl, O.p ? O.p : fpl + D.E,
+                      O.loss ? O.loss : fpl + 2 * D.E, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,369 @@
+// Fused router: logits GEMM + softmax + top-k + renormalise + aux partial sums.
+//
+// Follows MoELayer.route of "Mixture of Experts（MoE）の理論と実装"
+// (disassemble-channel.com) and TopKGating of "Sparse Mixture of Experts(MoE)
+// 아키텍처 심층 분석" (youngju.dev): s = x W_g^T (+ b), g = softmax(s), the k
+// largest entries, weights renormalised over the selection.
+//
+// One CTA owns 64 tokens (4 warps x 16).  The logits GEMM is narrow (N = E
+// <= 256), so bf16 runs on warp-level mma.sync m16n8k16 tiles fed by cp.async
+// through a 3-stage shared-memory ring; fp32 runs on FFMA.  The 64 x E logits
+// tile then goes through shared memory to a warp-per-token epilogue where the
+// lanes hold the experts: max / sum / arg-max are warp butterflies.
+#pragma once
+
+#include <float.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kRouterTokens = 64;
+constexpr int kRouterThreads = 128;
+constexpr int kRouterBK = 64;
+constexpr int kRouterStages = 3;
+constexpr int kRouterLd = kRouterBK + 8;  // bf16 elements per smem row (pad: conflict-free)
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  int src_bytes = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Warp-per-token epilogue over the logits tile S[64][ldS] (bias not yet added).
+// k == 0 writes logits only (expert-choice pre-pass).
+template <int NT>
+__device__ void router_epilogue(const float* S, int ldS, int tok0, int T, int E, int k,
+                                const float* __restrict__ bias, int32_t* __restrict__ idx_out,
+                                float* __restrict__ w_out, float* __restrict__ logits_out,
+                                float* __restrict__ probs_out, float* __restrict__ aux_row,
+                                float* s_aux, int* s_sel_e, float* s_sel_g) {
+  constexpr int EPL = (8 * NT + 31) / 32;  // experts per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float psum[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) psum[i] = 0.f;
+
+  for (int r = 0; r < 16; ++r) {
+    const int tl = warp * 16 + r;
+    const int t = tok0 + tl;
+    if (t >= T) break;  // warp-uniform
+    float v[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? S[tl * ldS + e] + (bias ? bias[e] : 0.f) : -FLT_MAX;
+    }
+    if (logits_out) {
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) logits_out[(size_t)t * E + e] = v[i];
+      }
+    }
+    if (k == 0) continue;
+    float m = v[0];
+#pragma unroll
+    for (int i = 1; i < EPL; ++i) m = fmaxf(m, v[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, off));
+    float ex[EPL];
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      ex[i] = (e < E) ? expf(v[i] - m) : 0.f;
+      sum += ex[i];
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFullMask, sum, off);
+    const float inv = 1.0f / sum;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      const float g = ex[i] * inv;
+      if (e < E) {
+        psum[i] += g;
+        if (probs_out) probs_out[(size_t)t * E + e] = g;
+      }
+    }
+    // top-k by repeated warp arg-max on the logits: larger value, then lower index
+    unsigned taken = 0;
+    float selsum = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float best = 0.f;
+      int bi = -1;
+#pragma unroll
+      for (int i = 0; i < EPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (bi < 0 || v[i] > best)) {
+          best = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFullMask, best, off);
+        const int oi = __shfl_xor_sync(kFullMask, bi, off);
+        if (oi >= 0 && (bi < 0 || ov > best || (ov == best && oi < bi))) {
+          best = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      const float gsel = expf(best - m) * inv;  // same arithmetic as the owner's g
+      selsum += gsel;
+      if (lane == 0) {
+        s_sel_e[warp * MOE_MAX_EXPERTS + j] = bi;
+        s_sel_g[warp * MOE_MAX_EXPERTS + j] = gsel;
+      }
+    }
+    __syncwarp();
+    const float rs = 1.0f / selsum;
+    for (int j = lane; j < k; j += 32) {
+      idx_out[(size_t)t * k + j] = s_sel_e[warp * MOE_MAX_EXPERTS + j];
+      w_out[(size_t)t * k + j] = s_sel_g[warp * MOE_MAX_EXPERTS + j] * rs;
+    }
+    __syncwarp();
+  }
+  if (aux_row != nullptr) {
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) s_aux[warp * MOE_MAX_EXPERTS + e] = psum[i];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+      aux_row[e] = ((s_aux[e] + s_aux[MOE_MAX_EXPERTS + e]) + s_aux[2 * MOE_MAX_EXPERTS + e]) +
+                   s_aux[3 * MOE_MAX_EXPERTS + e];
+  }
+}
+
+// Shared memory: max(stage ring, logits tile) + epilogue scratch.
+template <int NT>
+constexpr size_t router_smem_bytes_bf16() {
+  constexpr size_t ring = (size_t)kRouterStages * (kRouterTokens + 8 * NT) * kRouterLd * 2;
+  constexpr size_t tile = (size_t)kRouterTokens * (8 * NT + 1) * 4;
+  constexpr size_t main = ring > tile ? ring : tile;
+  return main + 4 * MOE_MAX_EXPERTS * (4 + 4 + 4);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kRouterThreads)
+    router_bf16_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg,
+                       const float* __restrict__ bias, int T, int d, int E, int k,
+                       int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                       float* __restrict__ logits_out, float* __restrict__ probs_out,
+                       float* __restrict__ aux_partials) {
+  constexpr int EP = 8 * NT;
+  extern __shared__ __align__(16) unsigned char smem[];
+  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
+  constexpr int stage_elems = (kRouterTokens + EP) * kRouterLd;
+  constexpr size_t ring_bytes = (size_t)kRouterStages * stage_elems * 2;
+  constexpr size_t tile_bytes = (size_t)kRouterTokens * (EP + 1) * 4;
+  constexpr size_t main_bytes = ring_bytes > tile_bytes ? ring_bytes : tile_bytes;
+  float* s_aux = reinterpret_cast<float*>(smem + main_bytes);
+  int* s_sel_e = reinterpret_cast<int*>(s_aux + 4 * MOE_MAX_EXPERTS);
+  float* s_sel_g = reinterpret_cast<float*>(s_sel_e + 4 * MOE_MAX_EXPERTS);
+
+  const int tok0 = blockIdx.x * kRouterTokens;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nk = d / kRouterBK;
+
+  auto load_stage = [&](int stage, int kc) {
+    __nv_bfloat16* xs = ring + stage * stage_elems;
+    __nv_bfloat16* ws = xs + kRouterTokens * kRouterLd;
+    const int kof = kc * kRouterBK;
+    for (int c = threadIdx.x; c < kRouterTokens * 8; c += kRouterThreads) {
+      const int r = c >> 3, ch = c & 7;
+      const int t = tok0 + r;
+      const bool ok = t < T;
+      const __nv_bfloat16* src = x + (size_t)(ok ? t : 0) * d + kof + ch * 8;
+      cp_async16(xs + r * kRouterLd + ch * 8, src, ok);
+    }
+    for (int c = threadIdx.x; c < EP * 8; c += kRouterThreads) {
+      const int r = c >> 3, ch = c & 7;
+      const bool ok = r < E;
+      const __nv_bfloat16* src = wg + (size_t)(ok ? r : 0) * d + kof + ch * 8;
+      cp_async16(ws + r * kRouterLd + ch * 8, src, ok);
+    }
+  };
+
+  float acc[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < kRouterStages - 1; ++s) {
+    if (s < nk) load_stage(s, s);
+    cp_async_commit();
+  }
+  const int g = lane >> 2, c4 = lane & 3;
+  for (int kc = 0; kc < nk; ++kc) {
+    cp_async_wait<kRouterStages - 2>();
+    __syncthreads();
+    {
+      const int nxt = kc + kRouterStages - 1;
+      if (nxt < nk) load_stage(nxt % kRouterStages, nxt);
+      cp_async_commit();
+    }
+    const __nv_bfloat16* xs = ring + (kc % kRouterStages) * stage_elems;
+    const __nv_bfloat16* ws = xs + kRouterTokens * kRouterLd;
+    const __nv_bfloat16* xw = xs + warp * 16 * kRouterLd;
+#pragma unroll
+    for (int kk = 0; kk < kRouterBK; kk += 16) {
+      uint32_t a[4];
+      a[0] = *reinterpret_cast<const uint32_t*>(xw + g * kRouterLd + kk + 2 * c4);
+      a[1] = *reinterpret_cast<const uint32_t*>(xw + (g + 8) * kRouterLd + kk + 2 * c4);
+      a[2] = *reinterpret_cast<const uint32_t*>(xw + g * kRouterLd + kk + 8 + 2 * c4);
+      a[3] = *reinterpret_cast<const uint32_t*>(xw + (g + 8) * kRouterLd + kk + 8 + 2 * c4);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        uint32_t b[2];
+        const __nv_bfloat16* wr = ws + (n * 8 + g) * kRouterLd + kk + 2 * c4;
+        b[0] = *reinterpret_cast<const uint32_t*>(wr);
+        b[1] = *reinterpret_cast<const uint32_t*>(wr + 8);
+        mma_bf16_16816(acc[n], a, b);
+      }
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // ring no longer read: the logits tile may alias it
+
+  float* S = reinterpret_cast<float*>(smem);
+  constexpr int ldS = EP + 1;
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int col = n * 8 + 2 * c4;
+    const int r0 = warp * 16 + g;
+    S[r0 * ldS + col] = acc[n][0];
+    S[r0 * ldS + col + 1] = acc[n][1];
+    S[(r0 + 8) * ldS + col] = acc[n][2];
+    S[(r0 + 8) * ldS + col + 1] = acc[n][3];
+  }
+  __syncthreads();
+  router_epilogue<NT>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
+                      aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, s_aux,
+                      s_sel_e, s_sel_g);
+}
+
+// fp32 router: FFMA over 32-wide d chunks, same epilogue.
+constexpr int kRouterBKf = 32;
+template <int NT>
+constexpr size_t router_smem_bytes_f32() {
+  constexpr size_t ld = kRouterBKf + 1;
+  constexpr size_t tiles = (size_t)(kRouterTokens + 8 * NT) * ld * 4;
+  constexpr size_t acc = (size_t)kRouterTokens * (8 * NT + 1) * 4;
+  return tiles + acc + 4 * MOE_MAX_EXPERTS * 12;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kRouterThreads)
+    router_f32_kernel(const float* __restrict__ x, const float* __restrict__ wg,
+                      const float* __restrict__ bias, int T, int d, int E, int k,
+                      int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                      float* __restrict__ logits_out, float* __restrict__ probs_out,
+                      float* __restrict__ aux_partials) {
+  constexpr int EP = 8 * NT;
+  constexpr int ld = kRouterBKf + 1;
+  constexpr int ldS = EP + 1;
+  extern __shared__ __align__(16) unsigned char smem[];
+  float* xs = reinterpret_cast<float*>(smem);
+  float* ws = xs + kRouterTokens * ld;
+  float* S = ws + EP * ld;
+  float* s_aux = S + kRouterTokens * ldS;
+  int* s_sel_e = reinterpret_cast<int*>(s_aux + 4 * MOE_MAX_EXPERTS);
+  float* s_sel_g = reinterpret_cast<float*>(s_sel_e + 4 * MOE_MAX_EXPERTS);
+  const int tok0 = blockIdx.x * kRouterTokens;
+  // thread -> (token, expert parity): token = tid % 64, experts tid/64 + 2*i
+  const int tt = threadIdx.x & 63, eh = threadIdx.x >> 6;
+  float acc[4 * NT];
+#pragma unroll
+  for (int i = 0; i < 4 * NT; ++i) acc[i] = 0.f;
+  for (int kof = 0; kof < d; kof += kRouterBKf) {
+    __syncthreads();
+    for (int c = threadIdx.x; c < kRouterTokens * kRouterBKf; c += kRouterThreads) {
+      const int r = c / kRouterBKf, cc = c % kRouterBKf;
+      const int t = tok0 + r;
+      xs[r * ld + cc] = (t < T && kof + cc < d) ? x[(size_t)t * d + kof + cc] : 0.f;
+    }
+    for (int c = threadIdx.x; c < EP * kRouterBKf; c += kRouterThreads) {
+      const int r = c / kRouterBKf, cc = c % kRouterBKf;
+      ws[r * ld + cc] = (r < E && kof + cc < d) ? wg[(size_t)r * d + kof + cc] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < kRouterBKf; ++kk) {
+      const float xv = xs[tt * ld + kk];
+#pragma unroll
+      for (int i = 0; i < 4 * NT; ++i) acc[i] = fmaf(xv, ws[(eh + 2 * i) * ld + kk], acc[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4 * NT; ++i) S[tt * ldS + eh + 2 * i] = acc[i];
+  __syncthreads();
+  router_epilogue<NT>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
+                      aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, s_aux,
+                      s_sel_e, s_sel_g);
+}
+
+inline int router_nt(int E) {
+  int ep = 8;
+  while (ep < E) ep <<= 1;
+  return ep / 8;
+}
+
+template <int NT>
+cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, int T, int d, int E,
+                             int k, bool bf16, int32_t* idx, float* w, float* logits, float* probs,
+                             float* aux, cudaStream_t st) {
+  const int grid = ceil_div(T, kRouterTokens);
+  if (bf16) {
+    const size_t sm = router_smem_bytes_bf16<NT>();
+    cudaError_t e = cudaFuncSetAttribute(router_bf16_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    router_bf16_kernel<NT><<<grid, kRouterThreads, sm, st>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wg), bias, T, d,
+        E, k, idx, w, logits, probs, aux);
+  } else {
+    const size_t sm = router_smem_bytes_f32<NT>();
+    cudaError_t e = cudaFuncSetAttribute(router_f32_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    router_f32_kernel<NT><<<grid, kRouterThreads, sm, st>>>(
+        static_cast<const float*>(x), static_cast<const float*>(wg), bias, T, d, E, k, idx, w,
+        logits, probs, aux);
+  }
+  return cudaGetLastError();
+}
+
+inline cudaError_t launch_router(const void* x, const void* wg, const float* bias, int T, int d,
+                                 int E, int k, bool bf16, int32_t* idx, float* w, float* logits,
+                                 float* probs, float* aux, cudaStream_t st) {
+  switch (router_nt(E)) {
+    case 1: return launch_router_nt<1>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
+    case 2: return launch_router_nt<2>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
+    case 4: return launch_router_nt<4>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
+    case 8: return launch_router_nt<8>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
+    case 16: return launch_router_nt<16>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
+    default: return launch_router_nt<32>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the device."""
+
+import ctypes
+
+import pytest
+
+import sparse_mixture_experts_67_b300 as moe
+from sparse_mixture_experts_67_b300 import build_lib
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return moe.lib()
+
+
+def test_header_symbols_exported(L):
+    declared = moe.declared_symbols()
+    assert "moe_layer_forward" in declared and len(declared) >= 15
+    for name in declared:
+        assert hasattr(L, name), f"{name} declared in include/moe.h but not exported"
+
+
+def test_status_strings(L):
+    for code, name in enumerate(["MOE_OK", "MOE_ERR_INVALID_ARG", "MOE_ERR_UNSUPPORTED",
+                                 "MOE_ERR_WORKSPACE", "MOE_ERR_CUDA"]):
+        assert L.moe_status_string(code).decode() == name
+
+
+def test_capacity_rule(L):
+    assert L.moe_expert_choice_capacity(8192, 16, 2.0) == 1024
+    assert L.moe_expert_choice_capacity(4, 2, 1.0) == 2
+    assert L.moe_expert_choice_capacity(10, 4, 0.3) == 0
+    assert L.moe_expert_choice_capacity(10, 3, 1.0) == 3
+    assert L.moe_expert_choice_capacity(10, 4, 0.0) == -1
+
+
+def test_aux_rows(L):
+    assert L.moe_route_aux_rows(0) == 0
+    assert L.moe_route_aux_rows(1) == 1
+    assert L.moe_route_aux_rows(64) == 1
+    assert L.moe_route_aux_rows(65) == 2
+
+
+def _nullp():
+    return ctypes.c_void_p(0)
+
+
+def _p(v=4096):
+    return ctypes.c_void_p(v)
+
+
+def test_route_argument_errors(L):
+    z = _nullp()
+    # k > E, E > 256, k < 1, negative T: invalid before any device work
+    assert L.moe_route(_p(), _p(), z, 8, 64, 4, 5, 1, _p(), _p(), z, z, z, z) == 1
+    assert L.moe_route(_p(), _p(), z, 8, 64, 300, 2, 1, _p(), _p(), z, z, z, z) == 1
+    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 0, 1, _p(), _p(), z, z, z, z) == 1
+    assert L.moe_route(_p(), _p(), z, -1, 64, 8, 2, 1, _p(), _p(), z, z, z, z) == 1
+    # null required pointers
+    assert L.moe_route(z, _p(), z, 8, 64, 8, 2, 1, _p(), _p(), z, z, z, z) == 1
+    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 2, 1, z, _p(), z, z, z, z) == 1
+    # bf16 with d not a multiple of 64, unknown dtype, misaligned bf16 pointer
+    assert L.moe_route(_p(), _p(), z, 8, 96, 8, 2, 1, _p(), _p(), z, z, z, z) == 2
+    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 2, 7, _p(), _p(), z, z, z, z) == 2
+    assert L.moe_route(_p(4098), _p(), z, 8, 64, 8, 2, 1, _p(), _p(), z, z, z, z) == 2
+    # T == 0 is a no-op
+    assert L.moe_route(z, z, z, 0, 64, 8, 2, 1, z, z, z, z, z, z) == 0
+
+
+def test_expert_choice_argument_errors(L):
+    z = _nullp()
+    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 4, 0.0, 1, _p(), _p(), _p(), _p(), z) == 1
+    # capacity above T
+    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 2, 4.0, 1, _p(), _p(), _p(), _p(), z) == 1
+    # beyond the shared-memory sort
+    assert L.moe_expert_choice_route(_p(), _p(), z, 20000, 64, 16, 1.0, 1, _p(), _p(), _p(), _p(), z) == 2
+    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 4, 1.0, 1, _p(), _p(), z, _p(), z) == 1
+
+
+def test_permute_and_experts_errors(L):
+    z = _nullp()
+    ws = L.moe_permute_workspace_size(100, 8, 2)
+    assert ws > 0
+    assert L.moe_permute(_p(), _p(), 100, 64, 8, 2, 1, _p(), _p(), _p(), _p(), _p(), _p(), ws - 1, z) == 3
+    assert L.moe_permute(_p(), _p(), 100, 64, 8, 2, 1, _p(), _p(), _p(), _p(), _p(), z, ws, z) == 3
+    assert L.moe_permute(_p(), _p(), 100, 64, 8, 9, 1, _p(), _p(), _p(), _p(), _p(), _p(), ws, z) == 1
+    assert L.moe_grouped_gateup_swiglu(_p(), _p(), _p(), _p(), 10, 64, 100, 8, 1, _p(), z) == 2
+    assert L.moe_grouped_gateup_swiglu(_p(), z, _p(), _p(), 10, 64, 128, 8, 1, _p(), z) == 1
+    assert L.moe_grouped_down(_p(), _p(), _p(), 10, 64, 128, 0, 1, _p(), z) == 1
+    assert L.moe_grouped_down(_p(), _p(), _p(), 0, 64, 128, 8, 1, z, z) == 0
+    assert L.moe_combine(_p(), _p(), _p(), 4, 6, 2, _p(), z) == 2
+    assert L.moe_combine(z, _p(), _p(), 4, 8, 2, _p(), z) == 1
+    assert L.moe_ec_combine(_p(), _p(), _p(), 4, 8, 2, 5, _p(), z) == 1
+    assert L.moe_aux_loss(z, z, _p(), 4, 8, 2, z, z, z, z) == 1
+
+
+def test_layer_workspace_and_errors(L):
+    d = moe._Desc(8192, 1024, 4096, 8, 2, 0, 0.0, 1)
+    ws = L.moe_layer_workspace_size(ctypes.byref(d))
+    A = 8192 * 2
+    # at least x_perm + h (bf16) + y_perm (fp32)
+    assert ws >= A * 1024 * 2 + A * 4096 * 2 + A * 1024 * 4
+    ec = moe._Desc(8192, 1024, 4096, 16, 0, 1, 2.0, 1)
+    R = 16 * 1024
+    assert L.moe_layer_workspace_size(ctypes.byref(ec)) >= R * 1024 * 2 + R * 4096 * 2 + R * 1024 * 4
+    bad = moe._Desc(8192, 1024, 4096, 8, 9, 0, 0.0, 1)
+    assert L.moe_layer_workspace_size(ctypes.byref(bad)) == 0
+    w = moe._Weights(4096, 0, 4096, 4096, 4096)
+    z = _nullp()
+    assert L.moe_layer_forward(ctypes.byref(d), ctypes.byref(w), _p(), _p(), None, _p(), ws - 1, z) == 3
+    assert L.moe_layer_forward(ctypes.byref(bad), ctypes.byref(w), _p(), _p(), None, _p(), ws, z) == 1
+    fp = moe._Desc(16, 64, 102, 8, 2, 0, 0.0, 0)  # fp32 F not a multiple of 4
+    assert L.moe_layer_forward(ctypes.byref(fp), ctypes.byref(w), _p(), _p(), None, _p(), 1 << 30, z) == 2
+
+
+def test_no_cpu_fallback_without_device():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(4, 64)
+    with pytest.raises(moe.MoEError):
+        moe.moe_route(x, torch.zeros(8, 64), None, 2)

@@ -1,0 +1,330 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Every case draws seeded inputs from the synthetic generator, runs the library
+on the device and compares with the oracle element by element: routing and
+dispatch integers bit-exactly (given the device's own logits, so both sides
+decide in the same precision), floating outputs within the stated tolerances.
+"""
+
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_mixture_experts_67_b300 import synth
+from helpers import (assert_close_output, cached_inputs, check_routing_agreement, dev_weights,
+                     require_gpu, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return require_gpu()
+
+
+@pytest.fixture(scope="module")
+def moe(torch):
+    import sparse_mixture_experts_67_b300 as m
+
+    m.moe_device_error(clear=True)
+    yield m
+    assert m.moe_device_error(clear=True) == 0, "a kernel gave up on a barrier wait"
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+ROUTER_CASES = [
+    # name, T, d, E, k, dtype, bias
+    ("tiny_fp32", 256, 64, 8, 2, "f32", None),
+    ("ragged_bf16_e8", 200, 128, 8, 2, "bf16", None),
+    ("zipf_bf16_e64", 130, 256, 64, 4, "bf16", "zipf"),
+    ("wide_bf16_e256", 100, 64, 256, 8, "bf16", None),
+    ("odd_bf16_e10", 77, 128, 10, 3, "bf16", None),
+    ("dense_bf16_e5", 64, 64, 5, 5, "bf16", None),
+    ("single_f32_e1", 33, 16, 1, 1, "f32", None),
+    ("one_token_f32", 1, 8, 4, 2, "f32", None),
+]
+
+
+@pytest.mark.parametrize("case", ROUTER_CASES, ids=[c[0] for c in ROUTER_CASES])
+def test_router_parity(moe, torch, case):
+    name, T, d, E, k, dt, bias = case
+    cfg = synth.small_config(name, T, d, 64, E, k, dt, seed=zlib.crc32(name.encode()) % 1000, wg_std=0.1,
+                             bias="zipf" if bias else "none")
+    x, w_g, b = synth.make_x(cfg), synth.make_router_weight(cfg), synth.router_bias(cfg)
+    out = moe.moe_route(to_dev(x), to_dev(w_g), None if b is None else to_dev(b), k,
+                        want_logits=True, want_probs=True, want_aux=True)
+    torch.cuda.synchronize()
+    x64, wg64 = synth.to_f64(x), synth.to_f64(w_g)
+    s_ref = oracle.router_logits(x64, wg64, b)
+    s_gpu = _np(out["logits"]).astype(np.float64)
+    bound = 1e-5 * (np.abs(x64) @ np.abs(wg64).T) + 1e-6
+    assert np.all(np.abs(s_gpu - s_ref) <= bound), "router logits outside the fp32 accumulation bound"
+    # same-precision decision: the oracle's selection on the device's logits
+    idx_ref, w_ref, g_ref = oracle.topk_route(s_gpu, k)
+    np.testing.assert_array_equal(_np(out["topk_idx"]), idx_ref)
+    np.testing.assert_allclose(_np(out["topk_w"]), w_ref, rtol=0, atol=2e-6)
+    np.testing.assert_allclose(_np(out["probs"]), g_ref, rtol=0, atol=2e-6)
+    np.testing.assert_allclose(_np(out["topk_w"]).sum(axis=1), 1.0, rtol=0, atol=3e-6)
+    # end to end against fp64 logits: only near-ties may differ
+    idx64, _, g64 = oracle.topk_route(s_ref, k)
+    check_routing_agreement(_np(out["topk_idx"]), idx64, g64)
+    # aux statistics from the router's partial sums
+    counts_ref, f_ref, p_ref, loss_ref = oracle.aux_stats(g_ref, idx_ref, E)
+    counts = torch.from_numpy(counts_ref.astype(np.int32)).cuda()
+    aux = moe.moe_aux_loss(counts, T, k, aux_partials=out["aux_partials"])
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(_np(aux["f"]), f_ref, rtol=1e-7, atol=0)
+    np.testing.assert_allclose(_np(aux["p"]), p_ref, rtol=0, atol=2e-6)
+    assert abs(float(_np(aux["loss"])[0]) - loss_ref) <= 1e-5 * max(1.0, loss_ref)
+    aux2 = moe.moe_aux_loss(counts, T, k, probs=out["probs"])
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(_np(aux2["p"]), p_ref, rtol=0, atol=2e-6)
+
+
+PERMUTE_CASES = [
+    # name, T, d, E, k, dtype, idx pattern
+    ("random_e8_bf16", 1000, 64, 8, 2, "bf16", "random"),
+    ("random_e64_k4", 3000, 128, 64, 4, "bf16", "random"),
+    ("skewed_e64_empty", 2500, 64, 64, 4, "bf16", "skewed"),
+    ("all_to_one", 700, 64, 8, 1, "bf16", "one"),
+    ("multi_tile_e256", 5000, 64, 256, 2, "bf16", "random"),
+    ("fp32_e8", 333, 16, 8, 2, "f32", "random"),
+]
+
+
+def _idx_pattern(rng, T, E, k, kind):
+    if kind == "one":
+        return np.full((T, k), 3 % E, np.int32)
+    if kind == "skewed":
+        p = 1.0 / (np.arange(E) + 1.0) ** 2
+        p[40:] = 0
+        p /= p.sum()
+        return np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    return np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("case", PERMUTE_CASES, ids=[c[0] for c in PERMUTE_CASES])
+def test_permute_bit_exact(moe, torch, case):
+    name, T, d, E, k, dt, kind = case
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    idx = _idx_pattern(rng, T, E, k, kind)
+    cfg = synth.small_config(name, T, d, 64, E, k, dt, seed=5)
+    x = synth.make_x(cfg)
+    out = moe.moe_permute(to_dev(x), torch.from_numpy(idx).cuda(), E)
+    torch.cuda.synchronize()
+    counts, offsets, perm, inv_perm = oracle.dispatch(idx.astype(np.int64), E)
+    np.testing.assert_array_equal(_np(out["counts"]), counts)
+    np.testing.assert_array_equal(_np(out["offsets"]), offsets)
+    np.testing.assert_array_equal(_np(out["perm"]), perm)
+    np.testing.assert_array_equal(_np(out["inv_perm"]), inv_perm)
+    xp = _np(out["x_perm"].view(torch.int16) if dt == "bf16" else out["x_perm"])
+    ref = x.view(np.int16)[perm // k] if dt == "bf16" else x[perm // k]
+    np.testing.assert_array_equal(xp, ref)
+
+
+EXPERT_CASES = [
+    # name, counts per expert, d, F, dtype
+    ("bf16_ragged", [130, 0, 1, 257, 64, 500, 3, 0], 128, 256, "bf16"),
+    ("bf16_one_expert", [300], 64, 192, "bf16"),
+    ("bf16_e64_skew", [400 // (e + 1) for e in range(64)], 128, 128, "bf16"),
+    ("f32_ragged", [70, 0, 5, 131], 64, 128, "f32"),
+]
+
+
+@pytest.mark.parametrize("case", EXPERT_CASES, ids=[c[0] for c in EXPERT_CASES])
+def test_grouped_experts_parity(moe, torch, case):
+    name, cnts, d, F, dt = case
+    E = len(cnts)
+    R = int(sum(cnts))
+    cfg = synth.small_config(name, R, d, F, E, 1, dt, seed=11, x_std=1.0, w_std=0.05)
+    inp = synth.make_inputs(cfg)
+    offsets = np.concatenate([[0], np.cumsum(cnts)]).astype(np.int32)
+    w = dev_weights(inp)
+    y_perm, h = moe.moe_experts_swiglu(to_dev(inp.x), torch.from_numpy(offsets).cuda(), w["w_gate"],
+                                       w["w_up"], w["w_down"])
+    torch.cuda.synchronize()
+    x64 = synth.to_f64(inp.x)
+    experts = synth.ExpertsF64(inp.w_gate, inp.w_up, inp.w_down)
+    y_ref = np.zeros((R, d))
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi > lo:
+            y_ref[lo:hi] = oracle.swiglu_expert(x64[lo:hi], *experts[e])
+    assert_close_output(_np(y_perm), y_ref, dt, "y_perm")
+
+
+def _run_layer(moe, torch, inp, outputs_spec):
+    cfg = inp.cfg
+    w = dev_weights(inp)
+    x = to_dev(inp.x)
+    outs = {}
+    for name, (shape, dtype) in outputs_spec.items():
+        outs[name] = torch.empty(shape, dtype=dtype, device="cuda")
+    if cfg.routing == "expert_choice":
+        y = moe.moe_layer_forward(x, w, k=0, routing=1, capacity_factor=cfg.capacity_factor, outputs=outs)
+    else:
+        y = moe.moe_layer_forward(x, w, k=cfg.k, outputs=outs)
+    torch.cuda.synchronize()
+    return y, outs
+
+
+def _topk_outputs(torch, cfg):
+    T, E, k = cfg.T, cfg.E, cfg.k
+    return {"topk_idx": ((T, k), torch.int32), "topk_w": ((T, k), torch.float32),
+            "logits": ((T, E), torch.float32), "counts": ((E,), torch.int32),
+            "offsets": ((E + 1,), torch.int32), "f": ((E,), torch.float32),
+            "p": ((E,), torch.float32), "loss": ((1,), torch.float32)}
+
+
+def _check_topk_layer(moe, torch, cfg, sample=None):
+    inp = cached_inputs(cfg)
+    y, outs = _run_layer(moe, torch, inp, _topk_outputs(torch, cfg))
+    x64 = synth.to_f64(inp.x)
+    s_gpu = _np(outs["logits"]).astype(np.float64)
+    # routing, dispatch and aux: full size, same-precision decisions
+    idx_g, w_g, g_g = oracle.topk_route(s_gpu, cfg.k)
+    np.testing.assert_array_equal(_np(outs["topk_idx"]), idx_g)
+    np.testing.assert_allclose(_np(outs["topk_w"]), w_g, rtol=0, atol=2e-6)
+    counts, offsets, _, _ = oracle.dispatch(idx_g, cfg.E)
+    np.testing.assert_array_equal(_np(outs["counts"]), counts)
+    np.testing.assert_array_equal(_np(outs["offsets"]), offsets)
+    _, f_ref, p_ref, loss_ref = oracle.aux_stats(g_g, idx_g, cfg.E)
+    np.testing.assert_allclose(_np(outs["f"]), f_ref, rtol=1e-6, atol=0)
+    np.testing.assert_allclose(_np(outs["p"]), p_ref, rtol=0, atol=1e-5)
+    assert abs(float(_np(outs["loss"])[0]) - loss_ref) <= 1e-4 * max(1.0, loss_ref)
+    # end-to-end routing against fp64 logits
+    s64 = oracle.router_logits(x64, synth.to_f64(inp.w_g), inp.bias)
+    idx64, w64, g64 = oracle.topk_route(s64, cfg.k)
+    agree = check_routing_agreement(_np(outs["topk_idx"]), idx64, g64)
+    # outputs (sampled at full size) against the fp64 oracle with its own routing
+    tokens = np.arange(cfg.T) if sample is None else np.sort(
+        np.random.default_rng(cfg.seed).choice(cfg.T, size=min(sample, cfg.T), replace=False))
+    tokens = tokens[agree[tokens]]
+    experts = synth.ExpertsF64(inp.w_gate, inp.w_up, inp.w_down)
+    y_ref = oracle.moe_forward(x64[tokens], idx64[tokens], w64[tokens], experts)
+    return assert_close_output(_np(y)[tokens], y_ref, cfg.dtype)
+
+
+def test_layer_tiny_fp32(moe, torch):
+    _check_topk_layer(moe, torch, synth.CONFIGS["tiny_fp32"])
+
+
+def test_layer_small_bf16_multi_tile(moe, torch):
+    cfg = synth.small_config("small_bf16", 1000, 256, 384, 8, 2, "bf16", seed=21, x_std=1.0,
+                             w_std=0.02, wg_std=0.1)
+    _check_topk_layer(moe, torch, cfg)
+
+
+@pytest.mark.slow
+def test_layer_top2_d1024(moe, torch):
+    _check_topk_layer(moe, torch, synth.CONFIGS["top2_d1024"], sample=1024)
+
+
+@pytest.mark.slow
+def test_layer_fine_e64(moe, torch):
+    _check_topk_layer(moe, torch, synth.CONFIGS["fine_e64"], sample=1024)
+
+
+@pytest.mark.slow
+def test_layer_fine_e64_forced_empty(moe, torch):
+    cfg = synth.CONFIGS["fine_e64_forced_empty"]
+    _check_topk_layer(moe, torch, cfg, sample=512)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T", synth.LARGE_T_SWEEP)
+def test_layer_large_d4096(moe, torch, T):
+    cfg = synth.CONFIGS["large_d4096"].with_tokens(T)
+    _check_topk_layer(moe, torch, cfg, sample=None if T <= 256 else 256)
+
+
+def _check_ec_layer(moe, torch, cfg):
+    inp = cached_inputs(cfg)
+    C = cfg.C
+    spec = {"logits": ((cfg.T, cfg.E), torch.float32), "ec_idx": ((cfg.E, C), torch.int32),
+            "ec_score": ((cfg.E, C), torch.float32), "pos": ((cfg.E, cfg.T), torch.int32)}
+    y, outs = _run_layer(moe, torch, inp, spec)
+    s_gpu = _np(outs["logits"]).astype(np.float64)
+    C_ref, idx_g, sc_g, pos_g = oracle.expert_choice_route(s_gpu, cfg.capacity_factor)
+    assert C_ref == C
+    np.testing.assert_array_equal(_np(outs["ec_idx"]), idx_g)
+    np.testing.assert_array_equal(_np(outs["pos"]), pos_g)
+    np.testing.assert_allclose(_np(outs["ec_score"]), sc_g, rtol=1e-5, atol=1e-9)
+    x64 = synth.to_f64(inp.x)
+    s64 = oracle.router_logits(x64, synth.to_f64(inp.w_g), inp.bias)
+    _, idx64, sc64, _ = oracle.expert_choice_route(s64, cfg.capacity_factor)
+    # selections may differ from fp64 only at near-ties of the per-expert scores
+    for e in range(cfg.E):
+        a, b = set(_np(outs["ec_idx"])[e].tolist()), set(idx64[e].tolist())
+        if a != b:
+            col = oracle.softmax(s64[:, e])
+            for t1 in a - b:
+                for t2 in b - a:
+                    assert abs(col[t1] - col[t2]) < 1e-6
+    experts = synth.ExpertsF64(inp.w_gate, inp.w_up, inp.w_down)
+    y_ref = oracle.expert_choice_forward(x64, idx64, sc64, experts)
+    return assert_close_output(_np(y), y_ref, cfg.dtype)
+
+
+def test_layer_small_expert_choice(moe, torch):
+    cfg = synth.LayerConfig("small_ec", T=500, d=128, F=256, E=6, k=0, dtype="bf16", x_std=1.0,
+                            w_std=0.05, wg_std=0.1, seed=31, routing="expert_choice",
+                            capacity_factor=1.5)
+    _check_ec_layer(moe, torch, cfg)
+
+
+def test_layer_expert_choice_fp32(moe, torch):
+    cfg = synth.LayerConfig("small_ec32", T=300, d=32, F=64, E=4, k=0, dtype="f32", x_std=0.5,
+                            w_std=0.05, wg_std=0.1, seed=32, routing="expert_choice",
+                            capacity_factor=1.0)
+    _check_ec_layer(moe, torch, cfg)
+
+
+@pytest.mark.slow
+def test_layer_ec_e16(moe, torch):
+    _check_ec_layer(moe, torch, synth.CONFIGS["ec_e16"])
+
+
+def test_expert_choice_zero_capacity(moe, torch):
+    cfg = synth.LayerConfig("ec_zero", T=10, d=64, F=64, E=4, k=0, dtype="bf16", x_std=1.0,
+                            w_std=0.05, wg_std=0.1, seed=33, routing="expert_choice",
+                            capacity_factor=0.3)
+    assert cfg.C == 0
+    inp = synth.make_inputs(cfg)
+    y, outs = _run_layer(moe, torch, inp, {"pos": ((cfg.E, cfg.T), torch.int32)})
+    assert np.all(_np(y) == 0)
+    assert np.all(_np(outs["pos"]) == -1)
+
+
+def test_layer_dense_limit_and_single_expert(moe, torch):
+    for E, k in ((4, 4), (1, 1)):
+        cfg = synth.small_config(f"dense{E}", 150, 64, 128, E, k, "f32", seed=40 + E, x_std=1.0,
+                                 w_std=0.05)
+        _check_topk_layer(moe, torch, cfg)
+
+
+def test_layer_zero_tokens(moe, torch):
+    cfg = synth.small_config("zero", 4, 64, 128, 8, 2, "bf16", seed=3)
+    inp = synth.make_inputs(cfg)
+    w = dev_weights(inp)
+    x = to_dev(inp.x)[:0]
+    y = torch.full((0, 64), 7.0, device="cuda")
+    moe.moe_layer_forward(x, w, k=2, y=y)
+    torch.cuda.synchronize()
+    assert y.shape == (0, 64)
+
+
+def test_layer_deterministic(moe, torch):
+    cfg = synth.small_config("det", 3000, 128, 256, 16, 4, "bf16", seed=50, x_std=1.0, w_std=0.05)
+    inp = synth.make_inputs(cfg)
+    w = dev_weights(inp)
+    x = to_dev(inp.x)
+    y1 = moe.moe_layer_forward(x, w, k=4).clone()
+    y2 = moe.moe_layer_forward(x, w, k=4)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
