@@ -1,21 +1,506 @@
-// Grouped bf16 expert GEMMs (placeholder: FFMA tiles until the tensor-core
-// kernels land).
+// Grouped bf16 expert GEMMs on the 5th-generation tensor cores (sm_103a).
+//
+// The SwiGLU expert of "Mixture of Experts（MoE）の理論と実装" (Expert.forward)
+// and "Sparse Mixture of Experts(MoE) 아키텍처 심층 분석" (SwiGLUExpert):
+//   gate/up:  H = silu(X_e W_gate,e^T) * (X_e W_up,e^T)   (bf16 out)
+//   down:     Y = H_e W_down,e^T                          (fp32 out)
+// over the variable-size expert segments [offsets[e], offsets[e+1]) of the
+// dispatched rows.  The segment sizes stay on the device.
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0     TMA producer (one thread): A tile [128 x 64] of the rows and the
+//              B tile [256 x 64] of the weights per k-block into a 4-stage
+//              ring (128-byte swizzle), completion on mbarriers;
+//   warp 1     allocates all 512 TMEM columns; one thread issues
+//              tcgen05.mma kind::f16 (M=128, N=256, K=16, fp32 accumulate)
+//              into one of two TMEM accumulators and commits to mbarriers;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = row), SwiGLU
+//              or plain fp32, vector stores masked at the segment end.
+// For gate/up the B tile stacks 128 rows of W_gate over the same 128 rows of
+// W_up, so one N=256 instruction produces both halves of the SwiGLU.
+// Tiles are (expert, 128-row block, n-block), enumerated on the device from
+// the offsets; CTAs stride over them.  Every barrier wait is bounded in time:
+// on expiry the kernel records a code in the device error word, drains its
+// in-flight copies and MMAs, frees TMEM and returns.
 #pragma once
 
-#include "grouped_simt.cuh"
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
 
 namespace moe {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int kThreads = 192;
+constexpr int kEpilogueWarp0 = 2;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 512;  // two 256-column fp32 accumulators
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
+// error-word codes
+constexpr uint32_t kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain = 8u;
+
+struct Smem {  // lives after the 1024-aligned stage ring
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int cum[MOE_MAX_EXPERTS + 1];  // prefix of 128-row blocks per expert
+  int off[MOE_MAX_EXPERTS + 1];  // segment offsets
+};
+constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + sizeof(Smem) + 1024;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `parity` to complete.  Gives up (false) when the
+// CTA's abort flag is raised or after kWaitTimeoutNs, recording `code`.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t code) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      record_error(code);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major tile with 128-byte rows in the
+// 128-byte swizzle (8-row atoms of 1024 bytes, stride byte offset 1024).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
+  d |= (uint64_t)1u << 16;                  // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024u >> 4) << 32;        // stride byte offset: next 8-row group
+  d |= (uint64_t)1u << 46;                  // descriptor version
+  d |= (uint64_t)2u << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+#define MOE_TMEM_LD32(taddr, r)                                                                   \
+  asm volatile(                                                                                   \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"              \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),       \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),   \
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),            \
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),            \
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])             \
+      : "r"(taddr))
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct TileCoord {
+  int e, row0, row_end, nt;
+};
+
+__device__ __forceinline__ TileCoord map_tile(const Smem& S, int E, int n_tiles, int tile) {
+  TileCoord c;
+  const int mt = tile / n_tiles;
+  c.nt = tile - mt * n_tiles;
+  int lo = 0, hi = E;  // S.cum[lo] <= mt < S.cum[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (S.cum[mid] <= mt) lo = mid;
+    else hi = mid;
+  }
+  c.e = lo;
+  c.row0 = S.off[lo] + (mt - S.cum[lo]) * BM;
+  c.row_end = S.off[lo + 1];
+  return c;
+}
+
+__device__ __forceinline__ float silu_fast(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// GATEUP: out = bf16 H [R, N] (N = F), B rows from two maps (gate, up), 128 each.
+// !GATEUP: out = fp32 Y [R, N] (N = d), B rows from one map, 256 per tile.
+template <bool GATEUP>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                      const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets,
+                      int R, int E, int N, int K, void* __restrict__ out) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* ring = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem& S = *reinterpret_cast<Smem*>(ring + (size_t)STAGES * STAGE_BYTES);
+  volatile int* abort_flag = &S.abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kTileN = GATEUP ? BN / 2 : BN;  // output columns per tile
+  const int n_tiles = (N + kTileN - 1) / kTileN;
+  const int num_kb = K / BK;
+
+  // --- setup
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) S.off[i] = min(max(offsets[i], 0), R);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&S.tmem_full[b], 1);
+      mbar_init(&S.tmem_empty[b], 128);
+    }
+    mbar_init(&S.drain, 1);
+    S.abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB0);
+    if (GATEUP) prefetch_tensormap(&tmB1);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&S.tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int cum = 0;
+    for (int e = 0; e < E; ++e) {
+      S.cum[e] = cum;
+      const int cnt = max(S.off[e + 1] - S.off[e], 0);
+      cum += (cnt + BM - 1) / BM;
+    }
+    S.cum[E] = cum;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = S.tmem_base;
+  const int total = S.cum[E] * n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_phase = 0;  // per-stage bits: loads issued, their parity
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const TileCoord c = map_tile(S, E, n_tiles, tile);
+        const int brow = c.e * N + c.nt * kTileN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, kErrProducer)) break;
+          unsigned char* sA = ring + (size_t)stage * STAGE_BYTES;
+          unsigned char* sB = sA + A_BYTES;
+          mbar_arrive_expect_tx(&S.full[stage], STAGE_BYTES);
+          tma_load_2d(sA, &tmA, &S.full[stage], kb * BK, c.row0);
+          if (GATEUP) {
+            tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
+            tma_load_2d(sB + B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, brow);
+          } else {
+            tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
+          }
+          issued |= 1u << stage;
+          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain: every issued load must have landed before the CTA may exit
+      for (int s = 0; s < STAGES; ++s) {
+        if (!((issued >> s) & 1u)) continue;
+        const uint32_t a = smem_u32(&S.full[s]);
+        const uint32_t par = (issued_phase >> s) & 1u;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(a, par)) {
+          if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+            record_error(kErrDrain);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        if (!mbar_wait(&S.tmem_empty[acc], acc_phase ^ 1u, abort_flag, kErrMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&S.full[stage], phase, abort_flag, kErrMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(ring + (size_t)stage * STAGE_BYTES);
+          const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            tc_mma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                       (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&S.empty[stage]);  // frees the smem stage once these MMAs finish
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&S.tmem_full[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // drain: all issued MMAs complete before TMEM is released
+      tc_commit(&S.drain);
+      const uint32_t a = smem_u32(&S.drain);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(a, 0)) {
+        if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+          record_error(kErrDrain);
+          break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileCoord c = map_tile(S, E, n_tiles, tile);
+      if (!mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kErrEpilogue)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      const int row = c.row0 + row_in_tile;
+      const bool valid = row < c.row_end;
+      const int n0 = c.nt * kTileN;
+      if (GATEUP) {
+        __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
+#pragma unroll 1
+        for (int cc = 0; cc < kTileN; cc += 32) {
+          uint32_t g[32], u[32];
+          MOE_TMEM_LD32(taddr + cc, g);
+          MOE_TMEM_LD32(taddr + kTileN + cc, u);
+          tmem_ld_wait();
+          if (valid && n0 + cc < N) {
+            uint32_t p[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+              const float h1 =
+                  silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+              p[i] = pack_bf16x2(h0, h1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(H + (size_t)row * N + n0 + cc);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+          }
+        }
+      } else {
+        float* Y = static_cast<float*>(out);
+#pragma unroll 1
+        for (int cc = 0; cc < kTileN; cc += 32) {
+          uint32_t v[32];
+          MOE_TMEM_LD32(taddr + cc, v);
+          tmem_ld_wait();
+          if (valid && n0 + cc < N) {
+            float4* dst = reinterpret_cast<float4*>(Y + (size_t)row * N + n0 + cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&S.tmem_empty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of [box_rows, 64] with the
+// 128-byte swizzle; out-of-range rows read as zero.
+inline bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+template <bool GATEUP>
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                   const int32_t* offsets, int R, int E, int N, int K, void* out, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel<GATEUP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  constexpr int tile_n = GATEUP ? BN / 2 : BN;
+  const long long max_tiles = (long long)((R + BM - 1) / BM + E) * ((N + tile_n - 1) / tile_n);
+  const int grid = (int)std::min<long long>(sm_count(), max_tiles);
+  grouped_tc_kernel<GATEUP><<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, offsets, R, E, N, K, out);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
 
 inline cudaError_t launch_gateup_tc(const __nv_bfloat16* x_perm, const int32_t* offsets,
                                     const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up, int R,
                                     int d, int F, int E, __nv_bfloat16* h, cudaStream_t s) {
-  return launch_grouped_simt<__nv_bfloat16, true>(x_perm, offsets, w_gate, w_up, R, F, d, E, h, s);
+  CUtensorMap a, b0, b1;
+  if (!tc::make_map(&a, x_perm, (uint64_t)R, (uint64_t)d, tc::BM) ||
+      !tc::make_map(&b0, w_gate, (uint64_t)E * F, (uint64_t)d, tc::BN / 2) ||
+      !tc::make_map(&b1, w_up, (uint64_t)E * F, (uint64_t)d, tc::BN / 2))
+    return cudaErrorInvalidValue;
+  return tc::launch<true>(a, b0, b1, offsets, R, E, F, d, h, s);
 }
 
 inline cudaError_t launch_down_tc(const __nv_bfloat16* h, const int32_t* offsets,
                                   const __nv_bfloat16* w_down, int R, int d, int F, int E,
                                   float* y_perm, cudaStream_t s) {
-  return launch_grouped_simt<__nv_bfloat16, false>(h, offsets, w_down, nullptr, R, d, F, E, y_perm, s);
+  CUtensorMap a, b0;
+  if (!tc::make_map(&a, h, (uint64_t)R, (uint64_t)F, tc::BM) ||
+      !tc::make_map(&b0, w_down, (uint64_t)E * d, (uint64_t)F, tc::BN))
+    return cudaErrorInvalidValue;
+  return tc::launch<false>(a, b0, b0, offsets, R, E, d, F, y_perm, s);
 }
 
 }  // namespace moe
