@@ -151,11 +151,13 @@ def test_grouped_experts_parity(moe, torch, case):
     x64 = synth.to_f64(inp.x)
     experts = synth.ExpertsF64(inp.w_gate, inp.w_up, inp.w_down)
     y_ref = np.zeros((R, d))
+    y_ref_h = np.zeros((R, d))
     for e in range(E):
         lo, hi = offsets[e], offsets[e + 1]
         if hi > lo:
             y_ref[lo:hi] = oracle.swiglu_expert(x64[lo:hi], *experts[e])
-    assert_close_output(_np(y_perm), y_ref, dt, "y_perm")
+            y_ref_h[lo:hi] = oracle.swiglu_expert(x64[lo:hi], *experts[e], round_h=oracle.bf16_round)
+    assert_close_output(_np(y_perm), y_ref, dt, f"y_perm[{name}]", ref_bf16_h=y_ref_h if dt == "bf16" else None)
 
 
 def _run_layer(moe, torch, inp, outputs_spec):
@@ -207,7 +209,12 @@ def _check_topk_layer(moe, torch, cfg, sample=None):
     tokens = tokens[agree[tokens]]
     experts = synth.ExpertsF64(inp.w_gate, inp.w_up, inp.w_down)
     y_ref = oracle.moe_forward(x64[tokens], idx64[tokens], w64[tokens], experts)
-    return assert_close_output(_np(y)[tokens], y_ref, cfg.dtype)
+    y_ref_h = None
+    if cfg.dtype == "bf16":
+        y_ref_h = oracle.moe_forward(x64[tokens], idx64[tokens], w64[tokens], experts,
+                                     round_h=oracle.bf16_round)
+    return assert_close_output(_np(y)[tokens], y_ref, cfg.dtype, what=f"y[{cfg.name}]",
+                               ref_bf16_h=y_ref_h)
 
 
 def test_layer_tiny_fp32(moe, torch):
@@ -268,7 +275,10 @@ def _check_ec_layer(moe, torch, cfg):
                     assert abs(col[t1] - col[t2]) < 1e-6
     experts = synth.ExpertsF64(inp.w_gate, inp.w_up, inp.w_down)
     y_ref = oracle.expert_choice_forward(x64, idx64, sc64, experts)
-    return assert_close_output(_np(y), y_ref, cfg.dtype)
+    y_ref_h = None
+    if cfg.dtype == "bf16":
+        y_ref_h = oracle.expert_choice_forward(x64, idx64, sc64, experts, round_h=oracle.bf16_round)
+    return assert_close_output(_np(y), y_ref, cfg.dtype, what=f"y[{cfg.name}]", ref_bf16_h=y_ref_h)
 
 
 def test_layer_small_expert_choice(moe, torch):
