@@ -126,6 +126,30 @@ moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int
                        int32_t* perm, int32_t* inv_perm, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
 
+/* Allocation-free variant of moe_permute: same arguments, outputs and
+ * results (bit-exact), but no workspace argument.  The pages have no
+ * counterpart; this exists for callers that cannot provide device scratch:
+ * plugin hosts that give a kernel only its input and output buffers, and
+ * deployments whose device memory is reserved up front by another allocator,
+ * so that nothing may call cudaMalloc while they run.  The scratch (per-tile
+ * expert counts and their scanned bases) lives in a fixed array of
+ * MOE_PERMUTE_NOALLOC_SCRATCH_BYTES inside the library's device memory, held
+ * by every GPU that loads the library until the process exits.
+ *   Limit: ceil(T*k / 2048) * E <= MOE_PERMUTE_NOALLOC_SCRATCH_BYTES / 8
+ *          (32768 for 256 KiB: e.g. T*k up to 262144 at E = 256, 1048576 at
+ *          E = 64); larger sizes return MOE_ERR_WORKSPACE without any work.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.  The call itself never allocates (no cudaMalloc or
+ *   cudaFree).
+ *   All calls share the one array and it keeps the last call's contents
+ *   (every entry a call reads it first writes); calls whose work overlaps on
+ *   the GPU race on it, so the caller must serialise them.                  */
+#define MOE_PERMUTE_NOALLOC_SCRATCH_BYTES (256u * 1024u)
+moe_status moe_permute_noalloc(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
+                               moe_dtype dt, void* x_perm, int32_t* counts, int32_t* offsets,
+                               int32_t* perm, int32_t* inv_perm, moe_stream_t stream);
+
 /* Row gather used by both routings: x_perm[r,:] = x[src[r] / div, :] for
  * r < R (div = k for top-k perm arrays, 1 for expert-choice token ids).    */
 moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, int T, int d,

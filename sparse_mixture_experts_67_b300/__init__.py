@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "MoEError", "lib", "declared_symbols", "moe_route", "moe_expert_choice_route",
-    "moe_expert_choice_capacity", "moe_permute", "moe_gather_rows", "moe_grouped_gateup_swiglu",
+    "moe_expert_choice_capacity", "moe_permute", "moe_permute_noalloc", "moe_gather_rows", "moe_grouped_gateup_swiglu",
     "moe_grouped_down", "moe_experts_swiglu", "moe_combine", "moe_ec_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_layer_workspace_size", "moe_route_aux_rows", "moe_device_error",
     "MoELayer",
@@ -72,6 +72,7 @@ _SIGS = {
     "moe_permute_workspace_size": ([_I, _I, _I], _Z),
     "moe_permute": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_gather_rows": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "moe_permute_noalloc": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gateup_swiglu": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "moe_grouped_down": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "moe_experts_swiglu": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
@@ -218,6 +219,31 @@ def moe_permute(x: torch.Tensor, topk_idx: torch.Tensor, E: int) -> Dict[str, to
         _ptr(out["offsets"]), _ptr(out["perm"]), _ptr(out["inv_perm"]), _ptr(ws), ws_bytes,
         _stream()))
     return out
+
+
+def moe_permute_noalloc(x: torch.Tensor, topk_idx: torch.Tensor, E: int,
+                        out: Optional[Dict[str, torch.Tensor]] = None) -> Dict[str, torch.Tensor]:
+    """moe_permute without a workspace: the library's fixed device scratch is used instead.
+
+    ``out`` may hold preallocated x_perm, counts, offsets, perm, inv_perm tensors
+    (missing ones are created here with torch).
+    """
+    _dev(x, topk_idx)
+    T, d = x.shape
+    k = topk_idx.shape[1]
+    A = T * k
+    shapes = {"x_perm": ((A, d), x.dtype), "counts": ((E,), torch.int32),
+              "offsets": ((E + 1,), torch.int32), "perm": ((A,), torch.int32),
+              "inv_perm": ((A,), torch.int32)}
+    res = dict(out or {})
+    for name, (shape, dtype) in shapes.items():
+        if name not in res:
+            res[name] = _empty(shape, dtype, x)
+        _dev(res[name])
+    _check("moe_permute_noalloc", lib().moe_permute_noalloc(
+        _ptr(x), _ptr(topk_idx), T, d, E, k, _dtype(x), _ptr(res["x_perm"]), _ptr(res["counts"]),
+        _ptr(res["offsets"]), _ptr(res["perm"]), _ptr(res["inv_perm"]), _stream()))
+    return res
 
 
 def moe_gather_rows(x: torch.Tensor, src: torch.Tensor, div: int) -> torch.Tensor:

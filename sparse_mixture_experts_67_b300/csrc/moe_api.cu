@@ -396,3 +396,6 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
 }
 
 }  // extern "C"
+
+// Allocation-free dispatch variant (static device scratch).
+#include "permute_noalloc.cu"
