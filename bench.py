@@ -270,7 +270,7 @@ def run_gpu(args, cfg):
 def launches_per_step(cfg) -> int:
     if cfg.routing == "expert_choice":
         return 7  # logits, EC select, offsets, gather, gate/up, down, EC combine
-    return 9  # router, hist, scan, scatter, gather, gate/up, down, combine, aux
+    return 7  # router (+ dispatch counts), scan, scatter + row copy, gate/up, down, combine, aux
 
 
 def stage_breakdown(moe, torch, cfg, x, w, flush, stream, steps):

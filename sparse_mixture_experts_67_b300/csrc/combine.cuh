@@ -109,30 +109,37 @@ __global__ void probs_partials_kernel(const float* __restrict__ probs, int T, in
   }
 }
 
-// One CTA of MOE_MAX_EXPERTS threads.
-__global__ void __launch_bounds__(MOE_MAX_EXPERTS)
+// One CTA of kAuxThreads.  Warp w reduces experts w, w + 8, ...: each lane sums
+// a fixed strided subset of the partial rows, then a fixed butterfly.
+constexpr int kAuxThreads = 256;
+__global__ void __launch_bounds__(kAuxThreads)
     aux_finalize_kernel(const float* __restrict__ partials, int rows, const int32_t* __restrict__ counts,
                         int T, int E, float* __restrict__ f, float* __restrict__ p,
                         float* __restrict__ loss) {
   __shared__ float s[MOE_MAX_EXPERTS];
-  const int e = threadIdx.x;
-  float fp = 0.f;
-  if (e < E) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int nwarps = kAuxThreads / 32;
+  for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += kAuxThreads) s[e] = 0.f;
+  __syncthreads();
+  for (int e = warp; e < E; e += nwarps) {
     float acc = 0.f;
-    for (int r = 0; r < rows; ++r) acc += partials[(size_t)r * E + e];
-    const float pe = acc / (float)T;
-    const float fe = (float)counts[e] / (float)T;
-    if (p) p[e] = pe;
-    if (f) f[e] = fe;
-    fp = fe * pe;
+    for (int r = lane; r < rows; r += 32) acc += partials[(size_t)r * E + e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+    if (lane == 0) {
+      const float pe = acc / (float)T;
+      const float fe = (float)counts[e] / (float)T;
+      if (p) p[e] = pe;
+      if (f) f[e] = fe;
+      s[e] = fe * pe;
+    }
   }
-  s[e] = fp;
   __syncthreads();
   for (int off = MOE_MAX_EXPERTS / 2; off > 0; off >>= 1) {
-    if (e < off) s[e] += s[e + off];
+    for (int e = threadIdx.x; e < off; e += kAuxThreads) s[e] += s[e + off];
     __syncthreads();
   }
-  if (e == 0 && loss) *loss = (float)E * s[0];
+  if (threadIdx.x == 0 && loss) *loss = (float)E * s[0];
 }
 
 }  // namespace moe

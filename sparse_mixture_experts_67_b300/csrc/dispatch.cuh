@@ -5,35 +5,37 @@
 // do in "Sparse Mixture of Experts(MoE) 아키텍처 심층 분석" (youngju.dev), with
 // the order inside an expert fixed to ascending assignment id a = t*k + j.
 //
-// Three small kernels make it deterministic without a global sort:
-//   hist:    each tile of kDispatchTile assignments counts its experts with
-//            warp-aggregated shared-memory atomics (match_any + popc);
+// Deterministic without a global sort, in tiles of `tile` consecutive
+// assignments (the layer uses one tile per router CTA, 64 tokens):
+//   hist:    per-tile expert counts with warp-aggregated shared-memory
+//            atomics (match_any + popc); in the layer the router's epilogue
+//            produces them instead;
 //   scan:    one CTA turns the [tiles, E] count matrix into per-(tile, expert)
-//            bases and the expert offsets (exclusive scan over experts);
+//            bases and the expert offsets, with warp scans over the tiles;
 //   scatter: each tile re-reads its assignments in order and ranks them among
 //            equal experts (warp match_any rank + per-warp counts in shared
-//            memory), giving perm / inv_perm bit-exactly.
-// The row gather then copies x rows into the dispatch order with 16-byte
-// vector loads, one warp per row.
+//            memory), giving perm / inv_perm bit-exactly, then its warps copy
+//            the x rows of the round into the dispatch order (16-byte vectors).
 #pragma once
 
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int kDispatchTile = 2048;
 constexpr int kDispatchThreads = 256;
 constexpr int kDispatchWarps = kDispatchThreads / 32;
+constexpr int kScanThreads = 1024;
 
-inline int dispatch_tiles(long long A) { return A == 0 ? 0 : ceil_div(A, kDispatchTile); }
+inline int dispatch_tiles(long long A, int tile) { return A == 0 ? 0 : ceil_div(A, tile); }
 
 __global__ void __launch_bounds__(kDispatchThreads)
-    dispatch_hist_kernel(const int32_t* __restrict__ idx, int A, int E, int32_t* __restrict__ tile_counts) {
+    dispatch_hist_kernel(const int32_t* __restrict__ idx, int A, int E, int tile,
+                         int32_t* __restrict__ tile_counts) {
   __shared__ int cnt[MOE_MAX_EXPERTS];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
-  const int a0 = blockIdx.x * kDispatchTile;
-  const int a1 = min(A, a0 + kDispatchTile);
+  const int a0 = blockIdx.x * tile;
+  const int a1 = min(A, a0 + tile);
   const int lane = threadIdx.x & 31;
   for (int base = a0; base < a1; base += kDispatchThreads) {
     const int a = base + threadIdx.x;
@@ -46,53 +48,87 @@ __global__ void __launch_bounds__(kDispatchThreads)
   for (int e = threadIdx.x; e < E; e += blockDim.x) tile_counts[(size_t)blockIdx.x * E + e] = cnt[e];
 }
 
-// One CTA of MOE_MAX_EXPERTS threads.  tile_base[tile][e] becomes the first
-// dispatch row of expert e's assignments that fall in `tile`.
-__global__ void __launch_bounds__(MOE_MAX_EXPERTS)
+// One CTA.  tile_base[t][e] = offsets[e] + sum of tile_counts[t'][e] over t' < t.
+__global__ void __launch_bounds__(kScanThreads)
     dispatch_scan_kernel(const int32_t* __restrict__ tile_counts, int tiles, int E, int A,
                          int32_t* __restrict__ tile_base, int32_t* __restrict__ counts,
                          int32_t* __restrict__ offsets) {
-  __shared__ int s[MOE_MAX_EXPERTS];
-  const int e = threadIdx.x;
-  int total = 0;
-  if (e < E) {
-    for (int t = 0; t < tiles; ++t) {
-      const int c = tile_counts[(size_t)t * E + e];
-      tile_base[(size_t)t * E + e] = total;
-      total += c;
+  __shared__ int s_tot[MOE_MAX_EXPERTS];
+  __shared__ int s_off[MOE_MAX_EXPERTS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int nwarps = kScanThreads / 32;
+  for (int e = warp; e < E; e += nwarps) {
+    int acc = 0;
+    for (int t = lane; t < tiles; t += 32) acc += tile_counts[(size_t)t * E + e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+    if (lane == 0) s_tot[e] = acc;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the (<= 256) totals: 8 per lane, then a warp scan
+    constexpr int per = MOE_MAX_EXPERTS / 32;
+    int v[per], run = 0;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      v[i] = e < E ? s_tot[e] : 0;
+      run += v[i];
+    }
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += n;
+    }
+    int ex = incl - run;
+#pragma unroll
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < E) s_off[e] = ex;
+      ex += v[i];
     }
   }
-  s[e] = (e < E) ? total : 0;
   __syncthreads();
-  // Hillis-Steele inclusive scan over the (<= 256) experts
-  for (int off = 1; off < MOE_MAX_EXPERTS; off <<= 1) {
-    const int v = (e >= off) ? s[e - off] : 0;
-    __syncthreads();
-    s[e] += v;
-    __syncthreads();
+  for (int e = warp; e < E; e += nwarps) {
+    int running = s_off[e];
+    for (int t0 = 0; t0 < tiles; t0 += 32) {
+      const int t = t0 + lane;
+      const int v = t < tiles ? tile_counts[(size_t)t * E + e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(kFullMask, incl, off);
+        if (lane >= off) incl += n;
+      }
+      if (t < tiles) tile_base[(size_t)t * E + e] = running + incl - v;
+      running += __shfl_sync(kFullMask, incl, 31);
+    }
+    if (lane == 0) {
+      counts[e] = s_tot[e];
+      offsets[e] = s_off[e];
+    }
   }
-  if (e < E) {
-    const int excl = s[e] - total;
-    counts[e] = total;
-    offsets[e] = excl;
-    for (int t = 0; t < tiles; ++t) tile_base[(size_t)t * E + e] += excl;
-  }
-  if (e == 0) offsets[E] = A;
+  if (threadIdx.x == 0) offsets[E] = A;
 }
 
+// Ranks each assignment among equal experts of its tile and writes perm /
+// inv_perm; with x != nullptr it also copies x[a / k] into x_perm[row].
 __global__ void __launch_bounds__(kDispatchThreads)
-    dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E,
+    dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E, int k, int tile,
                             const int32_t* __restrict__ tile_base, int32_t* __restrict__ perm,
-                            int32_t* __restrict__ inv_perm) {
+                            int32_t* __restrict__ inv_perm, const uint4* __restrict__ x,
+                            int vec_per_row, uint4* __restrict__ x_perm) {
   __shared__ int running[MOE_MAX_EXPERTS];
   __shared__ int wcnt[kDispatchWarps][MOE_MAX_EXPERTS];
+  __shared__ int s_row[kDispatchThreads];
+  __shared__ int s_tok[kDispatchThreads];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     running[e] = tile_base[(size_t)blockIdx.x * E + e];
     for (int w = 0; w < kDispatchWarps; ++w) wcnt[w][e] = 0;
   }
   __syncthreads();
-  const int a0 = blockIdx.x * kDispatchTile;
-  const int a1 = min(A, a0 + kDispatchTile);
+  const int a0 = blockIdx.x * tile;
+  const int a1 = min(A, a0 + tile);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int base = a0; base < a1; base += kDispatchThreads) {
     const int a = base + threadIdx.x;
@@ -107,6 +143,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
       for (int w = 0; w < warp; ++w) row += wcnt[w][e];
       perm[row] = a;
       inv_perm[a] = row;
+      s_row[threadIdx.x] = row;
+      s_tok[threadIdx.x] = a / k;
     }
     __syncthreads();
     for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
@@ -117,6 +155,23 @@ __global__ void __launch_bounds__(kDispatchThreads)
         wcnt[w][ee] = 0;
       }
       running[ee] += s;
+    }
+    if (x != nullptr) {  // copy this round's rows, one warp per row
+      const int nvalid = min(kDispatchThreads, a1 - base);
+      for (int i = warp; i < nvalid; i += kDispatchWarps) {
+        const uint4* src = x + (size_t)s_tok[i] * vec_per_row;
+        uint4* dst = x_perm + (size_t)s_row[i] * vec_per_row;
+        int v = lane;
+        for (; v + 96 < vec_per_row; v += 128) {
+          const uint4 q0 = __ldg(src + v), q1 = __ldg(src + v + 32), q2 = __ldg(src + v + 64),
+                      q3 = __ldg(src + v + 96);
+          dst[v] = q0;
+          dst[v + 32] = q1;
+          dst[v + 64] = q2;
+          dst[v + 96] = q3;
+        }
+        for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+      }
     }
     __syncthreads();
   }

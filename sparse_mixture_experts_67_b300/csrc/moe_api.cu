@@ -121,7 +121,7 @@ moe_status moe_expert_choice_route(const void* x, const void* w_g, const float* 
 
 size_t moe_permute_workspace_size(int T, int E, int k) {
   if (T < 0 || E < 1 || k < 1) return 0;
-  const int tiles = dispatch_tiles((long long)T * k);
+  const int tiles = dispatch_tiles((long long)T * k, kRouterTokens * k);
   return 2 * align256((size_t)tiles * E * sizeof(int32_t)) + 256;
 }
 
@@ -140,16 +140,42 @@ moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, in
   return cuda_status(cudaGetLastError());
 }
 
-moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
-                       moe_dtype dt, void* x_perm, int32_t* counts, int32_t* offsets, int32_t* perm,
-                       int32_t* inv_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+// Scan + scatter (+ row copy) of the dispatch; with counts_ready the per-tile
+// counts are already in tile_counts (written by the router), else a histogram
+// pass computes them.  Tiles are `tile` consecutive assignments.
+static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
+                                  moe_dtype dt, void* x_perm, int32_t* counts, int32_t* offsets,
+                                  int32_t* perm, int32_t* inv_perm, int32_t* tile_counts,
+                                  int32_t* tile_base, int tile, bool counts_ready, cudaStream_t s) {
+  const long long A = (long long)T * k;
+  const int tiles = dispatch_tiles(A, tile);
+  if (!counts_ready)
+    dispatch_hist_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile, tile_counts);
+  dispatch_scan_kernel<<<1, kScanThreads, 0, s>>>(tile_counts, tiles, E, (int)A, tile_base, counts,
+                                                  offsets);
+  dispatch_scatter_kernel<<<tiles, kDispatchThreads, 0, s>>>(
+      topk_idx, (int)A, E, k, tile, tile_base, perm, inv_perm, static_cast<const uint4*>(x),
+      (int)(d * elt_size(dt) / 16), static_cast<uint4*>(x_perm));
+  return cuda_status(cudaGetLastError());
+}
+
+static moe_status check_permute(const void* x, const void* x_perm, int T, int d, int E, int k,
+                                moe_dtype dt, const int32_t* counts, const int32_t* offsets) {
   if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
   moe_status st = check_dims(d, dt);
   if (st != MOE_OK) return st;
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if ((long long)T * k > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if (T > 0 && x && x_perm && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
+                       moe_dtype dt, void* x_perm, int32_t* counts, int32_t* offsets, int32_t* perm,
+                       int32_t* inv_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status st = check_permute(x, x_perm, T, d, E, k, dt, counts, offsets);
+  if (st != MOE_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  const long long A = (long long)T * k;
-  if (A > INT32_MAX) return MOE_ERR_UNSUPPORTED;
   if (T == 0) {  // empty: counts = 0, offsets = 0
     cudaError_t e = cudaMemsetAsync(counts, 0, E * sizeof(int32_t), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, (E + 1) * sizeof(int32_t), s);
@@ -157,19 +183,13 @@ moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int
   }
   if (!x || !topk_idx || !x_perm || !perm || !inv_perm) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < moe_permute_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
-  const int tiles = dispatch_tiles(A);
+  const int tiles = dispatch_tiles((long long)T * k, kRouterTokens * k);
   Carver cv{static_cast<char*>(ws)};
   cv.used = (256 - (reinterpret_cast<uintptr_t>(ws) & 255)) & 255;
   int32_t* tile_counts = cv.take<int32_t>((size_t)tiles * E);
   int32_t* tile_base = cv.take<int32_t>((size_t)tiles * E);
-  dispatch_hist_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile_counts);
-  dispatch_scan_kernel<<<1, MOE_MAX_EXPERTS, 0, s>>>(tile_counts, tiles, E, (int)A, tile_base,
-                                                     counts, offsets);
-  dispatch_scatter_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile_base, perm,
-                                                             inv_perm);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return moe_gather_rows(x, perm, (int)A, k, T, d, dt, x_perm, stream);
+  return dispatch_launch(x, topk_idx, T, d, E, k, dt, x_perm, counts, offsets, perm, inv_perm,
+                         tile_counts, tile_base, kRouterTokens * k, false, s);
 }
 
 static moe_status check_experts(int R, int d, int F, int E, moe_dtype dt) {
@@ -264,7 +284,7 @@ moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int
     if (!aux_partials) return MOE_ERR_INVALID_ARG;
     probs_partials_kernel<<<rows, 256, 0, s>>>(probs, T, E, const_cast<float*>(aux_partials));
   }
-  aux_finalize_kernel<<<1, MOE_MAX_EXPERTS, 0, s>>>(aux_partials, rows, counts, T, E, f, p, loss);
+  aux_finalize_kernel<<<1, kAuxThreads, 0, s>>>(aux_partials, rows, counts, T, E, f, p, loss);
   return cuda_status(cudaGetLastError());
 }
 
@@ -380,11 +400,19 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   if (O.topk_w) tw = O.topk_w;
   if (O.counts) counts = O.counts;
   if (O.offsets) offsets = O.offsets;
-  st = moe_route(x, w->w_g, w->bias, D.T, D.d, D.E, k, D.dtype, idx, tw, O.logits, nullptr, aux,
-                 stream);
+  st = check_permute(x, x_perm, D.T, D.d, D.E, k, D.dtype, counts, offsets);
   if (st != MOE_OK) return st;
-  st = moe_permute(x, idx, D.T, D.d, D.E, k, D.dtype, x_perm, counts, offsets, perm, inv_perm, pw,
-                   pws, stream);
+  if (D.dtype == MOE_BF16 && (!aligned16(x) || !aligned16(w->w_g))) return MOE_ERR_UNSUPPORTED;
+  // router CTAs double as dispatch tiles: the router writes the per-tile counts
+  const int tiles = dispatch_tiles((long long)A, kRouterTokens * k);
+  int32_t* tile_counts = static_cast<int32_t*>(pw);
+  int32_t* tile_base = reinterpret_cast<int32_t*>(static_cast<char*>(pw) +
+                                                  align256((size_t)tiles * D.E * sizeof(int32_t)));
+  if (launch_router(x, w->w_g, w->bias, D.T, D.d, D.E, k, D.dtype == MOE_BF16, idx, tw, O.logits,
+                    nullptr, aux, s, tile_counts) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = dispatch_launch(x, idx, D.T, D.d, D.E, k, D.dtype, x_perm, counts, offsets, perm, inv_perm,
+                       tile_counts, tile_base, kRouterTokens * k, true, s);
   if (st != MOE_OK) return st;
   st = moe_experts_swiglu(x_perm, offsets, w->w_gate, w->w_up, w->w_down, (int)A, D.d, D.F, D.E,
                           D.dtype, h, y_perm, stream);

@@ -63,7 +63,8 @@ extern "C" moe_status moe_permute_noalloc(const void* x, const int32_t* topk_idx
   if ((dt == MOE_BF16 && d % 64 != 0) || (dt == MOE_F32 && d % 4 != 0)) return MOE_ERR_UNSUPPORTED;
   const long long A = (long long)T * k;
   if (A > INT32_MAX) return MOE_ERR_UNSUPPORTED;
-  const int tiles = dispatch_tiles(A);
+  constexpr int kTile = 2048;  // assignments per dispatch tile
+  const int tiles = dispatch_tiles(A, kTile);
   if ((size_t)tiles * (size_t)E > kNoAllocHalf) return MOE_ERR_WORKSPACE;  // beyond the fixed scratch
   if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
@@ -78,11 +79,7 @@ extern "C" moe_status moe_permute_noalloc(const void* x, const int32_t* topk_idx
   if (st != MOE_OK) return st;
   int32_t* tile_counts = scratch;
   int32_t* tile_base = scratch + kNoAllocHalf;
-  dispatch_hist_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile_counts);
-  dispatch_scan_kernel<<<1, MOE_MAX_EXPERTS, 0, s>>>(tile_counts, tiles, E, (int)A, tile_base,
-                                                     counts, offsets);
-  dispatch_scatter_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile_base, perm,
-                                                             inv_perm);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  return moe_gather_rows(x, perm, (int)A, k, T, d, dt, x_perm, stream);
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
+  return dispatch_launch(x, topk_idx, T, d, E, k, dt, x_perm, counts, offsets, perm, inv_perm,
+                         tile_counts, tile_base, kTile, false, s);
 }

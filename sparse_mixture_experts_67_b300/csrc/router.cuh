@@ -7,9 +7,12 @@
 //
 // One CTA owns 64 tokens (4 warps x 16).  The logits GEMM is narrow (N = E
 // <= 256), so bf16 runs on warp-level mma.sync m16n8k16 tiles fed by cp.async
-// through a 3-stage shared-memory ring; fp32 runs on FFMA.  The 64 x E logits
-// tile then goes through shared memory to a warp-per-token epilogue where the
-// lanes hold the experts: max / sum / arg-max are warp butterflies.
+// through a deep shared-memory ring (up to 6 stages, so enough bytes of x are
+// in flight to stream it at HBM speed); fp32 runs on FFMA.  The 64 x E logits
+// tile then goes through shared memory to a thread-per-token epilogue (no
+// cross-lane reductions on the critical path): each thread reduces its own
+// row for max and sum, and selects its top-k by repeated arg-max.  Outputs
+// and the aux column sums are written cooperatively, in a fixed order.
 #pragma once
 
 #include <float.h>
@@ -21,7 +24,6 @@ namespace moe {
 constexpr int kRouterTokens = 64;
 constexpr int kRouterThreads = 128;
 constexpr int kRouterBK = 64;
-constexpr int kRouterStages = 3;
 constexpr int kRouterLd = kRouterBK + 8;  // bf16 elements per smem row (pad: conflict-free)
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
@@ -43,122 +45,103 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, cons
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Warp-per-token epilogue over the logits tile S[64][ldS] (bias not yet added).
-// k == 0 writes logits only (expert-choice pre-pass).
-template <int NT>
-__device__ void router_epilogue(const float* S, int ldS, int tok0, int T, int E, int k,
+// Thread-per-token epilogue over the logits tile S[64][ldS] (bias not yet
+// added; S is modified).  k == 0 writes logits only (expert-choice pre-pass).
+// s_m / s_inv: 64 floats each of shared scratch; s_cnt: MOE_MAX_EXPERTS ints.
+// tile_counts (nullable): this CTA's row of per-expert selection counts, the
+// dispatch histogram of its 64*k assignments.
+__device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k,
                                 const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                                 float* __restrict__ w_out, float* __restrict__ logits_out,
                                 float* __restrict__ probs_out, float* __restrict__ aux_row,
-                                float* s_aux, int* s_sel_e, float* s_sel_g) {
-  constexpr int EPL = (8 * NT + 31) / 32;  // experts per lane
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float psum[EPL];
-#pragma unroll
-  for (int i = 0; i < EPL; ++i) psum[i] = 0.f;
-
-  for (int r = 0; r < 16; ++r) {
-    const int tl = warp * 16 + r;
-    const int t = tok0 + tl;
-    if (t >= T) break;  // warp-uniform
-    float v[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? S[tl * ldS + e] + (bias ? bias[e] : 0.f) : -FLT_MAX;
+                                int32_t* __restrict__ tile_counts, float* s_m, float* s_inv,
+                                int* s_cnt) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int ntok = min(kRouterTokens, T - tok0);
+  if (bias) {
+    for (int i = tid; i < ntok * E; i += nthr) {
+      const int r = i / E, e = i - r * E;
+      S[r * ldS + e] += bias[e];
     }
-    if (logits_out) {
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) logits_out[(size_t)t * E + e] = v[i];
-      }
-    }
-    if (k == 0) continue;
-    float m = v[0];
-#pragma unroll
-    for (int i = 1; i < EPL; ++i) m = fmaxf(m, v[i]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, off));
-    float ex[EPL];
+    __syncthreads();
+  }
+  if (k > 0 && tid < ntok) {
+    const float* row = S + tid * ldS;
+    float m = row[0];
+    for (int e = 1; e < E; ++e) m = fmaxf(m, row[e]);
     float sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      ex[i] = (e < E) ? expf(v[i] - m) : 0.f;
-      sum += ex[i];
+    for (int e = 0; e < E; ++e) sum += expf(row[e] - m);
+    s_m[tid] = m;
+    s_inv[tid] = 1.0f / sum;
+  }
+  __syncthreads();
+  // coalesced optional outputs: element i of the CTA's [ntok, E] block
+  if (logits_out || probs_out) {
+    const size_t base = (size_t)tok0 * E;
+    for (int i = tid; i < ntok * E; i += nthr) {
+      const int r = i / E, e = i - r * E;
+      const float v = S[r * ldS + e];
+      if (logits_out) logits_out[base + i] = v;
+      if (probs_out) probs_out[base + i] = expf(v - s_m[r]) * s_inv[r];
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(kFullMask, sum, off);
-    const float inv = 1.0f / sum;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      const float g = ex[i] * inv;
-      if (e < E) {
-        psum[i] += g;
-        if (probs_out) probs_out[(size_t)t * E + e] = g;
-      }
+  }
+  if (k == 0) return;
+  if (tile_counts)
+    for (int e = tid; e < E; e += nthr) s_cnt[e] = 0;
+  if (aux_row) {  // fixed-order column sums of g over this CTA's tokens
+    for (int e = tid; e < E; e += nthr) {
+      float acc = 0.f;
+      for (int r = 0; r < ntok; ++r) acc += expf(S[r * ldS + e] - s_m[r]) * s_inv[r];
+      aux_row[e] = acc;
     }
-    // top-k by repeated warp arg-max on the logits: larger value, then lower index
-    unsigned taken = 0;
+  }
+  __syncthreads();  // the top-k below overwrites selected entries of S
+  if (tid < ntok) {
+    float* row = S + tid * ldS;
+    const float m = s_m[tid], inv = s_inv[tid];
+    const int t = tok0 + tid;
     float selsum = 0.f;
     for (int j = 0; j < k; ++j) {
       float best = 0.f;
       int bi = -1;
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (bi < 0 || v[i] > best)) {
-          best = v[i];
+      for (int e = 0; e < E; ++e) {  // ascending e + strict '>' keeps the lower index on ties
+        const float v = row[e];
+        if (bi < 0 ? v > -INFINITY : v > best) {
+          best = v;
           bi = e;
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(kFullMask, best, off);
-        const int oi = __shfl_xor_sync(kFullMask, bi, off);
-        if (oi >= 0 && (bi < 0 || ov > best || (ov == best && oi < bi))) {
-          best = ov;
-          bi = oi;
-        }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      const float gsel = expf(best - m) * inv;  // same arithmetic as the owner's g
+      row[bi] = -INFINITY;  // taken (logits are finite)
+      const float gsel = expf(best - m) * inv;  // same arithmetic as probs
       selsum += gsel;
-      if (lane == 0) {
-        s_sel_e[warp * MOE_MAX_EXPERTS + j] = bi;
-        s_sel_g[warp * MOE_MAX_EXPERTS + j] = gsel;
-      }
+      idx_out[(size_t)t * k + j] = bi;
+      w_out[(size_t)t * k + j] = gsel;
+      if (tile_counts) atomicAdd(&s_cnt[bi], 1);
     }
-    __syncwarp();
     const float rs = 1.0f / selsum;
-    for (int j = lane; j < k; j += 32) {
-      idx_out[(size_t)t * k + j] = s_sel_e[warp * MOE_MAX_EXPERTS + j];
-      w_out[(size_t)t * k + j] = s_sel_g[warp * MOE_MAX_EXPERTS + j] * rs;
-    }
-    __syncwarp();
+    for (int j = 0; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
   }
-  if (aux_row != nullptr) {
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E) s_aux[warp * MOE_MAX_EXPERTS + e] = psum[i];
-    }
+  if (tile_counts) {
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-      aux_row[e] = ((s_aux[e] + s_aux[MOE_MAX_EXPERTS + e]) + s_aux[2 * MOE_MAX_EXPERTS + e]) +
-                   s_aux[3 * MOE_MAX_EXPERTS + e];
+    for (int e = tid; e < E; e += nthr) tile_counts[(size_t)blockIdx.x * E + e] = s_cnt[e];
   }
+}
+
+// Pipeline depth: up to 6 stages within ~200 KB of shared memory.
+template <int NT>
+constexpr int router_stages() {
+  constexpr size_t stage = (size_t)(kRouterTokens + 8 * NT) * kRouterLd * 2;
+  constexpr size_t fit = (200u * 1024u) / stage;
+  return fit >= 6 ? 6 : (fit < 2 ? 2 : (int)fit);
 }
 
 // Shared memory: max(stage ring, logits tile) + epilogue scratch.
 template <int NT>
 constexpr size_t router_smem_bytes_bf16() {
-  constexpr size_t ring = (size_t)kRouterStages * (kRouterTokens + 8 * NT) * kRouterLd * 2;
+  constexpr size_t ring = (size_t)router_stages<NT>() * (kRouterTokens + 8 * NT) * kRouterLd * 2;
   constexpr size_t tile = (size_t)kRouterTokens * (8 * NT + 1) * 4;
   constexpr size_t main = ring > tile ? ring : tile;
-  return main + 4 * MOE_MAX_EXPERTS * (4 + 4 + 4);
+  return main + 2 * kRouterTokens * 4 + MOE_MAX_EXPERTS * 4;
 }
 
 template <int NT>
@@ -167,17 +150,18 @@ __global__ void __launch_bounds__(kRouterThreads)
                        const float* __restrict__ bias, int T, int d, int E, int k,
                        int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                        float* __restrict__ logits_out, float* __restrict__ probs_out,
-                       float* __restrict__ aux_partials) {
+                       float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts) {
   constexpr int EP = 8 * NT;
   extern __shared__ __align__(16) unsigned char smem[];
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
   constexpr int stage_elems = (kRouterTokens + EP) * kRouterLd;
-  constexpr size_t ring_bytes = (size_t)kRouterStages * stage_elems * 2;
+  constexpr int STAGES = router_stages<NT>();
+  constexpr size_t ring_bytes = (size_t)STAGES * stage_elems * 2;
   constexpr size_t tile_bytes = (size_t)kRouterTokens * (EP + 1) * 4;
   constexpr size_t main_bytes = ring_bytes > tile_bytes ? ring_bytes : tile_bytes;
-  float* s_aux = reinterpret_cast<float*>(smem + main_bytes);
-  int* s_sel_e = reinterpret_cast<int*>(s_aux + 4 * MOE_MAX_EXPERTS);
-  float* s_sel_g = reinterpret_cast<float*>(s_sel_e + 4 * MOE_MAX_EXPERTS);
+  float* s_m = reinterpret_cast<float*>(smem + main_bytes);
+  float* s_inv = s_m + kRouterTokens;
+  int* s_cnt = reinterpret_cast<int*>(s_inv + kRouterTokens);
 
   const int tok0 = blockIdx.x * kRouterTokens;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -209,20 +193,20 @@ __global__ void __launch_bounds__(kRouterThreads)
     for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
 
 #pragma unroll
-  for (int s = 0; s < kRouterStages - 1; ++s) {
+  for (int s = 0; s < STAGES - 1; ++s) {
     if (s < nk) load_stage(s, s);
     cp_async_commit();
   }
   const int g = lane >> 2, c4 = lane & 3;
   for (int kc = 0; kc < nk; ++kc) {
-    cp_async_wait<kRouterStages - 2>();
+    cp_async_wait<STAGES - 2>();
     __syncthreads();
     {
-      const int nxt = kc + kRouterStages - 1;
-      if (nxt < nk) load_stage(nxt % kRouterStages, nxt);
+      const int nxt = kc + STAGES - 1;
+      if (nxt < nk) load_stage(nxt % STAGES, nxt);
       cp_async_commit();
     }
-    const __nv_bfloat16* xs = ring + (kc % kRouterStages) * stage_elems;
+    const __nv_bfloat16* xs = ring + (kc % STAGES) * stage_elems;
     const __nv_bfloat16* ws = xs + kRouterTokens * kRouterLd;
     const __nv_bfloat16* xw = xs + warp * 16 * kRouterLd;
 #pragma unroll
@@ -257,9 +241,9 @@ __global__ void __launch_bounds__(kRouterThreads)
     S[(r0 + 8) * ldS + col + 1] = acc[n][3];
   }
   __syncthreads();
-  router_epilogue<NT>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
-                      aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, s_aux,
-                      s_sel_e, s_sel_g);
+  router_epilogue(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
+                  aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts, s_m,
+                  s_inv, s_cnt);
 }
 
 // fp32 router: FFMA over 32-wide d chunks, same epilogue.
@@ -269,7 +253,7 @@ constexpr size_t router_smem_bytes_f32() {
   constexpr size_t ld = kRouterBKf + 1;
   constexpr size_t tiles = (size_t)(kRouterTokens + 8 * NT) * ld * 4;
   constexpr size_t acc = (size_t)kRouterTokens * (8 * NT + 1) * 4;
-  return tiles + acc + 4 * MOE_MAX_EXPERTS * 12;
+  return tiles + acc + 2 * kRouterTokens * 4 + MOE_MAX_EXPERTS * 4;
 }
 
 template <int NT>
@@ -278,7 +262,7 @@ __global__ void __launch_bounds__(kRouterThreads)
                       const float* __restrict__ bias, int T, int d, int E, int k,
                       int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                       float* __restrict__ logits_out, float* __restrict__ probs_out,
-                      float* __restrict__ aux_partials) {
+                      float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts) {
   constexpr int EP = 8 * NT;
   constexpr int ld = kRouterBKf + 1;
   constexpr int ldS = EP + 1;
@@ -286,9 +270,9 @@ __global__ void __launch_bounds__(kRouterThreads)
   float* xs = reinterpret_cast<float*>(smem);
   float* ws = xs + kRouterTokens * ld;
   float* S = ws + EP * ld;
-  float* s_aux = S + kRouterTokens * ldS;
-  int* s_sel_e = reinterpret_cast<int*>(s_aux + 4 * MOE_MAX_EXPERTS);
-  float* s_sel_g = reinterpret_cast<float*>(s_sel_e + 4 * MOE_MAX_EXPERTS);
+  float* s_m = S + kRouterTokens * ldS;
+  float* s_inv = s_m + kRouterTokens;
+  int* s_cnt = reinterpret_cast<int*>(s_inv + kRouterTokens);
   const int tok0 = blockIdx.x * kRouterTokens;
   // thread -> (token, expert parity): token = tid % 64, experts tid/64 + 2*i
   const int tt = threadIdx.x & 63, eh = threadIdx.x >> 6;
@@ -317,9 +301,9 @@ __global__ void __launch_bounds__(kRouterThreads)
 #pragma unroll
   for (int i = 0; i < 4 * NT; ++i) S[tt * ldS + eh + 2 * i] = acc[i];
   __syncthreads();
-  router_epilogue<NT>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
-                      aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, s_aux,
-                      s_sel_e, s_sel_g);
+  router_epilogue(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
+                  aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts, s_m,
+                  s_inv, s_cnt);
 }
 
 inline int router_nt(int E) {
@@ -331,7 +315,7 @@ inline int router_nt(int E) {
 template <int NT>
 cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, int T, int d, int E,
                              int k, bool bf16, int32_t* idx, float* w, float* logits, float* probs,
-                             float* aux, cudaStream_t st) {
+                             float* aux, int32_t* tile_counts, cudaStream_t st) {
   const int grid = ceil_div(T, kRouterTokens);
   if (bf16) {
     const size_t sm = router_smem_bytes_bf16<NT>();
@@ -340,7 +324,7 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     if (e != cudaSuccess) return e;
     router_bf16_kernel<NT><<<grid, kRouterThreads, sm, st>>>(
         static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wg), bias, T, d,
-        E, k, idx, w, logits, probs, aux);
+        E, k, idx, w, logits, probs, aux, tile_counts);
   } else {
     const size_t sm = router_smem_bytes_f32<NT>();
     cudaError_t e = cudaFuncSetAttribute(router_f32_kernel<NT>,
@@ -348,21 +332,22 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     if (e != cudaSuccess) return e;
     router_f32_kernel<NT><<<grid, kRouterThreads, sm, st>>>(
         static_cast<const float*>(x), static_cast<const float*>(wg), bias, T, d, E, k, idx, w,
-        logits, probs, aux);
+        logits, probs, aux, tile_counts);
   }
   return cudaGetLastError();
 }
 
 inline cudaError_t launch_router(const void* x, const void* wg, const float* bias, int T, int d,
                                  int E, int k, bool bf16, int32_t* idx, float* w, float* logits,
-                                 float* probs, float* aux, cudaStream_t st) {
+                                 float* probs, float* aux, cudaStream_t st,
+                                 int32_t* tile_counts = nullptr) {
   switch (router_nt(E)) {
-    case 1: return launch_router_nt<1>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
-    case 2: return launch_router_nt<2>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
-    case 4: return launch_router_nt<4>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
-    case 8: return launch_router_nt<8>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
-    case 16: return launch_router_nt<16>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
-    default: return launch_router_nt<32>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st);
+    case 1: return launch_router_nt<1>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
+    case 2: return launch_router_nt<2>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
+    case 4: return launch_router_nt<4>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
+    case 8: return launch_router_nt<8>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
+    case 16: return launch_router_nt<16>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
+    default: return launch_router_nt<32>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
   }
 }
 
