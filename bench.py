@@ -270,7 +270,9 @@ def run_gpu(args, cfg):
 def launches_per_step(cfg) -> int:
     if cfg.routing == "expert_choice":
         return 7  # logits, EC select, offsets, gather, gate/up, down, EC combine
-    return 7  # router (+ dispatch counts), scan, scatter + row copy, gate/up, down, combine, aux
+    if cfg.dtype == "bf16" and cfg.k <= 2:
+        return 4  # router (+ dispatch counts), scatter (+ scan, aux, y = 0), gate/up, down + combine
+    return 5  # router (+ dispatch counts), scatter (+ scan, aux), gate/up, down, combine
 
 
 def stage_breakdown(moe, torch, cfg, x, w, flush, stream, steps):

@@ -131,8 +131,8 @@ moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int
  * counterpart; this exists for callers that cannot provide device scratch:
  * plugin hosts that give a kernel only its input and output buffers, and
  * deployments whose device memory is reserved up front by another allocator,
- * so that nothing may call cudaMalloc while they run.  The scratch (per-tile
- * expert counts and their scanned bases) lives in a fixed array of
+ * so that nothing may call cudaMalloc while they run.  The scratch (the
+ * per-tile expert counts) lives in a fixed array of
  * MOE_PERMUTE_NOALLOC_SCRATCH_BYTES inside the library's device memory, held
  * by every GPU that loads the library until the process exits.
  *   Limit: ceil(T*k / 2048) * E <= MOE_PERMUTE_NOALLOC_SCRATCH_BYTES / 8
@@ -169,6 +169,19 @@ moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, in
 moe_status moe_grouped_gateup_swiglu(const void* x_perm, const int32_t* offsets,
                                      const void* w_gate, const void* w_up, int R, int d, int F,
                                      int E, moe_dtype dt, void* h, moe_stream_t stream);
+/* Gate/up with the dispatch gather fused into the operand load: row r of the
+ * grouped input is x[src[r] / div, :] of x [T,d], so x_perm is never written.
+ * src = perm from moe_permute (div = k), or the expert-choice ec_idx (div = 1).
+ * Bit-identical to moe_permute / moe_gather_rows followed by
+ * moe_grouped_gateup_swiglu.  bf16 only (MOE_ERR_UNSUPPORTED otherwise);
+ * src values must lie in [0, T*div).  It saves the R x d x_perm buffer but is
+ * slower when the GEMM is compute-bound: each 128-row block is re-gathered
+ * (TMA gather4, 128-byte rows) for every n-block, where the contiguous path
+ * loads 16 KiB boxes; moe_layer_forward therefore materialises x_perm.      */
+moe_status moe_grouped_gateup_swiglu_gather(const void* x, const int32_t* src, int div, int T,
+                                            const int32_t* offsets, const void* w_gate,
+                                            const void* w_up, int R, int d, int F, int E,
+                                            moe_dtype dt, void* h, moe_stream_t stream);
 moe_status moe_grouped_down(const void* h, const int32_t* offsets, const void* w_down, int R,
                             int d, int F, int E, moe_dtype dt, float* y_perm,
                             moe_stream_t stream);

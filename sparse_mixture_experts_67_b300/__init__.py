@@ -20,6 +20,7 @@ import torch
 __all__ = [
     "MoEError", "lib", "declared_symbols", "moe_route", "moe_expert_choice_route",
     "moe_expert_choice_capacity", "moe_permute", "moe_permute_noalloc", "moe_gather_rows", "moe_grouped_gateup_swiglu",
+    "moe_grouped_gateup_swiglu_gather",
     "moe_grouped_down", "moe_experts_swiglu", "moe_combine", "moe_ec_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_layer_workspace_size", "moe_route_aux_rows", "moe_device_error",
     "MoELayer",
@@ -74,6 +75,8 @@ _SIGS = {
     "moe_gather_rows": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "moe_permute_noalloc": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_grouped_gateup_swiglu": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "moe_grouped_gateup_swiglu_gather": ([_P, _P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P],
+                                         _I),
     "moe_grouped_down": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "moe_experts_swiglu": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
@@ -266,6 +269,21 @@ def moe_grouped_gateup_swiglu(x_perm: torch.Tensor, offsets: torch.Tensor, w_gat
     _check("moe_grouped_gateup_swiglu", lib().moe_grouped_gateup_swiglu(
         _ptr(x_perm), _ptr(offsets), _ptr(w_gate), _ptr(w_up), R, d, F, E, _dtype(x_perm), _ptr(h),
         _stream()))
+    return h
+
+
+def moe_grouped_gateup_swiglu_gather(x: torch.Tensor, src: torch.Tensor, div: int,
+                                     offsets: torch.Tensor, w_gate: torch.Tensor,
+                                     w_up: torch.Tensor) -> torch.Tensor:
+    """Gate/up + SwiGLU reading row r of the grouped input from x[src[r] // div]."""
+    _dev(x, src, offsets, w_gate, w_up)
+    T, d = x.shape
+    R = src.numel()
+    E, F, _ = w_gate.shape
+    h = _empty((R, F), x.dtype, x)
+    _check("moe_grouped_gateup_swiglu_gather", lib().moe_grouped_gateup_swiglu_gather(
+        _ptr(x), _ptr(src), div, T, _ptr(offsets), _ptr(w_gate), _ptr(w_up), R, d, F, E, _dtype(x),
+        _ptr(h), _stream()))
     return h
 
 

@@ -10,12 +10,10 @@
 //   hist:    per-tile expert counts with warp-aggregated shared-memory
 //            atomics (match_any + popc); in the layer the router's epilogue
 //            produces them instead;
-//   scan:    one CTA turns the [tiles, E] count matrix into per-(tile, expert)
-//            bases and the expert offsets, with warp scans over the tiles;
-//   scatter: each tile re-reads its assignments in order and ranks them among
-//            equal experts (warp match_any rank + per-warp counts in shared
-//            memory), giving perm / inv_perm bit-exactly, then its warps copy
-//            the x rows of the round into the dispatch order (16-byte vectors).
+//   scatter: each tile derives its per-expert bases from the count matrix,
+//            re-reads its assignments in order and ranks them among equal
+//            experts (warp match_any rank + per-warp counts in shared memory),
+//            giving perm / inv_perm bit-exactly.
 #pragma once
 
 #include "common.cuh"
@@ -24,7 +22,6 @@ namespace moe {
 
 constexpr int kDispatchThreads = 256;
 constexpr int kDispatchWarps = kDispatchThreads / 32;
-constexpr int kScanThreads = 1024;
 
 inline int dispatch_tiles(long long A, int tile) { return A == 0 ? 0 : ceil_div(A, tile); }
 
@@ -48,22 +45,52 @@ __global__ void __launch_bounds__(kDispatchThreads)
   for (int e = threadIdx.x; e < E; e += blockDim.x) tile_counts[(size_t)blockIdx.x * E + e] = cnt[e];
 }
 
-// One CTA.  tile_base[t][e] = offsets[e] + sum of tile_counts[t'][e] over t' < t.
-__global__ void __launch_bounds__(kScanThreads)
-    dispatch_scan_kernel(const int32_t* __restrict__ tile_counts, int tiles, int E, int A,
-                         int32_t* __restrict__ tile_base, int32_t* __restrict__ counts,
-                         int32_t* __restrict__ offsets) {
+// Ranks each assignment of its tile among equal experts and writes perm /
+// inv_perm.  The tile's first dispatch row per expert comes from the count
+// matrix directly: every CTA reduces the [tiles, E] counts itself (totals,
+// and the sum over the tiles before its own), warp per expert, lanes over
+// tiles; the expert offsets are the exclusive scan of the totals.  CTA 0 also
+// writes counts / offsets and, given aux_partials, the load-balancing
+// statistics (same reduction order as aux_finalize_kernel).  Optional extras:
+// x != nullptr copies x[a / k] into x_perm[row] (16-byte vectors, warp per
+// row); y_zero != nullptr zeroes the y rows of the tile's tokens
+// (tokens_per_tile of them) for an accumulating combine downstream.
+__global__ void __launch_bounds__(kDispatchThreads)
+    dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E, int k, int tile,
+                            const int32_t* __restrict__ tile_counts, int tiles,
+                            int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
+                            int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                            const uint4* __restrict__ x, int vec_per_row, uint4* __restrict__ x_perm,
+                            const float* __restrict__ aux_partials, int T, float* __restrict__ f,
+                            float* __restrict__ p, float* __restrict__ loss,
+                            float4* __restrict__ y_zero, int d4, int tokens_per_tile) {
+  __shared__ int running[MOE_MAX_EXPERTS];
   __shared__ int s_tot[MOE_MAX_EXPERTS];
-  __shared__ int s_off[MOE_MAX_EXPERTS];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int nwarps = kScanThreads / 32;
-  for (int e = warp; e < E; e += nwarps) {
-    int acc = 0;
-    for (int t = lane; t < tiles; t += 32) acc += tile_counts[(size_t)t * E + e];
+  __shared__ int wcnt[kDispatchWarps][MOE_MAX_EXPERTS];
+  __shared__ int s_row[kDispatchThreads];
+  __shared__ int s_tok[kDispatchThreads];
+  __shared__ float s_fp[MOE_MAX_EXPERTS];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int me = blockIdx.x;
+  for (int e = warp; e < E; e += kDispatchWarps) {
+    int tot = 0, pre = 0;
+    for (int t = lane; t < tiles; t += 32) {
+      const int c = tile_counts[(size_t)t * E + e];
+      tot += c;
+      pre += t < me ? c : 0;
+    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
-    if (lane == 0) s_tot[e] = acc;
+    for (int off = 16; off > 0; off >>= 1) {
+      tot += __shfl_xor_sync(kFullMask, tot, off);
+      pre += __shfl_xor_sync(kFullMask, pre, off);
+    }
+    if (lane == 0) {
+      s_tot[e] = tot;
+      running[e] = pre;
+    }
   }
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    for (int w = 0; w < kDispatchWarps; ++w) wcnt[w][e] = 0;
   __syncthreads();
   if (warp == 0) {  // exclusive scan of the (<= 256) totals: 8 per lane, then a warp scan
     constexpr int per = MOE_MAX_EXPERTS / 32;
@@ -77,59 +104,33 @@ __global__ void __launch_bounds__(kScanThreads)
     int incl = run;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int n = __shfl_up_sync(kFullMask, incl, off);
-      if (lane >= off) incl += n;
+      const int nb = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += nb;
     }
     int ex = incl - run;
 #pragma unroll
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
-      if (e < E) s_off[e] = ex;
+      if (e < E) {
+        if (me == 0) {
+          counts[e] = v[i];
+          offsets[e] = ex;
+        }
+        running[e] += ex;
+      }
       ex += v[i];
     }
+    if (me == 0 && lane == 31) offsets[E] = A;
+  }
+  if (y_zero != nullptr) {
+    const int tk0 = me * tokens_per_tile;
+    const int tk1 = min(T, tk0 + tokens_per_tile);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (size_t i = (size_t)tk0 * d4 + threadIdx.x; i < (size_t)tk1 * d4; i += blockDim.x) y_zero[i] = z;
   }
   __syncthreads();
-  for (int e = warp; e < E; e += nwarps) {
-    int running = s_off[e];
-    for (int t0 = 0; t0 < tiles; t0 += 32) {
-      const int t = t0 + lane;
-      const int v = t < tiles ? tile_counts[(size_t)t * E + e] : 0;
-      int incl = v;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int n = __shfl_up_sync(kFullMask, incl, off);
-        if (lane >= off) incl += n;
-      }
-      if (t < tiles) tile_base[(size_t)t * E + e] = running + incl - v;
-      running += __shfl_sync(kFullMask, incl, 31);
-    }
-    if (lane == 0) {
-      counts[e] = s_tot[e];
-      offsets[e] = s_off[e];
-    }
-  }
-  if (threadIdx.x == 0) offsets[E] = A;
-}
-
-// Ranks each assignment among equal experts of its tile and writes perm /
-// inv_perm; with x != nullptr it also copies x[a / k] into x_perm[row].
-__global__ void __launch_bounds__(kDispatchThreads)
-    dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E, int k, int tile,
-                            const int32_t* __restrict__ tile_base, int32_t* __restrict__ perm,
-                            int32_t* __restrict__ inv_perm, const uint4* __restrict__ x,
-                            int vec_per_row, uint4* __restrict__ x_perm) {
-  __shared__ int running[MOE_MAX_EXPERTS];
-  __shared__ int wcnt[kDispatchWarps][MOE_MAX_EXPERTS];
-  __shared__ int s_row[kDispatchThreads];
-  __shared__ int s_tok[kDispatchThreads];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    running[e] = tile_base[(size_t)blockIdx.x * E + e];
-    for (int w = 0; w < kDispatchWarps; ++w) wcnt[w][e] = 0;
-  }
-  __syncthreads();
-  const int a0 = blockIdx.x * tile;
+  const int a0 = me * tile;
   const int a1 = min(A, a0 + tile);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int base = a0; base < a1; base += kDispatchThreads) {
     const int a = base + threadIdx.x;
     const bool valid = a < a1;
@@ -148,13 +149,13 @@ __global__ void __launch_bounds__(kDispatchThreads)
     }
     __syncthreads();
     for (int ee = threadIdx.x; ee < E; ee += blockDim.x) {
-      int s = 0;
+      int sum = 0;
 #pragma unroll
       for (int w = 0; w < kDispatchWarps; ++w) {
-        s += wcnt[w][ee];
+        sum += wcnt[w][ee];
         wcnt[w][ee] = 0;
       }
-      running[ee] += s;
+      running[ee] += sum;
     }
     if (x != nullptr) {  // copy this round's rows, one warp per row
       const int nvalid = min(kDispatchThreads, a1 - base);
@@ -175,6 +176,29 @@ __global__ void __launch_bounds__(kDispatchThreads)
     }
     __syncthreads();
   }
+  if (me != 0 || aux_partials == nullptr) return;
+  // CTA 0: aux statistics from the router's per-tile partial sums of g
+  for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) s_fp[e] = 0.f;
+  __syncthreads();
+  for (int e = warp; e < E; e += kDispatchWarps) {
+    float acc = 0.f;
+    for (int r = lane; r < tiles; r += 32) acc += aux_partials[(size_t)r * E + e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+    if (lane == 0) {
+      const float pe = acc / (float)T;
+      const float fe = (float)s_tot[e] / (float)T;
+      if (p) p[e] = pe;
+      if (f) f[e] = fe;
+      s_fp[e] = fe * pe;
+    }
+  }
+  __syncthreads();
+  for (int off = MOE_MAX_EXPERTS / 2; off > 0; off >>= 1) {
+    for (int e = threadIdx.x; e < off; e += blockDim.x) s_fp[e] += s_fp[e + off];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0 && loss) *loss = (float)E * s_fp[0];
 }
 
 // x_perm[r,:] = x[src[r] / div, :]; one warp per row, 16-byte vectors.

@@ -18,13 +18,15 @@
 //              or plain fp32, vector stores masked at the segment end.
 // For gate/up the B tile stacks 128 rows of W_gate over the same 128 rows of
 // W_up, so one N=256 instruction produces both halves of the SwiGLU.
-// Tiles are (expert, 128-row block, n-block), enumerated on the device from
-// the offsets; CTAs stride over them.  Every barrier wait is bounded in time:
+// Tiles are (expert, n-block, 128-row block), enumerated on the device from
+// the offsets with the row block fastest; CTAs stride over them.  Every barrier wait is bounded in time:
 // on expiry the kernel records a code in the device error word, drains its
 // in-flight copies and MMAs, frees TMEM and returns.
 #pragma once
 
 #include <cuda.h>
+
+#include <stdlib.h>
 
 #include <algorithm>
 
@@ -33,17 +35,24 @@
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int kThreads = 192;
-constexpr int kEpilogueWarp0 = 2;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KiB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t TMEM_COLS = 512;  // two 256-column fp32 accumulators
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;
 // error-word codes
 constexpr uint32_t kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain = 8u;
 
+// Per-width constants: BN is the MMA N (output columns for down; gate + up
+// halves for gate/up).  Narrow tiles leave room for more stages in flight.
+template <int BN>
+struct Cfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (192 * 1024) / STAGE_BYTES > 8 ? 8 : (192 * 1024) / STAGE_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
+};
+
+template <int STAGES>
 struct Smem {  // lives after the 1024-aligned stage ring
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -55,7 +64,11 @@ struct Smem {  // lives after the 1024-aligned stage ring
   int cum[MOE_MAX_EXPERTS + 1];  // prefix of 128-row blocks per expert
   int off[MOE_MAX_EXPERTS + 1];  // segment offsets
 };
-constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + sizeof(Smem) + 1024;
+
+template <int BN>
+constexpr size_t smem_bytes() {
+  return (size_t)Cfg<BN>::STAGES * Cfg<BN>::STAGE_BYTES + sizeof(Smem<Cfg<BN>::STAGES>) + 1024;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -112,6 +125,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
       "%3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Four rows r0..r3 (64 columns from x) of a 2-D tensor whose map has a
+// one-row box, written as four consecutive 128-byte rows at dst.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -178,18 +203,24 @@ struct TileCoord {
   int e, row0, row_end, nt;
 };
 
-__device__ __forceinline__ TileCoord map_tile(const Smem& S, int E, int n_tiles, int tile) {
+// Tiles are enumerated expert by expert; inside an expert the 128-row block
+// varies fastest and the n-block slowest, so the CTAs of one wave share each
+// weight tile (read from HBM once) while the expert's rows stay in L2.
+template <class SmemT>
+__device__ __forceinline__ TileCoord map_tile(const SmemT& S, int E, int n_tiles, int tile) {
   TileCoord c;
-  const int mt = tile / n_tiles;
-  c.nt = tile - mt * n_tiles;
-  int lo = 0, hi = E;  // S.cum[lo] <= mt < S.cum[hi]
+  int lo = 0, hi = E;  // S.cum[lo] * n_tiles <= tile < S.cum[hi] * n_tiles
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (S.cum[mid] <= mt) lo = mid;
+    if (S.cum[mid] * n_tiles <= tile) lo = mid;
     else hi = mid;
   }
+  const int m_tiles = S.cum[lo + 1] - S.cum[lo];
+  const int local = tile - S.cum[lo] * n_tiles;
+  const int nt = local / m_tiles;
   c.e = lo;
-  c.row0 = S.off[lo] + (mt - S.cum[lo]) * BM;
+  c.nt = nt;
+  c.row0 = S.off[lo] + (local - nt * m_tiles) * BM;
   c.row_end = S.off[lo + 1];
   return c;
 }
@@ -201,17 +232,33 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// GATEUP: out = bf16 H [R, N] (N = F), B rows from two maps (gate, up), 128 each.
-// !GATEUP: out = fp32 Y [R, N] (N = d), B rows from one map, 256 per tile.
-template <bool GATEUP>
+// GATEUP: out = bf16 H [R, N] (N = F), B rows from two maps (gate, up), BN/2 each.
+// !GATEUP: out = fp32 Y [R, N] (N = d), B rows from one map, BN per tile.
+// COMBINE (down only): instead of Y, row r adds topk_w[a] * Y[r,:] into
+// out = y [T, N] (zeroed beforehand) at token a / kslots, a = perm[r], with
+// float4 atomics.  With kslots <= 2 every element of y receives at most two
+// additions onto zero, so the sum is the same in either order: deterministic.
+// GATHER (gate/up only): row r of A is row gsrc[r] / gdiv of the tensor behind
+// tmA (x itself, mapped with a one-row box) instead of row r; each producer
+// lane brings 4 of the tile's 128 rows per k-block with one TMA gather4.
+template <bool GATEUP, int BN, bool COMBINE = false, bool GATHER = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets,
-                      int R, int E, int N, int K, void* __restrict__ out) {
+                      int R, int E, int N, int K, void* __restrict__ out,
+                      const int32_t* __restrict__ perm = nullptr,
+                      const float* __restrict__ topk_w = nullptr, int kslots = 1,
+                      const __nv_bfloat16* __restrict__ gx = nullptr,
+                      const int32_t* __restrict__ gsrc = nullptr, int gdiv = 1) {
+  constexpr int STAGES = Cfg<BN>::STAGES;
+  constexpr int STAGE_BYTES = Cfg<BN>::STAGE_BYTES;
+  constexpr int B_BYTES = Cfg<BN>::B_BYTES;
+  constexpr uint32_t TMEM_COLS = Cfg<BN>::TMEM_COLS;
+  using SmemT = Smem<STAGES>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* ring = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Smem& S = *reinterpret_cast<Smem*>(ring + (size_t)STAGES * STAGE_BYTES);
+  SmemT& S = *reinterpret_cast<SmemT*>(ring + (size_t)STAGES * STAGE_BYTES);
   volatile int* abort_flag = &S.abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -262,24 +309,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (GATHER || lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_phase = 0;  // per-stage bits: loads issued, their parity
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
         const TileCoord c = map_tile(S, E, n_tiles, tile);
         const int brow = c.e * N + c.nt * kTileN;
+        int tok[4] = {0, 0, 0, 0};  // GATHER: source rows of tile rows 4 * lane + i
+        if (GATHER) {               // (rows past the segment read row 0; never stored)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = c.row0 + 4 * lane + i;
+            tok[i] = r < c.row_end ? gsrc[r] / gdiv : 0;
+          }
+        }
+        bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, kErrProducer)) break;
+          int go = 1;
+          if (lane == 0) go = mbar_wait(&S.empty[stage], phase ^ 1u, abort_flag, kErrProducer);
+          if (GATHER) go = __shfl_sync(kFullMask, go, 0);
+          if (!go) {
+            ok = false;
+            break;
+          }
           unsigned char* sA = ring + (size_t)stage * STAGE_BYTES;
           unsigned char* sB = sA + A_BYTES;
-          mbar_arrive_expect_tx(&S.full[stage], STAGE_BYTES);
-          tma_load_2d(sA, &tmA, &S.full[stage], kb * BK, c.row0);
-          if (GATEUP) {
-            tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
-            tma_load_2d(sB + B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, brow);
-          } else {
-            tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
+          if (lane == 0) mbar_arrive_expect_tx(&S.full[stage], STAGE_BYTES);
+          if (GATHER) {
+            __syncwarp();  // the expected byte count is set before any gather lands
+            tma_gather4(sA + lane * 4 * 128, &tmA, &S.full[stage], kb * BK, tok[0], tok[1], tok[2],
+                        tok[3]);
+          }
+          if (lane == 0) {
+            if (!GATHER) tma_load_2d(sA, &tmA, &S.full[stage], kb * BK, c.row0);
+            if (GATEUP) {
+              tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
+              tma_load_2d(sB + B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, brow);
+            } else {
+              tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
+            }
           }
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -288,17 +357,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
         }
+        if (!ok) break;
       }
       // drain: every issued load must have landed before the CTA may exit
-      for (int s = 0; s < STAGES; ++s) {
-        if (!((issued >> s) & 1u)) continue;
-        const uint32_t a = smem_u32(&S.full[s]);
-        const uint32_t par = (issued_phase >> s) & 1u;
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(a, par)) {
-          if (global_timer_ns() - t0 > kWaitTimeoutNs) {
-            record_error(kErrDrain);
-            break;
+      if (lane == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+          if (!((issued >> s) & 1u)) continue;
+          const uint32_t a = smem_u32(&S.full[s]);
+          const uint32_t par = (issued_phase >> s) & 1u;
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(a, par)) {
+            if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+              record_error(kErrDrain);
+              break;
+            }
           }
         }
       }
@@ -390,6 +462,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
           }
         }
+      } else if (COMBINE) {
+        const int a = valid ? perm[row] : 0;
+        const float wgt = valid ? topk_w[a] : 0.f;
+        float* yrow = static_cast<float*>(out) + (size_t)(a / kslots) * N;
+#pragma unroll 1
+        for (int cc = 0; cc < kTileN; cc += 32) {
+          uint32_t v[32];
+          MOE_TMEM_LD32(taddr + cc, v);
+          tmem_ld_wait();
+          if (valid && n0 + cc < N) {
+            float4* dst = reinterpret_cast<float4*>(yrow + n0 + cc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              atomicAdd(dst + i, make_float4(wgt * __uint_as_float(v[4 * i]),
+                                             wgt * __uint_as_float(v[4 * i + 1]),
+                                             wgt * __uint_as_float(v[4 * i + 2]),
+                                             wgt * __uint_as_float(v[4 * i + 3])));
+          }
+        }
       } else {
         float* Y = static_cast<float*>(out);
 #pragma unroll 1
@@ -467,17 +558,49 @@ inline int sm_count() {
   return n;
 }
 
-template <bool GATEUP>
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                   const int32_t* offsets, int R, int E, int N, int K, void* out, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel<GATEUP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+template <bool GATEUP, int BN, bool COMBINE = false, bool GATHER = false>
+cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                      const int32_t* offsets, int R, int E, int N, int K, void* out, int sms,
+                      cudaStream_t s, const int32_t* perm = nullptr, const float* topk_w = nullptr,
+                      int kslots = 1, const __nv_bfloat16* gx = nullptr,
+                      const int32_t* gsrc = nullptr, int gdiv = 1) {
+  constexpr size_t sm = smem_bytes<BN>();
+  cudaError_t e = cudaFuncSetAttribute(grouped_tc_kernel<GATEUP, BN, COMBINE, GATHER>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   constexpr int tile_n = GATEUP ? BN / 2 : BN;
   const long long max_tiles = (long long)((R + BM - 1) / BM + E) * ((N + tile_n - 1) / tile_n);
-  const int grid = (int)std::min<long long>(sm_count(), max_tiles);
-  grouped_tc_kernel<GATEUP><<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, offsets, R, E, N, K, out);
+  const int grid = (int)std::min<long long>(sms, max_tiles);
+  grouped_tc_kernel<GATEUP, BN, COMBINE, GATHER><<<grid, kThreads, sm, s>>>(
+      a, b0, b1, offsets, R, E, N, K, out, perm, topk_w, kslots, gx, gsrc, gdiv);
   return cudaGetLastError();
+}
+
+// MMA width for a launch.  256 everywhere it was measured best (both GEMMs
+// when compute-bound, down always); gate/up with fewer than 256 rows per
+// expert on average is weight-bandwidth-bound and uses 128-wide tiles, twice
+// as many as 256-wide ones, for a better-filled last wave.
+// MOE_GROUPED_TILE_N in the environment forces a width (used by the tests).
+inline int choose_bn(int R, int E, int N, bool gateup, int sms) {
+  if (const char* force = getenv("MOE_GROUPED_TILE_N")) {  // testing override: 64, 128 or 256
+    const int v = atoi(force);
+    if (v == 64 || v == 128 || v == 256) return v;
+  }
+  (void)N;
+  (void)sms;
+  if (gateup && (long long)R < 2LL * BM * E) return 128;
+  return 256;
+}
+
+template <bool GATEUP>
+cudaError_t launch(const CUtensorMap* maps_by_bn, int bn, const int32_t* offsets, int R, int E, int N,
+                   int K, void* out, int sms, cudaStream_t s) {
+  // maps_by_bn: {A, B0, B1} for the chosen width
+  switch (bn) {
+    case 64: return launch_bn<GATEUP, 64>(maps_by_bn[0], maps_by_bn[1], maps_by_bn[2], offsets, R, E, N, K, out, sms, s);
+    case 128: return launch_bn<GATEUP, 128>(maps_by_bn[0], maps_by_bn[1], maps_by_bn[2], offsets, R, E, N, K, out, sms, s);
+    default: return launch_bn<GATEUP, 256>(maps_by_bn[0], maps_by_bn[1], maps_by_bn[2], offsets, R, E, N, K, out, sms, s);
+  }
 }
 
 }  // namespace tc
@@ -485,22 +608,70 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMa
 inline cudaError_t launch_gateup_tc(const __nv_bfloat16* x_perm, const int32_t* offsets,
                                     const __nv_bfloat16* w_gate, const __nv_bfloat16* w_up, int R,
                                     int d, int F, int E, __nv_bfloat16* h, cudaStream_t s) {
-  CUtensorMap a, b0, b1;
-  if (!tc::make_map(&a, x_perm, (uint64_t)R, (uint64_t)d, tc::BM) ||
-      !tc::make_map(&b0, w_gate, (uint64_t)E * F, (uint64_t)d, tc::BN / 2) ||
-      !tc::make_map(&b1, w_up, (uint64_t)E * F, (uint64_t)d, tc::BN / 2))
+  const int sms = tc::sm_count();
+  const int bn = tc::choose_bn(R, E, F, true, sms);
+  CUtensorMap m[3];
+  if (!tc::make_map(&m[0], x_perm, (uint64_t)R, (uint64_t)d, tc::BM) ||
+      !tc::make_map(&m[1], w_gate, (uint64_t)E * F, (uint64_t)d, bn / 2) ||
+      !tc::make_map(&m[2], w_up, (uint64_t)E * F, (uint64_t)d, bn / 2))
     return cudaErrorInvalidValue;
-  return tc::launch<true>(a, b0, b1, offsets, R, E, F, d, h, s);
+  return tc::launch<true>(m, bn, offsets, R, E, F, d, h, sms, s);
+}
+
+// Gate/up with the dispatch gather fused into the A load: row r of the
+// segment-ordered A is x[src[r] / div] (src = perm with div = k for top-k,
+// the expert-choice token ids with div = 1); x_perm is never materialised.
+inline cudaError_t launch_gateup_gather_tc(const __nv_bfloat16* x, int T, const int32_t* src,
+                                           int div, const int32_t* offsets, const __nv_bfloat16* w_gate,
+                                           const __nv_bfloat16* w_up, int R, int d, int F, int E,
+                                           __nv_bfloat16* h, cudaStream_t s) {
+  const int sms = tc::sm_count();
+  const int bn = tc::choose_bn(R, E, F, true, sms);
+  CUtensorMap m[3];
+  if (!tc::make_map(&m[0], x, (uint64_t)T, (uint64_t)d, 1) ||  // one-row box for gather4
+      !tc::make_map(&m[1], w_gate, (uint64_t)E * F, (uint64_t)d, bn / 2) ||
+      !tc::make_map(&m[2], w_up, (uint64_t)E * F, (uint64_t)d, bn / 2))
+    return cudaErrorInvalidValue;
+  switch (bn) {
+    case 64:
+      return tc::launch_bn<true, 64, false, true>(m[0], m[1], m[2], offsets, R, E, F, d, h, sms, s,
+                                                  nullptr, nullptr, 1, x, src, div);
+    case 128:
+      return tc::launch_bn<true, 128, false, true>(m[0], m[1], m[2], offsets, R, E, F, d, h, sms, s,
+                                                   nullptr, nullptr, 1, x, src, div);
+    default:
+      return tc::launch_bn<true, 256, false, true>(m[0], m[1], m[2], offsets, R, E, F, d, h, sms, s,
+                                                   nullptr, nullptr, 1, x, src, div);
+  }
 }
 
 inline cudaError_t launch_down_tc(const __nv_bfloat16* h, const int32_t* offsets,
                                   const __nv_bfloat16* w_down, int R, int d, int F, int E,
                                   float* y_perm, cudaStream_t s) {
-  CUtensorMap a, b0;
-  if (!tc::make_map(&a, h, (uint64_t)R, (uint64_t)F, tc::BM) ||
-      !tc::make_map(&b0, w_down, (uint64_t)E * d, (uint64_t)F, tc::BN))
+  const int sms = tc::sm_count();
+  const int bn = tc::choose_bn(R, E, d, false, sms);
+  CUtensorMap m[3];
+  if (!tc::make_map(&m[0], h, (uint64_t)R, (uint64_t)F, tc::BM) ||
+      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, bn))
     return cudaErrorInvalidValue;
-  return tc::launch<false>(a, b0, b0, offsets, R, E, d, F, y_perm, s);
+  m[2] = m[1];
+  return tc::launch<false>(m, bn, offsets, R, E, d, F, y_perm, sms, s);
+}
+
+// Down projection fused with the combine for k <= 2 (deterministic, see the
+// kernel): y [T, d] must be zero on entry; row r adds topk_w[perm[r]] * (h_r
+// W_down^T) into y[perm[r] / k].
+inline cudaError_t launch_down_combine_tc(const __nv_bfloat16* h, const int32_t* offsets,
+                                          const __nv_bfloat16* w_down, int R, int d, int F, int E,
+                                          const int32_t* perm, const float* topk_w, int k, float* y,
+                                          cudaStream_t s) {
+  const int sms = tc::sm_count();
+  CUtensorMap m[2];
+  if (!tc::make_map(&m[0], h, (uint64_t)R, (uint64_t)F, tc::BM) ||
+      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, 256))
+    return cudaErrorInvalidValue;
+  return tc::launch_bn<false, 256, true>(m[0], m[1], m[1], offsets, R, E, d, F, y, sms, s, perm,
+                                         topk_w, k);
 }
 
 }  // namespace moe

@@ -111,18 +111,18 @@ moe_status moe_expert_choice_route(const void* x, const void* w_g, const float* 
   cudaError_t e = launch_router(x, w_g, bias, T, d, E, /*k=*/0, dt == MOE_BF16, nullptr, nullptr,
                                 logits, nullptr, nullptr, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  const int n2 = next_pow2(T);
-  const size_t sm = (size_t)n2 * sizeof(unsigned long long);
+  const int c2 = next_pow2(C > 0 ? C : 1);
+  const size_t sm = ec_route_smem(T, C > 0 ? C : 1);
   e = cudaFuncSetAttribute(ec_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  ec_route_kernel<<<E, kEcThreads, sm, s>>>(logits, T, E, C, n2, ec_idx, ec_score, pos);
+  ec_route_kernel<<<E, kEcThreads, sm, s>>>(logits, T, E, C, c2, ec_idx, ec_score, pos);
   return cuda_status(cudaGetLastError());
 }
 
 size_t moe_permute_workspace_size(int T, int E, int k) {
   if (T < 0 || E < 1 || k < 1) return 0;
   const int tiles = dispatch_tiles((long long)T * k, kRouterTokens * k);
-  return 2 * align256((size_t)tiles * E * sizeof(int32_t)) + 256;
+  return align256((size_t)tiles * E * sizeof(int32_t)) + 256;
 }
 
 moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, int T, int d,
@@ -140,22 +140,26 @@ moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, in
   return cuda_status(cudaGetLastError());
 }
 
-// Scan + scatter (+ row copy) of the dispatch; with counts_ready the per-tile
-// counts are already in tile_counts (written by the router), else a histogram
-// pass computes them.  Tiles are `tile` consecutive assignments.
+// Dispatch: (histogram when the counts are not ready) + scatter with the row
+// copy.  With counts_ready the per-tile counts are already in tile_counts
+// (written by the router).  Tiles are `tile` consecutive assignments.  With
+// aux_partials the scatter's CTA 0 also writes f, p and loss; with y_zero the
+// scatter zeroes y for the fused down+combine.
 static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
                                   moe_dtype dt, void* x_perm, int32_t* counts, int32_t* offsets,
-                                  int32_t* perm, int32_t* inv_perm, int32_t* tile_counts,
-                                  int32_t* tile_base, int tile, bool counts_ready, cudaStream_t s) {
+                                  int32_t* perm, int32_t* inv_perm, int32_t* tile_counts, int tile,
+                                  bool counts_ready, cudaStream_t s,
+                                  const float* aux_partials = nullptr, float* f = nullptr,
+                                  float* p = nullptr, float* loss = nullptr,
+                                  float* y_zero = nullptr) {
   const long long A = (long long)T * k;
   const int tiles = dispatch_tiles(A, tile);
   if (!counts_ready)
     dispatch_hist_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile, tile_counts);
-  dispatch_scan_kernel<<<1, kScanThreads, 0, s>>>(tile_counts, tiles, E, (int)A, tile_base, counts,
-                                                  offsets);
   dispatch_scatter_kernel<<<tiles, kDispatchThreads, 0, s>>>(
-      topk_idx, (int)A, E, k, tile, tile_base, perm, inv_perm, static_cast<const uint4*>(x),
-      (int)(d * elt_size(dt) / 16), static_cast<uint4*>(x_perm));
+      topk_idx, (int)A, E, k, tile, tile_counts, tiles, perm, inv_perm, counts, offsets,
+      static_cast<const uint4*>(x), (int)(d * elt_size(dt) / 16), static_cast<uint4*>(x_perm),
+      aux_partials, T, f, p, loss, reinterpret_cast<float4*>(y_zero), d / 4, tile / k);
   return cuda_status(cudaGetLastError());
 }
 
@@ -187,9 +191,8 @@ moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int
   Carver cv{static_cast<char*>(ws)};
   cv.used = (256 - (reinterpret_cast<uintptr_t>(ws) & 255)) & 255;
   int32_t* tile_counts = cv.take<int32_t>((size_t)tiles * E);
-  int32_t* tile_base = cv.take<int32_t>((size_t)tiles * E);
   return dispatch_launch(x, topk_idx, T, d, E, k, dt, x_perm, counts, offsets, perm, inv_perm,
-                         tile_counts, tile_base, kRouterTokens * k, false, s);
+                         tile_counts, kRouterTokens * k, false, s);
 }
 
 static moe_status check_experts(int R, int d, int F, int E, moe_dtype dt) {
@@ -217,6 +220,24 @@ moe_status moe_grouped_gateup_swiglu(const void* x_perm, const int32_t* offsets,
   return cuda_status(launch_grouped_simt<float, true>(
       static_cast<const float*>(x_perm), offsets, static_cast<const float*>(w_gate),
       static_cast<const float*>(w_up), R, F, d, E, h, s));
+}
+
+moe_status moe_grouped_gateup_swiglu_gather(const void* x, const int32_t* src, int div, int T,
+                                            const int32_t* offsets, const void* w_gate,
+                                            const void* w_up, int R, int d, int F, int E,
+                                            moe_dtype dt, void* h, moe_stream_t stream) {
+  moe_status st = check_experts(R, d, F, E, dt);
+  if (st != MOE_OK) return st;
+  if (dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (div < 1 || T < 1) return R == 0 ? MOE_OK : MOE_ERR_INVALID_ARG;
+  if (R == 0) return MOE_OK;
+  if (!x || !src || !offsets || !w_gate || !w_up || !h) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(h))
+    return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_gateup_gather_tc(
+      static_cast<const __nv_bfloat16*>(x), T, src, div, offsets,
+      static_cast<const __nv_bfloat16*>(w_gate), static_cast<const __nv_bfloat16*>(w_up), R, d, F, E,
+      static_cast<__nv_bfloat16*>(h), (cudaStream_t)stream));
 }
 
 moe_status moe_grouped_down(const void* h, const int32_t* offsets, const void* w_down, int R, int d,
@@ -404,23 +425,34 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   if (st != MOE_OK) return st;
   if (D.dtype == MOE_BF16 && (!aligned16(x) || !aligned16(w->w_g))) return MOE_ERR_UNSUPPORTED;
   // router CTAs double as dispatch tiles: the router writes the per-tile counts
-  const int tiles = dispatch_tiles((long long)A, kRouterTokens * k);
   int32_t* tile_counts = static_cast<int32_t*>(pw);
-  int32_t* tile_base = reinterpret_cast<int32_t*>(static_cast<char*>(pw) +
-                                                  align256((size_t)tiles * D.E * sizeof(int32_t)));
   if (launch_router(x, w->w_g, w->bias, D.T, D.d, D.E, k, D.dtype == MOE_BF16, idx, tw, O.logits,
                     nullptr, aux, s, tile_counts) != cudaSuccess)
     return MOE_ERR_CUDA;
+  // k <= 2 (bf16): the down GEMM accumulates the combine into y, zeroed by the scatter
+  const bool fused_combine = D.dtype == MOE_BF16 && k <= 2;
+  if (fused_combine && (!aligned16(w->w_down) || !aligned16(y))) return MOE_ERR_UNSUPPORTED;
+  // the scatter also copies the x rows into dispatch order: contiguous row blocks
+  // keep the gate/up operand loads full-width TMA boxes (gathering rows inside
+  // the GEMM re-fetches them once per n-block and measured several times slower)
   st = dispatch_launch(x, idx, D.T, D.d, D.E, k, D.dtype, x_perm, counts, offsets, perm, inv_perm,
-                       tile_counts, tile_base, kRouterTokens * k, true, s);
+                       tile_counts, kRouterTokens * k, true, s, aux, O.f ? O.f : fpl,
+                       O.p ? O.p : fpl + D.E, O.loss ? O.loss : fpl + 2 * D.E,
+                       fused_combine ? y : nullptr);
   if (st != MOE_OK) return st;
+  if (fused_combine) {
+    // down projection with the combine in its epilogue (deterministic for k <= 2)
+    st = moe_grouped_gateup_swiglu(x_perm, offsets, w->w_gate, w->w_up, (int)A, D.d, D.F, D.E,
+                                   D.dtype, h, stream);
+    if (st != MOE_OK) return st;
+    return cuda_status(launch_down_combine_tc(static_cast<const __nv_bfloat16*>(h), offsets,
+                                              static_cast<const __nv_bfloat16*>(w->w_down), (int)A,
+                                              D.d, D.F, D.E, perm, tw, k, y, s));
+  }
   st = moe_experts_swiglu(x_perm, offsets, w->w_gate, w->w_up, w->w_down, (int)A, D.d, D.F, D.E,
                           D.dtype, h, y_perm, stream);
   if (st != MOE_OK) return st;
-  st = moe_combine(y_perm, inv_perm, tw, D.T, D.d, k, y, stream);
-  if (st != MOE_OK) return st;
-  return moe_aux_loss(nullptr, aux, counts, D.T, D.E, k, O.f ? O.f : fpl, O.p ? O.p : fpl + D.E,
-                      O.loss ? O.loss : fpl + 2 * D.E, stream);
+  return moe_combine(y_perm, inv_perm, tw, D.T, D.d, k, y, stream);
 }
 
 }  // extern "C"

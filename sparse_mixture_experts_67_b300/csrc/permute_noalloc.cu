@@ -26,7 +26,7 @@
 namespace {
 
 constexpr size_t kNoAllocScratchInts = MOE_PERMUTE_NOALLOC_SCRATCH_BYTES / sizeof(int32_t);
-constexpr size_t kNoAllocHalf = kNoAllocScratchInts / 2;  // tile counts | tile bases
+constexpr size_t kNoAllocHalf = kNoAllocScratchInts / 2;  // per-tile counts (the stated limit)
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
@@ -78,8 +78,7 @@ extern "C" moe_status moe_permute_noalloc(const void* x, const int32_t* topk_idx
   moe_status st = noalloc_scratch(&scratch);
   if (st != MOE_OK) return st;
   int32_t* tile_counts = scratch;
-  int32_t* tile_base = scratch + kNoAllocHalf;
   if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
   return dispatch_launch(x, topk_idx, T, d, E, k, dt, x_perm, counts, offsets, perm, inv_perm,
-                         tile_counts, tile_base, kTile, false, s);
+                         tile_counts, kTile, false, s);
 }

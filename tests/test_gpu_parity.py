@@ -136,9 +136,14 @@ EXPERT_CASES = [
 ]
 
 
+@pytest.mark.parametrize("tile_n", ["auto", "64", "128", "256"])
 @pytest.mark.parametrize("case", EXPERT_CASES, ids=[c[0] for c in EXPERT_CASES])
-def test_grouped_experts_parity(moe, torch, case):
+def test_grouped_experts_parity(moe, torch, case, tile_n, monkeypatch):
     name, cnts, d, F, dt = case
+    if tile_n != "auto":
+        if dt != "bf16":
+            pytest.skip("tile width applies to the tensor-core path")
+        monkeypatch.setenv("MOE_GROUPED_TILE_N", tile_n)
     E = len(cnts)
     R = int(sum(cnts))
     cfg = synth.small_config(name, R, d, F, E, 1, dt, seed=11, x_std=1.0, w_std=0.05)
@@ -329,12 +334,49 @@ def test_layer_zero_tokens(moe, torch):
     assert y.shape == (0, 64)
 
 
-def test_layer_deterministic(moe, torch):
-    cfg = synth.small_config("det", 3000, 128, 256, 16, 4, "bf16", seed=50, x_std=1.0, w_std=0.05)
+@pytest.mark.parametrize("k", [1, 2, 4])
+def test_layer_deterministic(moe, torch, k):
+    """Bit-identical outputs on repeated runs (k <= 2 combines in the down GEMM with atomics)."""
+    cfg = synth.small_config("det", 3000, 128, 256, 16, k, "bf16", seed=50, x_std=1.0, w_std=0.05)
     inp = synth.make_inputs(cfg)
     w = dev_weights(inp)
     x = to_dev(inp.x)
-    y1 = moe.moe_layer_forward(x, w, k=4).clone()
-    y2 = moe.moe_layer_forward(x, w, k=4)
+    ys = [moe.moe_layer_forward(x, w, k=k).clone() for _ in range(3)]
     torch.cuda.synchronize()
-    assert torch.equal(y1, y2)
+    assert all(torch.equal(ys[0], yi) for yi in ys[1:])
+
+
+GATHER_CASES = [
+    # name, T, d, F, E, k (0: expert-choice style token ids, div 1)
+    ("topk_e8_k2", 700, 128, 256, 8, 2),
+    ("topk_e64_k4", 1200, 128, 128, 64, 4),
+    ("ec_style_e5", 300, 64, 192, 5, 0),
+]
+
+
+@pytest.mark.parametrize("tile_n", ["auto", "64", "128", "256"])
+@pytest.mark.parametrize("case", GATHER_CASES, ids=[c[0] for c in GATHER_CASES])
+def test_gateup_gather_bit_identical(moe, torch, case, tile_n, monkeypatch):
+    """Gathering rows inside the GEMM equals materialising x_perm first, bit for bit."""
+    name, T, d, F, E, k = case
+    if tile_n != "auto":
+        monkeypatch.setenv("MOE_GROUPED_TILE_N", tile_n)
+    rng = np.random.default_rng(zlib.crc32(name.encode()))
+    cfg = synth.small_config(name, T, d, F, E, max(k, 1), "bf16", seed=7, w_std=0.05)
+    inp = synth.make_inputs(cfg)
+    x = to_dev(inp.x)
+    w = dev_weights(inp)
+    if k > 0:
+        idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+        p = moe.moe_permute(x, torch.from_numpy(idx).cuda(), E)
+        x_perm, offsets, src, div = p["x_perm"], p["offsets"], p["perm"], k
+    else:
+        C = T // 3
+        src_np = np.concatenate([rng.choice(T, size=C, replace=False) for _ in range(E)]).astype(np.int32)
+        src = torch.from_numpy(src_np).cuda()
+        offsets = torch.from_numpy((np.arange(E + 1) * C).astype(np.int32)).cuda()
+        x_perm, div = moe.moe_gather_rows(x, src, 1), 1
+    h_ref = moe.moe_grouped_gateup_swiglu(x_perm, offsets, w["w_gate"], w["w_up"])
+    h_gat = moe.moe_grouped_gateup_swiglu_gather(x, src, div, offsets, w["w_gate"], w["w_up"])
+    torch.cuda.synchronize()
+    assert torch.equal(h_ref.view(torch.int16), h_gat.view(torch.int16))
