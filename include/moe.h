@@ -83,8 +83,9 @@ moe_status moe_device_error(uint32_t* word, int clear);
  *   topk_idx [T,k] int32, topk_w [T,k] fp32             (required outputs)
  *   logits [T,E] fp32, probs [T,E] fp32                 (optional, NULL to skip)
  *   aux_partials: optional fp32 [moe_route_aux_rows(T), E]; when given, row r
- *             holds sum of g[t,e] over the r-th block of tokens, consumed by
- *             moe_aux_loss.
+ *             holds sum of g[t,e] over the r-th block of tokens (32 tokens
+ *             for E <= 16, 64 above; moe_route_aux_rows(T) covers both),
+ *             consumed by moe_aux_loss.
  * Limits: 1 <= k <= E <= 256.                                               */
 size_t moe_route_aux_rows(int T);
 moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, int d, int E,
@@ -131,8 +132,8 @@ moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int
  * counterpart; this exists for callers that cannot provide device scratch:
  * plugin hosts that give a kernel only its input and output buffers, and
  * deployments whose device memory is reserved up front by another allocator,
- * so that nothing may call cudaMalloc while they run.  The scratch (the
- * per-tile expert counts) lives in a fixed array of
+ * so that nothing may call cudaMalloc while they run.  The scratch (per-tile
+ * expert counts and their scanned bases) lives in a fixed array of
  * MOE_PERMUTE_NOALLOC_SCRATCH_BYTES inside the library's device memory, held
  * by every GPU that loads the library until the process exits.
  *   Limit: ceil(T*k / 2048) * E <= MOE_PERMUTE_NOALLOC_SCRATCH_BYTES / 8

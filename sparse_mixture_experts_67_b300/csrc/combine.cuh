@@ -97,11 +97,12 @@ __global__ void __launch_bounds__(kCombineThreads)
   }
 }
 
-// Per-block partial column sums of probs [T,E] in the router's block layout.
-__global__ void probs_partials_kernel(const float* __restrict__ probs, int T, int E,
+// Per-block partial column sums of probs [T,E] in the router's block layout
+// (blocks of tok tokens).
+__global__ void probs_partials_kernel(const float* __restrict__ probs, int T, int E, int tok,
                                       float* __restrict__ partials) {
-  const int t0 = blockIdx.x * kRouterTokens;
-  const int t1 = min(T, t0 + kRouterTokens);
+  const int t0 = blockIdx.x * tok;
+  const int t1 = min(T, t0 + tok);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     float s = 0.f;
     for (int t = t0; t < t1; ++t) s += probs[(size_t)t * E + e];

@@ -6,7 +6,7 @@
 // the order inside an expert fixed to ascending assignment id a = t*k + j.
 //
 // Deterministic without a global sort, in tiles of `tile` consecutive
-// assignments (the layer uses one tile per router CTA, 64 tokens):
+// assignments (the layer uses one tile per router CTA):
 //   hist:    per-tile expert counts with warp-aggregated shared-memory
 //            atomics (match_any + popc); in the layer the router's epilogue
 //            produces them instead;
@@ -46,18 +46,84 @@ __global__ void __launch_bounds__(kDispatchThreads)
 }
 
 // Ranks each assignment of its tile among equal experts and writes perm /
-// inv_perm.  The tile's first dispatch row per expert comes from the count
-// matrix directly: every CTA reduces the [tiles, E] counts itself (totals,
-// and the sum over the tiles before its own), warp per expert, lanes over
-// tiles; the expert offsets are the exclusive scan of the totals.  CTA 0 also
-// writes counts / offsets and, given aux_partials, the load-balancing
-// statistics (same reduction order as aux_finalize_kernel).  Optional extras:
+// inv_perm.  The tile's first dispatch row per expert comes from tile_base
+// when given (dispatch_scan_kernel), else from the count matrix directly:
+// every CTA reduces the [tiles, E] counts itself (totals, and the sum over
+// the tiles before its own), warp per expert, lanes over tiles; the expert
+// offsets are the exclusive scan of the totals, and CTA 0 also writes counts /
+// offsets and, given aux_partials, the load-balancing statistics (same
+// reduction order as aux_finalize_kernel).  Optional extras:
 // x != nullptr copies x[a / k] into x_perm[row] (16-byte vectors, warp per
 // row); y_zero != nullptr zeroes the y rows of the tile's tokens
 // (tokens_per_tile of them) for an accumulating combine downstream.
+// Large count matrices: one CTA computes every tile's first dispatch row per
+// expert (tile_base), the counts and the offsets; the scatter CTAs then read
+// their row of tile_base instead of reducing the whole matrix each.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads)
+    dispatch_scan_kernel(const int32_t* __restrict__ tile_counts, int tiles, int E, int A,
+                         int32_t* __restrict__ tile_base, int32_t* __restrict__ counts,
+                         int32_t* __restrict__ offsets) {
+  __shared__ int s_tot[MOE_MAX_EXPERTS];
+  __shared__ int s_off[MOE_MAX_EXPERTS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int nwarps = kScanThreads / 32;
+  for (int e = warp; e < E; e += nwarps) {
+    int acc = 0;
+    for (int t = lane; t < tiles; t += 32) acc += tile_counts[(size_t)t * E + e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+    if (lane == 0) s_tot[e] = acc;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int per = MOE_MAX_EXPERTS / 32;
+    const int e0 = lane * per;
+    int run = 0;
+    for (int e = e0; e < min(E, e0 + per); ++e) run += s_tot[e];
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int nb = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += nb;
+    }
+    int ex = incl - run;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      s_off[e] = ex;
+      ex += s_tot[e];
+    }
+  }
+  __syncthreads();
+  for (int e = warp; e < E; e += nwarps) {
+    int running = s_off[e];
+    for (int t0 = 0; t0 < tiles; t0 += 32) {
+      const int t = t0 + lane;
+      const int v = t < tiles ? tile_counts[(size_t)t * E + e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int nb = __shfl_up_sync(kFullMask, incl, off);
+        if (lane >= off) incl += nb;
+      }
+      if (t < tiles) tile_base[(size_t)t * E + e] = running + incl - v;
+      running += __shfl_sync(kFullMask, incl, 31);
+    }
+    if (lane == 0) {
+      counts[e] = s_tot[e];
+      offsets[e] = s_off[e];
+    }
+  }
+  if (threadIdx.x == 0) offsets[E] = A;
+}
+
+// The in-CTA reduction reads tiles * E counts per CTA; above this many
+// tiles^2 * E reads in total the separate scan is cheaper.
+constexpr long long kFusedScanMaxReads = 4LL * 1024 * 1024;
+
 __global__ void __launch_bounds__(kDispatchThreads)
     dispatch_scatter_kernel(const int32_t* __restrict__ idx, int A, int E, int k, int tile,
-                            const int32_t* __restrict__ tile_counts, int tiles,
+                            const int32_t* __restrict__ tile_counts,
+                            const int32_t* __restrict__ tile_base, int tiles,
                             int32_t* __restrict__ perm, int32_t* __restrict__ inv_perm,
                             int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                             const uint4* __restrict__ x, int vec_per_row, uint4* __restrict__ x_perm,
@@ -72,7 +138,10 @@ __global__ void __launch_bounds__(kDispatchThreads)
   __shared__ float s_fp[MOE_MAX_EXPERTS];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int me = blockIdx.x;
-  for (int e = warp; e < E; e += kDispatchWarps) {
+  const bool fused_scan = tile_base == nullptr;
+  for (int e = fused_scan ? E : threadIdx.x; e < E; e += blockDim.x)
+    running[e] = tile_base[(size_t)me * E + e];
+  for (int e = fused_scan ? warp : E; e < E; e += kDispatchWarps) {
     int tot = 0, pre = 0;
     for (int t = lane; t < tiles; t += 32) {
       const int c = tile_counts[(size_t)t * E + e];
@@ -92,15 +161,11 @@ __global__ void __launch_bounds__(kDispatchThreads)
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     for (int w = 0; w < kDispatchWarps; ++w) wcnt[w][e] = 0;
   __syncthreads();
-  if (warp == 0) {  // exclusive scan of the (<= 256) totals: 8 per lane, then a warp scan
+  if (fused_scan && warp == 0) {  // exclusive scan of the (<= 256) totals, 8 per lane
     constexpr int per = MOE_MAX_EXPERTS / 32;
-    int v[per], run = 0;
-#pragma unroll
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      v[i] = e < E ? s_tot[e] : 0;
-      run += v[i];
-    }
+    const int e0 = lane * per;
+    int run = 0;
+    for (int e = e0; e < min(E, e0 + per); ++e) run += s_tot[e];
     int incl = run;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -108,17 +173,14 @@ __global__ void __launch_bounds__(kDispatchThreads)
       if (lane >= off) incl += nb;
     }
     int ex = incl - run;
-#pragma unroll
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      if (e < E) {
-        if (me == 0) {
-          counts[e] = v[i];
-          offsets[e] = ex;
-        }
-        running[e] += ex;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      const int v = s_tot[e];
+      if (me == 0) {
+        counts[e] = v;
+        offsets[e] = ex;
       }
-      ex += v[i];
+      running[e] += ex;
+      ex += v;
     }
     if (me == 0 && lane == 31) offsets[E] = A;
   }
@@ -176,7 +238,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
     }
     __syncthreads();
   }
-  if (me != 0 || aux_partials == nullptr) return;
+  if (me != 0 || aux_partials == nullptr || !fused_scan) return;
   // CTA 0: aux statistics from the router's per-tile partial sums of g
   for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) s_fp[e] = 0.f;
   __syncthreads();

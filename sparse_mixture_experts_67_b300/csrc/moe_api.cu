@@ -74,7 +74,8 @@ moe_status moe_device_error(uint32_t* word, int clear) {
   return cuda_status(e);
 }
 
-size_t moe_route_aux_rows(int T) { return T <= 0 ? 0 : (size_t)ceil_div(T, kRouterTokens); }
+// Rows for the smallest router block (an upper bound for every E).
+size_t moe_route_aux_rows(int T) { return T <= 0 ? 0 : (size_t)ceil_div(T, kRouterTokensMin); }
 
 moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, int d, int E, int k,
                      moe_dtype dt, int32_t* topk_idx, float* topk_w, float* logits, float* probs,
@@ -121,8 +122,8 @@ moe_status moe_expert_choice_route(const void* x, const void* w_g, const float* 
 
 size_t moe_permute_workspace_size(int T, int E, int k) {
   if (T < 0 || E < 1 || k < 1) return 0;
-  const int tiles = dispatch_tiles((long long)T * k, kRouterTokens * k);
-  return align256((size_t)tiles * E * sizeof(int32_t)) + 256;
+  const int tiles = dispatch_tiles((long long)T * k, router_tokens(E) * k);
+  return 2 * align256((size_t)tiles * E * sizeof(int32_t)) + 256;
 }
 
 moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, int T, int d,
@@ -147,8 +148,8 @@ moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, in
 // scatter zeroes y for the fused down+combine.
 static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
                                   moe_dtype dt, void* x_perm, int32_t* counts, int32_t* offsets,
-                                  int32_t* perm, int32_t* inv_perm, int32_t* tile_counts, int tile,
-                                  bool counts_ready, cudaStream_t s,
+                                  int32_t* perm, int32_t* inv_perm, int32_t* tile_counts,
+                                  int32_t* tile_base, int tile, bool counts_ready, cudaStream_t s,
                                   const float* aux_partials = nullptr, float* f = nullptr,
                                   float* p = nullptr, float* loss = nullptr,
                                   float* y_zero = nullptr) {
@@ -156,10 +157,18 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
   const int tiles = dispatch_tiles(A, tile);
   if (!counts_ready)
     dispatch_hist_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile, tile_counts);
+  const bool separate_scan = (long long)tiles * tiles * E > kFusedScanMaxReads;
+  if (separate_scan) {
+    dispatch_scan_kernel<<<1, kScanThreads, 0, s>>>(tile_counts, tiles, E, (int)A, tile_base,
+                                                    counts, offsets);
+    if (aux_partials)
+      aux_finalize_kernel<<<1, kAuxThreads, 0, s>>>(aux_partials, tiles, counts, T, E, f, p, loss);
+  }
   dispatch_scatter_kernel<<<tiles, kDispatchThreads, 0, s>>>(
-      topk_idx, (int)A, E, k, tile, tile_counts, tiles, perm, inv_perm, counts, offsets,
-      static_cast<const uint4*>(x), (int)(d * elt_size(dt) / 16), static_cast<uint4*>(x_perm),
-      aux_partials, T, f, p, loss, reinterpret_cast<float4*>(y_zero), d / 4, tile / k);
+      topk_idx, (int)A, E, k, tile, tile_counts, separate_scan ? tile_base : nullptr, tiles, perm,
+      inv_perm, counts, offsets, static_cast<const uint4*>(x), (int)(d * elt_size(dt) / 16),
+      static_cast<uint4*>(x_perm), aux_partials, T, f, p, loss,
+      reinterpret_cast<float4*>(y_zero), d / 4, tile / k);
   return cuda_status(cudaGetLastError());
 }
 
@@ -187,12 +196,14 @@ moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int
   }
   if (!x || !topk_idx || !x_perm || !perm || !inv_perm) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < moe_permute_workspace_size(T, E, k)) return MOE_ERR_WORKSPACE;
-  const int tiles = dispatch_tiles((long long)T * k, kRouterTokens * k);
+  const int tile = router_tokens(E) * k;
+  const int tiles = dispatch_tiles((long long)T * k, tile);
   Carver cv{static_cast<char*>(ws)};
   cv.used = (256 - (reinterpret_cast<uintptr_t>(ws) & 255)) & 255;
   int32_t* tile_counts = cv.take<int32_t>((size_t)tiles * E);
+  int32_t* tile_base = cv.take<int32_t>((size_t)tiles * E);
   return dispatch_launch(x, topk_idx, T, d, E, k, dt, x_perm, counts, offsets, perm, inv_perm,
-                         tile_counts, kRouterTokens * k, false, s);
+                         tile_counts, tile_base, tile, false, s);
 }
 
 static moe_status check_experts(int R, int d, int F, int E, moe_dtype dt) {
@@ -299,11 +310,12 @@ moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int
   if (T == 0) return MOE_OK;
   if (!counts || (!probs && !aux_partials)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  const int rows = (int)moe_route_aux_rows(T);
+  const int tok = router_tokens(E);  // the router's block of tokens for this E
+  const int rows = ceil_div(T, tok);
   if (probs) {
     // probs given: rebuild the per-block partial sums in place of the router's
     if (!aux_partials) return MOE_ERR_INVALID_ARG;
-    probs_partials_kernel<<<rows, 256, 0, s>>>(probs, T, E, const_cast<float*>(aux_partials));
+    probs_partials_kernel<<<rows, 256, 0, s>>>(probs, T, E, tok, const_cast<float*>(aux_partials));
   }
   aux_finalize_kernel<<<1, kAuxThreads, 0, s>>>(aux_partials, rows, counts, T, E, f, p, loss);
   return cuda_status(cudaGetLastError());
@@ -425,7 +437,11 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   if (st != MOE_OK) return st;
   if (D.dtype == MOE_BF16 && (!aligned16(x) || !aligned16(w->w_g))) return MOE_ERR_UNSUPPORTED;
   // router CTAs double as dispatch tiles: the router writes the per-tile counts
+  const int tile = router_tokens(D.E) * k;
+  const int tiles = dispatch_tiles((long long)A, tile);
   int32_t* tile_counts = static_cast<int32_t*>(pw);
+  int32_t* tile_base = reinterpret_cast<int32_t*>(static_cast<char*>(pw) +
+                                                  align256((size_t)tiles * D.E * sizeof(int32_t)));
   if (launch_router(x, w->w_g, w->bias, D.T, D.d, D.E, k, D.dtype == MOE_BF16, idx, tw, O.logits,
                     nullptr, aux, s, tile_counts) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -436,7 +452,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   // keep the gate/up operand loads full-width TMA boxes (gathering rows inside
   // the GEMM re-fetches them once per n-block and measured several times slower)
   st = dispatch_launch(x, idx, D.T, D.d, D.E, k, D.dtype, x_perm, counts, offsets, perm, inv_perm,
-                       tile_counts, kRouterTokens * k, true, s, aux, O.f ? O.f : fpl,
+                       tile_counts, tile_base, tile, true, s, aux, O.f ? O.f : fpl,
                        O.p ? O.p : fpl + D.E, O.loss ? O.loss : fpl + 2 * D.E,
                        fused_combine ? y : nullptr);
   if (st != MOE_OK) return st;

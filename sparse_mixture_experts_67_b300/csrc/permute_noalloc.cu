@@ -26,7 +26,7 @@
 namespace {
 
 constexpr size_t kNoAllocScratchInts = MOE_PERMUTE_NOALLOC_SCRATCH_BYTES / sizeof(int32_t);
-constexpr size_t kNoAllocHalf = kNoAllocScratchInts / 2;  // per-tile counts (the stated limit)
+constexpr size_t kNoAllocHalf = kNoAllocScratchInts / 2;  // tile counts | tile bases
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
@@ -79,6 +79,8 @@ extern "C" moe_status moe_permute_noalloc(const void* x, const int32_t* topk_idx
   if (st != MOE_OK) return st;
   int32_t* tile_counts = scratch;
   if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
+  // second half of the array holds the tile bases when the separate scan runs
+  int32_t* tile_base = scratch + kNoAllocHalf;
   return dispatch_launch(x, topk_idx, T, d, E, k, dt, x_perm, counts, offsets, perm, inv_perm,
-                         tile_counts, kTile, false, s);
+                         tile_counts, tile_base, kTile, false, s);
 }

@@ -5,7 +5,7 @@
 // 아키텍처 심층 분석" (youngju.dev): s = x W_g^T (+ b), g = softmax(s), the k
 // largest entries, weights renormalised over the selection.
 //
-// One CTA owns 64 tokens (4 warps x 16).  The logits GEMM is narrow (N = E
+// One CTA owns TOK = 32 or 64 tokens (warps of 16), chosen by the expert count.  The logits GEMM is narrow (N = E
 // <= 256), so bf16 runs on warp-level mma.sync m16n8k16 tiles fed by cp.async
 // through a deep shared-memory ring (up to 6 stages, so enough bytes of x are
 // in flight to stream it at HBM speed); fp32 runs on FFMA.  The 64 x E logits
@@ -21,8 +21,11 @@
 
 namespace moe {
 
-constexpr int kRouterTokens = 64;
-constexpr int kRouterThreads = 128;
+// Tokens per CTA (and per dispatch tile): 32 for small expert counts (more,
+// shorter CTAs stream x faster), 64 from E > 16 on (W_g re-reads per token
+// halve).  Threads per CTA: 2 * TOK (TOK / 16 warps of 16-token mma tiles).
+constexpr int kRouterTokensMin = 32;
+inline int router_tokens(int E) { return E <= 16 ? 32 : 64; }
 constexpr int kRouterBK = 64;
 constexpr int kRouterLd = kRouterBK + 8;  // bf16 elements per smem row (pad: conflict-free)
 
@@ -45,11 +48,12 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, cons
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Thread-per-token epilogue over the logits tile S[64][ldS] (bias not yet
+// Thread-per-token epilogue over the logits tile S[TOK][ldS] (bias not yet
 // added; S is modified).  k == 0 writes logits only (expert-choice pre-pass).
-// s_m / s_inv: 64 floats each of shared scratch; s_cnt: MOE_MAX_EXPERTS ints.
+// s_m / s_inv: TOK floats each of shared scratch; s_cnt: MOE_MAX_EXPERTS ints.
 // tile_counts (nullable): this CTA's row of per-expert selection counts, the
-// dispatch histogram of its 64*k assignments.
+// dispatch histogram of its TOK*k assignments.
+template <int TOK>
 __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k,
                                 const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                                 float* __restrict__ w_out, float* __restrict__ logits_out,
@@ -57,7 +61,7 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
                                 int32_t* __restrict__ tile_counts, float* s_m, float* s_inv,
                                 int* s_cnt) {
   const int tid = threadIdx.x, nthr = blockDim.x;
-  const int ntok = min(kRouterTokens, T - tok0);
+  const int ntok = min(TOK, T - tok0);
   if (bias) {
     for (int i = tid; i < ntok * E; i += nthr) {
       const int r = i / E, e = i - r * E;
@@ -128,24 +132,24 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
 }
 
 // Pipeline depth: up to 6 stages within ~200 KB of shared memory.
-template <int NT>
+template <int NT, int TOK>
 constexpr int router_stages() {
-  constexpr size_t stage = (size_t)(kRouterTokens + 8 * NT) * kRouterLd * 2;
+  constexpr size_t stage = (size_t)(TOK + 8 * NT) * kRouterLd * 2;
   constexpr size_t fit = (200u * 1024u) / stage;
   return fit >= 6 ? 6 : (fit < 2 ? 2 : (int)fit);
 }
 
 // Shared memory: max(stage ring, logits tile) + epilogue scratch.
-template <int NT>
+template <int NT, int TOK>
 constexpr size_t router_smem_bytes_bf16() {
-  constexpr size_t ring = (size_t)router_stages<NT>() * (kRouterTokens + 8 * NT) * kRouterLd * 2;
-  constexpr size_t tile = (size_t)kRouterTokens * (8 * NT + 1) * 4;
+  constexpr size_t ring = (size_t)router_stages<NT, TOK>() * (TOK + 8 * NT) * kRouterLd * 2;
+  constexpr size_t tile = (size_t)TOK * (8 * NT + 1) * 4;
   constexpr size_t main = ring > tile ? ring : tile;
-  return main + 2 * kRouterTokens * 4 + MOE_MAX_EXPERTS * 4;
+  return main + 2 * TOK * 4 + MOE_MAX_EXPERTS * 4;
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kRouterThreads)
+template <int NT, int TOK>
+__global__ void __launch_bounds__(2 * TOK)
     router_bf16_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg,
                        const float* __restrict__ bias, int T, int d, int E, int k,
                        int32_t* __restrict__ idx_out, float* __restrict__ w_out,
@@ -154,31 +158,32 @@ __global__ void __launch_bounds__(kRouterThreads)
   constexpr int EP = 8 * NT;
   extern __shared__ __align__(16) unsigned char smem[];
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
-  constexpr int stage_elems = (kRouterTokens + EP) * kRouterLd;
-  constexpr int STAGES = router_stages<NT>();
+  constexpr int kThr = 2 * TOK;
+  constexpr int stage_elems = (TOK + EP) * kRouterLd;
+  constexpr int STAGES = router_stages<NT, TOK>();
   constexpr size_t ring_bytes = (size_t)STAGES * stage_elems * 2;
-  constexpr size_t tile_bytes = (size_t)kRouterTokens * (EP + 1) * 4;
+  constexpr size_t tile_bytes = (size_t)TOK * (EP + 1) * 4;
   constexpr size_t main_bytes = ring_bytes > tile_bytes ? ring_bytes : tile_bytes;
   float* s_m = reinterpret_cast<float*>(smem + main_bytes);
-  float* s_inv = s_m + kRouterTokens;
-  int* s_cnt = reinterpret_cast<int*>(s_inv + kRouterTokens);
+  float* s_inv = s_m + TOK;
+  int* s_cnt = reinterpret_cast<int*>(s_inv + TOK);
 
-  const int tok0 = blockIdx.x * kRouterTokens;
+  const int tok0 = blockIdx.x * TOK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = d / kRouterBK;
 
   auto load_stage = [&](int stage, int kc) {
     __nv_bfloat16* xs = ring + stage * stage_elems;
-    __nv_bfloat16* ws = xs + kRouterTokens * kRouterLd;
+    __nv_bfloat16* ws = xs + TOK * kRouterLd;
     const int kof = kc * kRouterBK;
-    for (int c = threadIdx.x; c < kRouterTokens * 8; c += kRouterThreads) {
+    for (int c = threadIdx.x; c < TOK * 8; c += kThr) {
       const int r = c >> 3, ch = c & 7;
       const int t = tok0 + r;
       const bool ok = t < T;
       const __nv_bfloat16* src = x + (size_t)(ok ? t : 0) * d + kof + ch * 8;
       cp_async16(xs + r * kRouterLd + ch * 8, src, ok);
     }
-    for (int c = threadIdx.x; c < EP * 8; c += kRouterThreads) {
+    for (int c = threadIdx.x; c < EP * 8; c += kThr) {
       const int r = c >> 3, ch = c & 7;
       const bool ok = r < E;
       const __nv_bfloat16* src = wg + (size_t)(ok ? r : 0) * d + kof + ch * 8;
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(kRouterThreads)
       cp_async_commit();
     }
     const __nv_bfloat16* xs = ring + (kc % STAGES) * stage_elems;
-    const __nv_bfloat16* ws = xs + kRouterTokens * kRouterLd;
+    const __nv_bfloat16* ws = xs + TOK * kRouterLd;
     const __nv_bfloat16* xw = xs + warp * 16 * kRouterLd;
 #pragma unroll
     for (int kk = 0; kk < kRouterBK; kk += 16) {
@@ -241,23 +246,23 @@ __global__ void __launch_bounds__(kRouterThreads)
     S[(r0 + 8) * ldS + col + 1] = acc[n][3];
   }
   __syncthreads();
-  router_epilogue(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
+  router_epilogue<TOK>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                   aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts, s_m,
                   s_inv, s_cnt);
 }
 
 // fp32 router: FFMA over 32-wide d chunks, same epilogue.
 constexpr int kRouterBKf = 32;
-template <int NT>
+template <int NT, int TOK>
 constexpr size_t router_smem_bytes_f32() {
   constexpr size_t ld = kRouterBKf + 1;
-  constexpr size_t tiles = (size_t)(kRouterTokens + 8 * NT) * ld * 4;
-  constexpr size_t acc = (size_t)kRouterTokens * (8 * NT + 1) * 4;
-  return tiles + acc + 2 * kRouterTokens * 4 + MOE_MAX_EXPERTS * 4;
+  constexpr size_t tiles = (size_t)(TOK + 8 * NT) * ld * 4;
+  constexpr size_t acc = (size_t)TOK * (8 * NT + 1) * 4;
+  return tiles + acc + 2 * TOK * 4 + MOE_MAX_EXPERTS * 4;
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kRouterThreads)
+template <int NT, int TOK>
+__global__ void __launch_bounds__(2 * TOK)
     router_f32_kernel(const float* __restrict__ x, const float* __restrict__ wg,
                       const float* __restrict__ bias, int T, int d, int E, int k,
                       int32_t* __restrict__ idx_out, float* __restrict__ w_out,
@@ -268,25 +273,26 @@ __global__ void __launch_bounds__(kRouterThreads)
   constexpr int ldS = EP + 1;
   extern __shared__ __align__(16) unsigned char smem[];
   float* xs = reinterpret_cast<float*>(smem);
-  float* ws = xs + kRouterTokens * ld;
+  constexpr int kThr = 2 * TOK;
+  float* ws = xs + TOK * ld;
   float* S = ws + EP * ld;
-  float* s_m = S + kRouterTokens * ldS;
-  float* s_inv = s_m + kRouterTokens;
-  int* s_cnt = reinterpret_cast<int*>(s_inv + kRouterTokens);
-  const int tok0 = blockIdx.x * kRouterTokens;
-  // thread -> (token, expert parity): token = tid % 64, experts tid/64 + 2*i
-  const int tt = threadIdx.x & 63, eh = threadIdx.x >> 6;
+  float* s_m = S + TOK * ldS;
+  float* s_inv = s_m + TOK;
+  int* s_cnt = reinterpret_cast<int*>(s_inv + TOK);
+  const int tok0 = blockIdx.x * TOK;
+  // thread -> (token, expert group): token = tid % TOK, experts eh + 2*i
+  const int tt = threadIdx.x % TOK, eh = threadIdx.x / TOK;
   float acc[4 * NT];
 #pragma unroll
   for (int i = 0; i < 4 * NT; ++i) acc[i] = 0.f;
   for (int kof = 0; kof < d; kof += kRouterBKf) {
     __syncthreads();
-    for (int c = threadIdx.x; c < kRouterTokens * kRouterBKf; c += kRouterThreads) {
+    for (int c = threadIdx.x; c < TOK * kRouterBKf; c += kThr) {
       const int r = c / kRouterBKf, cc = c % kRouterBKf;
       const int t = tok0 + r;
       xs[r * ld + cc] = (t < T && kof + cc < d) ? x[(size_t)t * d + kof + cc] : 0.f;
     }
-    for (int c = threadIdx.x; c < EP * kRouterBKf; c += kRouterThreads) {
+    for (int c = threadIdx.x; c < EP * kRouterBKf; c += kThr) {
       const int r = c / kRouterBKf, cc = c % kRouterBKf;
       ws[r * ld + cc] = (r < E && kof + cc < d) ? wg[(size_t)r * d + kof + cc] : 0.f;
     }
@@ -301,7 +307,7 @@ __global__ void __launch_bounds__(kRouterThreads)
 #pragma unroll
   for (int i = 0; i < 4 * NT; ++i) S[tt * ldS + eh + 2 * i] = acc[i];
   __syncthreads();
-  router_epilogue(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
+  router_epilogue<TOK>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                   aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts, s_m,
                   s_inv, s_cnt);
 }
@@ -312,25 +318,25 @@ inline int router_nt(int E) {
   return ep / 8;
 }
 
-template <int NT>
+template <int NT, int TOK>
 cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, int T, int d, int E,
                              int k, bool bf16, int32_t* idx, float* w, float* logits, float* probs,
                              float* aux, int32_t* tile_counts, cudaStream_t st) {
-  const int grid = ceil_div(T, kRouterTokens);
+  const int grid = ceil_div(T, TOK);
   if (bf16) {
-    const size_t sm = router_smem_bytes_bf16<NT>();
-    cudaError_t e = cudaFuncSetAttribute(router_bf16_kernel<NT>,
+    const size_t sm = router_smem_bytes_bf16<NT, TOK>();
+    cudaError_t e = cudaFuncSetAttribute(router_bf16_kernel<NT, TOK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    router_bf16_kernel<NT><<<grid, kRouterThreads, sm, st>>>(
+    router_bf16_kernel<NT, TOK><<<grid, 2 * TOK, sm, st>>>(
         static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wg), bias, T, d,
         E, k, idx, w, logits, probs, aux, tile_counts);
   } else {
-    const size_t sm = router_smem_bytes_f32<NT>();
-    cudaError_t e = cudaFuncSetAttribute(router_f32_kernel<NT>,
+    const size_t sm = router_smem_bytes_f32<NT, TOK>();
+    cudaError_t e = cudaFuncSetAttribute(router_f32_kernel<NT, TOK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    router_f32_kernel<NT><<<grid, kRouterThreads, sm, st>>>(
+    router_f32_kernel<NT, TOK><<<grid, 2 * TOK, sm, st>>>(
         static_cast<const float*>(x), static_cast<const float*>(wg), bias, T, d, E, k, idx, w,
         logits, probs, aux, tile_counts);
   }
@@ -341,14 +347,24 @@ inline cudaError_t launch_router(const void* x, const void* wg, const float* bia
                                  int E, int k, bool bf16, int32_t* idx, float* w, float* logits,
                                  float* probs, float* aux, cudaStream_t st,
                                  int32_t* tile_counts = nullptr) {
+#define MOE_ROUTER_CASE(NT_)                                                                     \
+  case NT_:                                                                                      \
+    return router_tokens(E) == 32                                                                \
+               ? launch_router_nt<NT_, 32>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, \
+                                           aux, tile_counts, st)                                 \
+               : launch_router_nt<NT_, 64>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, \
+                                           aux, tile_counts, st);
   switch (router_nt(E)) {
-    case 1: return launch_router_nt<1>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
-    case 2: return launch_router_nt<2>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
-    case 4: return launch_router_nt<4>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
-    case 8: return launch_router_nt<8>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
-    case 16: return launch_router_nt<16>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
-    default: return launch_router_nt<32>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, tile_counts, st);
+    MOE_ROUTER_CASE(1)
+    MOE_ROUTER_CASE(2)
+    MOE_ROUTER_CASE(4)
+    MOE_ROUTER_CASE(8)
+    MOE_ROUTER_CASE(16)
+    default:
+      return launch_router_nt<32, 64>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux,
+                                      tile_counts, st);
   }
+#undef MOE_ROUTER_CASE
 }
 
 }  // namespace moe

@@ -37,10 +37,12 @@ def test_capacity_rule(L):
 
 
 def test_aux_rows(L):
+    # one row per router block of 32 tokens
     assert L.moe_route_aux_rows(0) == 0
     assert L.moe_route_aux_rows(1) == 1
-    assert L.moe_route_aux_rows(64) == 1
-    assert L.moe_route_aux_rows(65) == 2
+    assert L.moe_route_aux_rows(32) == 1
+    assert L.moe_route_aux_rows(33) == 2
+    assert L.moe_route_aux_rows(8192) == 256
 
 
 def _nullp():
