@@ -7,8 +7,8 @@
 //
 // One CTA owns TOK = 32 or 64 tokens (warps of 16), chosen by the expert count.  The logits GEMM is narrow (N = E
 // <= 256), so bf16 runs on warp-level mma.sync m16n8k16 tiles fed by cp.async
-// through a deep shared-memory ring (up to 6 stages, so enough bytes of x are
-// in flight to stream it at HBM speed); fp32 runs on FFMA.  The 64 x E logits
+// through a shared-memory ring, 8 warps per CTA splitting tokens and K (see
+// router_bf16_kernel); fp32 runs on FFMA.  The 64 x E logits
 // tile then goes through shared memory to a thread-per-token epilogue (no
 // cross-lane reductions on the critical path): each thread reduces its own
 // row for max and sum, and selects its top-k by repeated arg-max.  Outputs
@@ -50,7 +50,8 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, cons
 
 // Thread-per-token epilogue over the logits tile S[TOK][ldS] (bias not yet
 // added; S is modified).  k == 0 writes logits only (expert-choice pre-pass).
-// s_m / s_inv: TOK floats each of shared scratch; s_cnt: MOE_MAX_EXPERTS ints.
+// s_m / s_inv: TOK floats each of shared scratch; s_cnt: MOE_MAX_EXPERTS ints;
+// s_part: blockDim.x floats.
 // tile_counts (nullable): this CTA's row of per-expert selection counts, the
 // dispatch histogram of its TOK*k assignments.
 template <int TOK>
@@ -59,7 +60,7 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
                                 float* __restrict__ w_out, float* __restrict__ logits_out,
                                 float* __restrict__ probs_out, float* __restrict__ aux_row,
                                 int32_t* __restrict__ tile_counts, float* s_m, float* s_inv,
-                                int* s_cnt) {
+                                int* s_cnt, float* s_part) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int ntok = min(TOK, T - tok0);
   if (bias) {
@@ -92,10 +93,20 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
   if (k == 0) return;
   if (tile_counts)
     for (int e = tid; e < E; e += nthr) s_cnt[e] = 0;
-  if (aux_row) {  // fixed-order column sums of g over this CTA's tokens
+  if (aux_row) {
+    // column sums of g over this CTA's tokens: G row groups per expert sum
+    // strided rows, then one thread per expert adds the G partials in order
+    const int G = max(1, nthr / E);
+    if (tid < G * E) {
+      const int e = tid % E, gi = tid / E;
+      float acc = 0.f;
+      for (int r = gi; r < ntok; r += G) acc += expf(S[r * ldS + e] - s_m[r]) * s_inv[r];
+      s_part[gi * E + e] = acc;
+    }
+    __syncthreads();
     for (int e = tid; e < E; e += nthr) {
       float acc = 0.f;
-      for (int r = 0; r < ntok; ++r) acc += expf(S[r * ldS + e] - s_m[r]) * s_inv[r];
+      for (int gi = 0; gi < G; ++gi) acc += s_part[gi * E + e];
       aux_row[e] = acc;
     }
   }
@@ -131,63 +142,82 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
   }
 }
 
-// Pipeline depth: up to 6 stages within ~200 KB of shared memory.
-template <int NT, int TOK>
-constexpr int router_stages() {
-  constexpr size_t stage = (size_t)(TOK + 8 * NT) * kRouterLd * 2;
-  constexpr size_t fit = (200u * 1024u) / stage;
-  return fit >= 6 ? 6 : (fit < 2 ? 2 : (int)fit);
-}
+// bf16 router CTA: 8 warps = TOK/16 token groups x K groups.  Each stage holds
+// one 64-column chunk per K group; every warp runs its 16 tokens over its own
+// chunk, and the K groups' partial logits are summed in a fixed order at the
+// end (more warps per SM than one warp per token group: the small GEMM and
+// the epilogue are latency-bound, not bandwidth-bound).
+constexpr int kRouterWarps = 8;
+constexpr int kRouterThreadsBf16 = 32 * kRouterWarps;
 
-// Shared memory: max(stage ring, logits tile) + epilogue scratch.
+template <int NT, int TOK>
+struct RouterBf16 {
+  static constexpr int EP = 8 * NT;
+  static constexpr int TG = TOK / 16;            // token groups
+  static constexpr int KG = kRouterWarps / TG;   // K groups
+  static constexpr int SBK = kRouterBK * KG;     // columns per stage
+  static constexpr int LD = SBK + 8;             // bf16 row pitch (conflict-free fragments)
+  static constexpr int STAGE_ELEMS = (TOK + EP) * LD;
+  static constexpr size_t STAGE_BYTES = (size_t)STAGE_ELEMS * 2;
+  // up to 8 stages within ~110 KB (two CTAs per SM); at least 3 while they fit
+  // in 200 KB; 2 for the widest expert counts
+  static constexpr size_t FIT2 = (110u * 1024u) / STAGE_BYTES;
+  static constexpr size_t FIT1 = (200u * 1024u) / STAGE_BYTES;
+  static constexpr int STAGES =
+      FIT2 >= 3 ? (FIT2 > 8 ? 8 : (int)FIT2) : (FIT1 >= 3 ? 3 : (FIT1 < 2 ? 2 : (int)FIT1));
+  static constexpr size_t RING = (size_t)STAGES * STAGE_BYTES;
+  static constexpr int LDS = EP + 1;
+  static constexpr size_t PART = (size_t)KG * TOK * LDS * 4;  // per-K-group partial logits
+  static constexpr size_t TILE = (size_t)TOK * LDS * 4;
+  static constexpr size_t MAIN = RING > PART + TILE ? RING : PART + TILE;
+  static constexpr size_t SMEM = MAIN + 2 * TOK * 4 + MOE_MAX_EXPERTS * 4 + kRouterThreadsBf16 * 4;
+  static_assert(SMEM <= 227 * 1024, "router shared memory");
+};
+
 template <int NT, int TOK>
 constexpr size_t router_smem_bytes_bf16() {
-  constexpr size_t ring = (size_t)router_stages<NT, TOK>() * (TOK + 8 * NT) * kRouterLd * 2;
-  constexpr size_t tile = (size_t)TOK * (8 * NT + 1) * 4;
-  constexpr size_t main = ring > tile ? ring : tile;
-  return main + 2 * TOK * 4 + MOE_MAX_EXPERTS * 4;
+  return RouterBf16<NT, TOK>::SMEM;
 }
 
 template <int NT, int TOK>
-__global__ void __launch_bounds__(2 * TOK)
+__global__ void __launch_bounds__(kRouterThreadsBf16)
     router_bf16_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wg,
                        const float* __restrict__ bias, int T, int d, int E, int k,
                        int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                        float* __restrict__ logits_out, float* __restrict__ probs_out,
                        float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts) {
-  constexpr int EP = 8 * NT;
+  using C = RouterBf16<NT, TOK>;
+  constexpr int EP = C::EP, LD = C::LD, SBK = C::SBK, STAGES = C::STAGES;
   extern __shared__ __align__(16) unsigned char smem[];
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem);
-  constexpr int kThr = 2 * TOK;
-  constexpr int stage_elems = (TOK + EP) * kRouterLd;
-  constexpr int STAGES = router_stages<NT, TOK>();
-  constexpr size_t ring_bytes = (size_t)STAGES * stage_elems * 2;
-  constexpr size_t tile_bytes = (size_t)TOK * (EP + 1) * 4;
-  constexpr size_t main_bytes = ring_bytes > tile_bytes ? ring_bytes : tile_bytes;
-  float* s_m = reinterpret_cast<float*>(smem + main_bytes);
+  float* s_m = reinterpret_cast<float*>(smem + C::MAIN);
   float* s_inv = s_m + TOK;
   int* s_cnt = reinterpret_cast<int*>(s_inv + TOK);
+  float* s_part = reinterpret_cast<float*>(s_cnt + MOE_MAX_EXPERTS);
 
   const int tok0 = blockIdx.x * TOK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nk = d / kRouterBK;
+  const int tg = warp % C::TG, kg = warp / C::TG;
+  const int nsc = (d + SBK - 1) / SBK;  // stages of SBK columns (the last may be partial)
 
-  auto load_stage = [&](int stage, int kc) {
-    __nv_bfloat16* xs = ring + stage * stage_elems;
-    __nv_bfloat16* ws = xs + TOK * kRouterLd;
-    const int kof = kc * kRouterBK;
-    for (int c = threadIdx.x; c < TOK * 8; c += kThr) {
-      const int r = c >> 3, ch = c & 7;
-      const int t = tok0 + r;
-      const bool ok = t < T;
-      const __nv_bfloat16* src = x + (size_t)(ok ? t : 0) * d + kof + ch * 8;
-      cp_async16(xs + r * kRouterLd + ch * 8, src, ok);
+  auto load_stage = [&](int stage, int sc) {
+    __nv_bfloat16* xs = ring + stage * C::STAGE_ELEMS;
+    __nv_bfloat16* ws = xs + TOK * LD;
+    const int kof = sc * SBK;
+    constexpr int CH = SBK / 8;  // 16-byte chunks per row
+    for (int c = threadIdx.x; c < TOK * CH; c += kRouterThreadsBf16) {
+      const int r = c / CH, ch = c % CH;
+      const int t = tok0 + r, col = kof + ch * 8;
+      const bool ok = t < T && col < d;
+      const __nv_bfloat16* src = ok ? x + (size_t)t * d + col : x;
+      cp_async16(xs + r * LD + ch * 8, src, ok);
     }
-    for (int c = threadIdx.x; c < EP * 8; c += kThr) {
-      const int r = c >> 3, ch = c & 7;
-      const bool ok = r < E;
-      const __nv_bfloat16* src = wg + (size_t)(ok ? r : 0) * d + kof + ch * 8;
-      cp_async16(ws + r * kRouterLd + ch * 8, src, ok);
+    for (int c = threadIdx.x; c < EP * CH; c += kRouterThreadsBf16) {
+      const int r = c / CH, ch = c % CH;
+      const int col = kof + ch * 8;
+      const bool ok = r < E && col < d;
+      const __nv_bfloat16* src = ok ? wg + (size_t)r * d + col : wg;
+      cp_async16(ws + r * LD + ch * 8, src, ok);
     }
   };
 
@@ -199,32 +229,32 @@ __global__ void __launch_bounds__(2 * TOK)
 
 #pragma unroll
   for (int s = 0; s < STAGES - 1; ++s) {
-    if (s < nk) load_stage(s, s);
+    if (s < nsc) load_stage(s, s);
     cp_async_commit();
   }
   const int g = lane >> 2, c4 = lane & 3;
-  for (int kc = 0; kc < nk; ++kc) {
+  for (int sc = 0; sc < nsc; ++sc) {
     cp_async_wait<STAGES - 2>();
     __syncthreads();
     {
-      const int nxt = kc + STAGES - 1;
-      if (nxt < nk) load_stage(nxt % STAGES, nxt);
+      const int nxt = sc + STAGES - 1;
+      if (nxt < nsc) load_stage(nxt % STAGES, nxt);
       cp_async_commit();
     }
-    const __nv_bfloat16* xs = ring + (kc % STAGES) * stage_elems;
-    const __nv_bfloat16* ws = xs + TOK * kRouterLd;
-    const __nv_bfloat16* xw = xs + warp * 16 * kRouterLd;
+    const __nv_bfloat16* xs = ring + (sc % STAGES) * C::STAGE_ELEMS;
+    const __nv_bfloat16* ws = xs + TOK * LD + kg * kRouterBK;
+    const __nv_bfloat16* xw = xs + tg * 16 * LD + kg * kRouterBK;
 #pragma unroll
     for (int kk = 0; kk < kRouterBK; kk += 16) {
       uint32_t a[4];
-      a[0] = *reinterpret_cast<const uint32_t*>(xw + g * kRouterLd + kk + 2 * c4);
-      a[1] = *reinterpret_cast<const uint32_t*>(xw + (g + 8) * kRouterLd + kk + 2 * c4);
-      a[2] = *reinterpret_cast<const uint32_t*>(xw + g * kRouterLd + kk + 8 + 2 * c4);
-      a[3] = *reinterpret_cast<const uint32_t*>(xw + (g + 8) * kRouterLd + kk + 8 + 2 * c4);
+      a[0] = *reinterpret_cast<const uint32_t*>(xw + g * LD + kk + 2 * c4);
+      a[1] = *reinterpret_cast<const uint32_t*>(xw + (g + 8) * LD + kk + 2 * c4);
+      a[2] = *reinterpret_cast<const uint32_t*>(xw + g * LD + kk + 8 + 2 * c4);
+      a[3] = *reinterpret_cast<const uint32_t*>(xw + (g + 8) * LD + kk + 8 + 2 * c4);
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         uint32_t b[2];
-        const __nv_bfloat16* wr = ws + (n * 8 + g) * kRouterLd + kk + 2 * c4;
+        const __nv_bfloat16* wr = ws + (n * 8 + g) * LD + kk + 2 * c4;
         b[0] = *reinterpret_cast<const uint32_t*>(wr);
         b[1] = *reinterpret_cast<const uint32_t*>(wr + 8);
         mma_bf16_16816(acc[n], a, b);
@@ -232,23 +262,35 @@ __global__ void __launch_bounds__(2 * TOK)
     }
   }
   cp_async_wait<0>();
-  __syncthreads();  // ring no longer read: the logits tile may alias it
+  __syncthreads();  // ring no longer read: the partial tiles may alias it
 
-  float* S = reinterpret_cast<float*>(smem);
-  constexpr int ldS = EP + 1;
+  constexpr int ldS = C::LDS;
+  float* P = reinterpret_cast<float*>(smem);  // [KG][TOK][ldS]
+  float* S = P + C::KG * TOK * ldS;           // [TOK][ldS]
+  {
+    float* Pk = P + kg * TOK * ldS;
 #pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    const int col = n * 8 + 2 * c4;
-    const int r0 = warp * 16 + g;
-    S[r0 * ldS + col] = acc[n][0];
-    S[r0 * ldS + col + 1] = acc[n][1];
-    S[(r0 + 8) * ldS + col] = acc[n][2];
-    S[(r0 + 8) * ldS + col + 1] = acc[n][3];
+    for (int n = 0; n < NT; ++n) {
+      const int col = n * 8 + 2 * c4;
+      const int r0 = tg * 16 + g;
+      Pk[r0 * ldS + col] = acc[n][0];
+      Pk[r0 * ldS + col + 1] = acc[n][1];
+      Pk[(r0 + 8) * ldS + col] = acc[n][2];
+      Pk[(r0 + 8) * ldS + col + 1] = acc[n][3];
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < TOK * EP; i += kRouterThreadsBf16) {
+    const int r = i / EP, e = i % EP;
+    float v = P[r * ldS + e];
+#pragma unroll
+    for (int q = 1; q < C::KG; ++q) v += P[(q * TOK + r) * ldS + e];  // fixed K-group order
+    S[r * ldS + e] = v;
   }
   __syncthreads();
   router_epilogue<TOK>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
-                  aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts, s_m,
-                  s_inv, s_cnt);
+                       aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
+                       s_m, s_inv, s_cnt, s_part);
 }
 
 // fp32 router: FFMA over 32-wide d chunks, same epilogue.
@@ -258,7 +300,7 @@ constexpr size_t router_smem_bytes_f32() {
   constexpr size_t ld = kRouterBKf + 1;
   constexpr size_t tiles = (size_t)(TOK + 8 * NT) * ld * 4;
   constexpr size_t acc = (size_t)TOK * (8 * NT + 1) * 4;
-  return tiles + acc + 2 * TOK * 4 + MOE_MAX_EXPERTS * 4;
+  return tiles + acc + 2 * TOK * 4 + MOE_MAX_EXPERTS * 4 + 2 * TOK * 4;
 }
 
 template <int NT, int TOK>
@@ -279,6 +321,7 @@ __global__ void __launch_bounds__(2 * TOK)
   float* s_m = S + TOK * ldS;
   float* s_inv = s_m + TOK;
   int* s_cnt = reinterpret_cast<int*>(s_inv + TOK);
+  float* s_part = reinterpret_cast<float*>(s_cnt + MOE_MAX_EXPERTS);
   const int tok0 = blockIdx.x * TOK;
   // thread -> (token, expert group): token = tid % TOK, experts eh + 2*i
   const int tt = threadIdx.x % TOK, eh = threadIdx.x / TOK;
@@ -308,8 +351,8 @@ __global__ void __launch_bounds__(2 * TOK)
   for (int i = 0; i < 4 * NT; ++i) S[tt * ldS + eh + 2 * i] = acc[i];
   __syncthreads();
   router_epilogue<TOK>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
-                  aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts, s_m,
-                  s_inv, s_cnt);
+                       aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
+                       s_m, s_inv, s_cnt, s_part);
 }
 
 inline int router_nt(int E) {
@@ -328,7 +371,7 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     cudaError_t e = cudaFuncSetAttribute(router_bf16_kernel<NT, TOK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    router_bf16_kernel<NT, TOK><<<grid, 2 * TOK, sm, st>>>(
+    router_bf16_kernel<NT, TOK><<<grid, kRouterThreadsBf16, sm, st>>>(
         static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wg), bias, T, d,
         E, k, idx, w, logits, probs, aux, tile_counts);
   } else {
