@@ -196,6 +196,18 @@ def run_gpu(args, cfg):
     for _ in range(max(3, args.warmup)):
         layer(x, y=y)
     torch.cuda.synchronize()
+    # the step is replayed from a CUDA graph: one launch per step, no host work
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer(x, y=y)
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        layer(x, y=y)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
 
     clocks = ClockSampler(local_rank)
     clocks.start()
@@ -208,13 +220,23 @@ def run_gpu(args, cfg):
     for i in range(K):
         flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
-        layer(x, y=y)
+        graph.replay()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     local_s = sum(step_ms) / 1e3
+    # the same step launched eagerly through the API, for comparison
+    eager = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(min(K, 20))]
+    for i, (a, b) in enumerate(eager):
+        flush.fill_(i & 0xFF)
+        a.record(stream)
+        layer(x, y=y)
+        b.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = sum(a.elapsed_time(b) for a, b in eager) / len(eager)
 
     # per-stage breakdown through the individual entry points (same kernels)
     stages = stage_breakdown(moe, torch, cfg, x, w, flush, stream, min(K, 50)) if not ec else {}
@@ -239,7 +261,9 @@ def run_gpu(args, cfg):
         "config": {"workload": describe(cfg), "T_per_gpu": cfg.T, "d_model": cfg.d, "d_ff": cfg.F,
                    "experts": cfg.E, "k": cfg.k, "routing": cfg.routing,
                    "l2": "flushed between timed steps (256 MiB write)",
+                   "launch": "CUDA graph replay of moe_layer_forward (one graph launch per step)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "ms_per_step_eager_launch": eager_ms,
         "active_tflops": tflops,
         "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
                               "sustained": tflops / peaks["bf16_tflops_sustained"],
