@@ -305,7 +305,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = S.tmem_base;
-  const int total = S.cum[E] * n_tiles;
+  // Work units.  A down launch whose last wave would be partly empty splits each
+  // tile of that wave into two 128-column halves (N = 128 MMAs on the first half
+  // of the loaded B tile), so the wave takes half as long.
+  const int total_tiles = S.cum[E] * n_tiles;
+  int full_units = total_tiles, split_tiles = 0;
+  if (!GATEUP && BN == 256) {
+    const int rem = total_tiles % (int)gridDim.x;
+    if (rem > 0 && 2 * rem <= (int)gridDim.x) {
+      full_units = total_tiles - rem;
+      split_tiles = rem;
+    }
+  }
+  const int total = full_units + 2 * split_tiles;
+  // unit -> tile coordinates, first output column inside the tile, column count
+  auto unit_at = [&](int u, TileCoord& c, int& col_off, int& width) {
+    if (u < full_units) {
+      c = map_tile(S, E, n_tiles, u);
+      col_off = 0;
+      width = kTileN;
+    } else {
+      const int v = u - full_units;
+      c = map_tile(S, E, n_tiles, full_units + (v >> 1));
+      col_off = (v & 1) * (kTileN / 2);
+      width = kTileN / 2;
+    }
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -314,8 +339,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_phase = 0;  // per-stage bits: loads issued, their parity
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
-        const TileCoord c = map_tile(S, E, n_tiles, tile);
-        const int brow = c.e * N + c.nt * kTileN;
+        TileCoord c;
+        int col_off, width;
+        unit_at(tile, c, col_off, width);
+        const int brow = c.e * N + c.nt * kTileN + col_off;
         int tok[4] = {0, 0, 0, 0};  // GATHER: source rows of tile rows 4 * lane + i
         if (GATHER) {               // (rows past the segment read row 0; never stored)
 #pragma unroll
@@ -335,7 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           unsigned char* sA = ring + (size_t)stage * STAGE_BYTES;
           unsigned char* sB = sA + A_BYTES;
-          if (lane == 0) mbar_arrive_expect_tx(&S.full[stage], STAGE_BYTES);
+          // a half unit of the down GEMM loads only the 128 B rows it uses (tmB1)
+          const bool half_unit = !GATEUP && tile >= full_units;
+          if (lane == 0)
+            mbar_arrive_expect_tx(&S.full[stage], half_unit ? STAGE_BYTES - B_BYTES / 2 : STAGE_BYTES);
           if (GATHER) {
             __syncwarp();  // the expected byte count is set before any gather lands
             tma_gather4(sA + lane * 4 * 128, &tmA, &S.full[stage], kb * BK, tok[0], tok[1], tok[2],
@@ -347,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
               tma_load_2d(sB + B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, brow);
             } else {
-              tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
+              tma_load_2d(sB, half_unit ? &tmB1 : &tmB0, &S.full[stage], kb * BK, brow);
             }
           }
           issued |= 1u << stage;
@@ -378,12 +408,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(BM, BN);
+      constexpr uint32_t idesc_full = make_idesc_bf16(BM, BN);
+      constexpr uint32_t idesc_half = make_idesc_bf16(BM, BN / 2);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const uint32_t idesc = tile < full_units ? idesc_full : idesc_half;
         if (!mbar_wait(&S.tmem_empty[acc], acc_phase ^ 1u, abort_flag, kErrMma)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -432,13 +464,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileCoord c = map_tile(S, E, n_tiles, tile);
+      TileCoord c;
+      int col_off, width;
+      unit_at(tile, c, col_off, width);
       if (!mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       const int row = c.row0 + row_in_tile;
       const bool valid = row < c.row_end;
-      const int n0 = c.nt * kTileN;
+      const int n0 = c.nt * kTileN + col_off;
       if (GATEUP) {
         __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
 #pragma unroll 1
@@ -467,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float wgt = valid ? topk_w[a] : 0.f;
         float* yrow = static_cast<float*>(out) + (size_t)(a / kslots) * N;
 #pragma unroll 1
-        for (int cc = 0; cc < kTileN; cc += 32) {
+        for (int cc = 0; cc < width; cc += 32) {
           uint32_t v[32];
           MOE_TMEM_LD32(taddr + cc, v);
           tmem_ld_wait();
@@ -484,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         float* Y = static_cast<float*>(out);
 #pragma unroll 1
-        for (int cc = 0; cc < kTileN; cc += 32) {
+        for (int cc = 0; cc < width; cc += 32) {
           uint32_t v[32];
           MOE_TMEM_LD32(taddr + cc, v);
           tmem_ld_wait();
@@ -650,11 +684,11 @@ inline cudaError_t launch_down_tc(const __nv_bfloat16* h, const int32_t* offsets
                                   float* y_perm, cudaStream_t s) {
   const int sms = tc::sm_count();
   const int bn = tc::choose_bn(R, E, d, false, sms);
-  CUtensorMap m[3];
+  CUtensorMap m[3];  // A, B, and B with a half-height box for split tail tiles
   if (!tc::make_map(&m[0], h, (uint64_t)R, (uint64_t)F, tc::BM) ||
-      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, bn))
+      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, bn) ||
+      !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, bn / 2))
     return cudaErrorInvalidValue;
-  m[2] = m[1];
   return tc::launch<false>(m, bn, offsets, R, E, d, F, y_perm, sms, s);
 }
 
@@ -666,11 +700,12 @@ inline cudaError_t launch_down_combine_tc(const __nv_bfloat16* h, const int32_t*
                                           const int32_t* perm, const float* topk_w, int k, float* y,
                                           cudaStream_t s) {
   const int sms = tc::sm_count();
-  CUtensorMap m[2];
+  CUtensorMap m[3];  // A, B, and B with a half-height box for split tail tiles
   if (!tc::make_map(&m[0], h, (uint64_t)R, (uint64_t)F, tc::BM) ||
-      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, 256))
+      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, 256) ||
+      !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, 128))
     return cudaErrorInvalidValue;
-  return tc::launch_bn<false, 256, true>(m[0], m[1], m[1], offsets, R, E, d, F, y, sms, s, perm,
+  return tc::launch_bn<false, 256, true>(m[0], m[1], m[2], offsets, R, E, d, F, y, sms, s, perm,
                                          topk_w, k);
 }
 

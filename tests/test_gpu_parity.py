@@ -133,6 +133,8 @@ EXPERT_CASES = [
     ("bf16_one_expert", [300], 64, 192, "bf16"),
     ("bf16_e64_skew", [400 // (e + 1) for e in range(64)], 128, 128, "bf16"),
     ("f32_ragged", [70, 0, 5, 131], 64, 128, "f32"),
+    # 197 row blocks on <= 148 CTAs: the down GEMM splits its last partial wave
+    ("bf16_tail_split", [20000, 5000], 256, 128, "bf16"),
 ]
 
 
