@@ -15,7 +15,8 @@
 //              tcgen05.mma kind::f16 (M=128, N=256, K=16, fp32 accumulate)
 //              into one of two TMEM accumulators and commits to mbarriers;
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator (thread = row), SwiGLU
-//              or plain fp32, vector stores masked at the segment end.
+//              or plain fp32, transposed through shared memory and stored as
+//              whole row segments, masked at the segment end.
 // For gate/up the B tile stacks 128 rows of W_gate over the same 128 rows of
 // W_up, so one N=256 instruction produces both halves of the SwiGLU.
 // Tiles are (expert, n-block, 128-row block), enumerated on the device from
@@ -52,8 +53,13 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
 };
 
+constexpr int kStagePitch = 36;  // floats per row of an epilogue warp's 32 x 32 staging tile
+
 template <int STAGES>
 struct Smem {  // lives after the 1024-aligned stage ring
+  // per epilogue warp: a 32-row chunk of the accumulator, transposed through
+  // shared memory so that global stores cover whole row segments
+  alignas(16) float stage_out[4][32 * kStagePitch];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t tmem_full[2];
@@ -140,6 +146,28 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// As tma_load_2d, written to the same offset (and signalling the mbarrier at
+// the same offset) in every CTA of the cluster named in cta_mask.
+__device__ __forceinline__ void tma_load_2d_mcast(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                  int x, int y, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::"
+      "cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -155,6 +183,16 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
+      : "memory");
+}
+
+// Arrive on the mbarrier at this offset in every CTA of cta_mask when this
+// thread's issued MMAs complete.
+__device__ __forceinline__ void tc_commit_mcast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 
@@ -207,7 +245,8 @@ struct TileCoord {
 // varies fastest and the n-block slowest, so the CTAs of one wave share each
 // weight tile (read from HBM once) while the expert's rows stay in L2.
 template <class SmemT>
-__device__ __forceinline__ TileCoord map_tile(const SmemT& S, int E, int n_tiles, int tile) {
+__device__ __forceinline__ TileCoord map_tile(const SmemT& S, int E, int n_tiles, int tile,
+                                              int unit_rows = BM) {
   TileCoord c;
   int lo = 0, hi = E;  // S.cum[lo] * n_tiles <= tile < S.cum[hi] * n_tiles
   while (hi - lo > 1) {
@@ -220,7 +259,7 @@ __device__ __forceinline__ TileCoord map_tile(const SmemT& S, int E, int n_tiles
   const int nt = local / m_tiles;
   c.e = lo;
   c.nt = nt;
-  c.row0 = S.off[lo] + (local - nt * m_tiles) * BM;
+  c.row0 = S.off[lo] + (local - nt * m_tiles) * unit_rows;
   c.row_end = S.off[lo + 1];
   return c;
 }
@@ -241,7 +280,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // GATHER (gate/up only): row r of A is row gsrc[r] / gdiv of the tensor behind
 // tmA (x itself, mapped with a one-row box) instead of row r; each producer
 // lane brings 4 of the tile's 128 rows per k-block with one TMA gather4.
-template <bool GATEUP, int BN, bool COMBINE = false, bool GATHER = false>
+// MCAST: launched in clusters of 2.  The two CTAs take the two 128-row halves
+// of a 256-row block for the same weight tile; each loads half of the B tile
+// and multicasts it into both CTAs' shared memory (half the weight-tile L2
+// requests).  A stage is refilled only after both CTAs' MMAs released it: each
+// MMA thread commits to the empty barriers of both CTAs (arrival count 2).
+template <bool GATEUP, int BN, bool COMBINE = false, bool GATHER = false, bool MCAST = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets,
@@ -263,6 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kTileN = GATEUP ? BN / 2 : BN;  // output columns per tile
+  constexpr int kUnitRows = MCAST ? 2 * BM : BM;  // rows of one work unit (a cluster's)
+  const uint32_t crank = MCAST ? cluster_ctarank() : 0u;
+  const int unit0 = MCAST ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustride = MCAST ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  constexpr uint16_t kPair = 0x3;
   const int n_tiles = (N + kTileN - 1) / kTileN;
   const int num_kb = K / BK;
 
@@ -271,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
+      mbar_init(&S.empty[s], MCAST ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.tmem_full[b], 1);
@@ -297,12 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = 0; e < E; ++e) {
       S.cum[e] = cum;
       const int cnt = max(S.off[e + 1] - S.off[e], 0);
-      cum += (cnt + BM - 1) / BM;
+      cum += (cnt + kUnitRows - 1) / kUnitRows;
     }
     S.cum[E] = cum;
   }
   tc_fence_before();
   __syncthreads();
+  if (MCAST) cluster_sync_all();  // the peer's barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = S.tmem_base;
   // Work units.  A down launch whose last wave would be partly empty splits each
@@ -310,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // of the loaded B tile), so the wave takes half as long.
   const int total_tiles = S.cum[E] * n_tiles;
   int full_units = total_tiles, split_tiles = 0;
-  if (!GATEUP && BN == 256) {
+  if (!GATEUP && !MCAST && BN == 256) {
     const int rem = total_tiles % (int)gridDim.x;
     if (rem > 0 && 2 * rem <= (int)gridDim.x) {
       full_units = total_tiles - rem;
@@ -321,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // unit -> tile coordinates, first output column inside the tile, column count
   auto unit_at = [&](int u, TileCoord& c, int& col_off, int& width) {
     if (u < full_units) {
-      c = map_tile(S, E, n_tiles, u);
+      c = map_tile(S, E, n_tiles, u, kUnitRows);
+      c.row0 += (int)crank * BM;  // this CTA's half of the cluster's rows
       col_off = 0;
       width = kTileN;
     } else {
@@ -338,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_phase = 0;  // per-stage bits: loads issued, their parity
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+      for (int tile = unit0; tile < total && !*abort_flag; tile += ustride) {
         TileCoord c;
         int col_off, width;
         unit_at(tile, c, col_off, width);
@@ -373,7 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0) {
             if (!GATHER) tma_load_2d(sA, &tmA, &S.full[stage], kb * BK, c.row0);
-            if (GATEUP) {
+            if (MCAST) {
+              // this CTA's half of B (gate/up: rank 0 the gate rows, rank 1 the up
+              // rows; down: rows brow + rank * BN/2 through the half-height map)
+              tma_load_2d_mcast(sB + crank * (B_BYTES / 2), GATEUP && crank == 0 ? &tmB0 : &tmB1,
+                                &S.full[stage], kb * BK,
+                                GATEUP ? brow : brow + (int)crank * (BN / 2), kPair);
+            } else if (GATEUP) {
               tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
               tma_load_2d(sB + B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, brow);
             } else {
@@ -414,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+      for (int tile = unit0; tile < total && !*abort_flag; tile += ustride) {
         const uint32_t idesc = tile < full_units ? idesc_full : idesc_half;
         if (!mbar_wait(&S.tmem_empty[acc], acc_phase ^ 1u, abort_flag, kErrMma)) break;
         tc_fence_after();
@@ -433,7 +490,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_mma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                        (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(&S.empty[stage]);  // frees the smem stage once these MMAs finish
+          // frees the smem stage once these MMAs finish (in both CTAs when multicasting)
+          if (MCAST) tc_commit_mcast(&S.empty[stage], kPair);
+          else tc_commit(&S.empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -459,18 +518,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    // Each warp owns TMEM lane quarter q (tile rows 32q .. 32q+31, thread = row
+    // when reading TMEM).  A 32-column chunk goes through the warp's staging tile
+    // in shared memory and leaves as whole row segments (4-8 rows per store
+    // instruction instead of 32 scattered 16-byte pieces).
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_in_tile = q * 32 + lane;
+    float* stg = S.stage_out[q];
+    uint32_t* stg_w = reinterpret_cast<uint32_t*>(stg);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = unit0; tile < total; tile += ustride) {
       TileCoord c;
       int col_off, width;
       unit_at(tile, c, col_off, width);
       if (!mbar_wait(&S.tmem_full[acc], acc_phase, abort_flag, kErrEpilogue)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
-      const int row = c.row0 + row_in_tile;
+      const int rbase = c.row0 + q * 32;  // row of lane 0
+      const int row = rbase + lane;
       const bool valid = row < c.row_end;
       const int n0 = c.nt * kTileN + col_off;
       if (GATEUP) {
@@ -481,54 +546,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           MOE_TMEM_LD32(taddr + cc, g);
           MOE_TMEM_LD32(taddr + kTileN + cc, u);
           tmem_ld_wait();
-          if (valid && n0 + cc < N) {
-            uint32_t p[16];
+          uint32_t p[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-              const float h1 =
-                  silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-              p[i] = pack_bf16x2(h0, h1);
+          for (int i = 0; i < 16; ++i) {
+            const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+            const float h1 = silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+            p[i] = pack_bf16x2(h0, h1);
+          }
+          // stage: row `lane` = 32 bf16 = 64 bytes at a pitch of 80 bytes
+          uint4* srow = reinterpret_cast<uint4*>(stg_w + lane * 20);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) srow[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+          __syncwarp();
+          if (n0 + cc < N) {  // 4 lanes per row, 8 rows per store
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int r = j * 8 + (lane >> 2), part = lane & 3;
+              const int grow = rbase + r;
+              if (grow < c.row_end)
+                *reinterpret_cast<uint4*>(H + (size_t)grow * N + n0 + cc + part * 8) =
+                    *reinterpret_cast<const uint4*>(stg_w + r * 20 + part * 4);
             }
-            uint4* dst = reinterpret_cast<uint4*>(H + (size_t)row * N + n0 + cc);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
           }
-        }
-      } else if (COMBINE) {
-        const int a = valid ? perm[row] : 0;
-        const float wgt = valid ? topk_w[a] : 0.f;
-        float* yrow = static_cast<float*>(out) + (size_t)(a / kslots) * N;
-#pragma unroll 1
-        for (int cc = 0; cc < width; cc += 32) {
-          uint32_t v[32];
-          MOE_TMEM_LD32(taddr + cc, v);
-          tmem_ld_wait();
-          if (valid && n0 + cc < N) {
-            float4* dst = reinterpret_cast<float4*>(yrow + n0 + cc);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              atomicAdd(dst + i, make_float4(wgt * __uint_as_float(v[4 * i]),
-                                             wgt * __uint_as_float(v[4 * i + 1]),
-                                             wgt * __uint_as_float(v[4 * i + 2]),
-                                             wgt * __uint_as_float(v[4 * i + 3])));
-          }
+          __syncwarp();
         }
       } else {
+        // COMBINE: this row's token and routing weight, shuffled to the storing lanes
+        const int a = (COMBINE && valid) ? perm[row] : 0;
+        const float wgt = (COMBINE && valid) ? topk_w[a] : 0.f;
+        const int tok = a / kslots;
         float* Y = static_cast<float*>(out);
 #pragma unroll 1
         for (int cc = 0; cc < width; cc += 32) {
           uint32_t v[32];
           MOE_TMEM_LD32(taddr + cc, v);
           tmem_ld_wait();
-          if (valid && n0 + cc < N) {
-            float4* dst = reinterpret_cast<float4*>(Y + (size_t)row * N + n0 + cc);
+          float4* srow = reinterpret_cast<float4*>(stg + lane * kStagePitch);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          for (int i = 0; i < 8; ++i)
+            srow[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          __syncwarp();
+          if (n0 + cc < N) {  // 8 lanes per row, 4 rows per store
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int r = j * 4 + (lane >> 3), part = lane & 7;
+              const int grow = rbase + r;
+              const float4 val = *reinterpret_cast<const float4*>(stg + r * kStagePitch + part * 4);
+              if (COMBINE) {
+                const int rt = __shfl_sync(kFullMask, tok, r);
+                const float rw = __shfl_sync(kFullMask, wgt, r);
+                if (grow < c.row_end)
+                  atomicAdd(reinterpret_cast<float4*>(Y + (size_t)rt * N + n0 + cc + part * 4),
+                            make_float4(rw * val.x, rw * val.y, rw * val.z, rw * val.w));
+              } else if (grow < c.row_end) {
+                *reinterpret_cast<float4*>(Y + (size_t)grow * N + n0 + cc + part * 4) = val;
+              }
+            }
           }
+          __syncwarp();
         }
       }
       tc_fence_before();
@@ -542,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (MCAST) cluster_sync_all();  // the peer no longer writes here or arrives on our barriers
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -610,6 +687,55 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   return cudaGetLastError();
 }
 
+// Cluster-of-2 multicast launch of a 256-wide kernel (MCAST).  The grid is the
+// number of clusters that fit at once (queried once per device), capped by the
+// work, times two.
+inline bool mcast_enabled() {
+  const char* v = getenv("MOE_GROUPED_MCAST");  // "0" turns the cluster path off (tests, A/B)
+  return !(v && v[0] == '0');
+}
+
+template <bool GATEUP, bool COMBINE>
+cudaError_t launch_mcast(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                         const int32_t* offsets, int R, int E, int N, int K, void* out,
+                         cudaStream_t s, const int32_t* perm = nullptr,
+                         const float* topk_w = nullptr, int kslots = 1) {
+  constexpr int BN = 256;
+  constexpr size_t sm = smem_bytes<BN>();
+  auto kern = grouped_tc_kernel<GATEUP, BN, COMBINE, false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  static int max_clusters[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_clusters[dev] == 0) {
+    cfg.gridDim = dim3(2 * 74, 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters[dev] = n > 0 ? n : 1;
+  }
+  constexpr int tile_n = GATEUP ? BN / 2 : BN;
+  const long long units = (long long)((R + 2 * BM - 1) / (2 * BM) + E) * ((N + tile_n - 1) / tile_n);
+  const int clusters = (int)std::min<long long>(max_clusters[dev], units);
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, a, b0, b1, offsets, R, E, N, K, out, perm, topk_w, kslots,
+                         (const __nv_bfloat16*)nullptr, (const int32_t*)nullptr, 1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // MMA width for a launch.  256 everywhere it was measured best (both GEMMs
 // when compute-bound, down always); gate/up with fewer than 256 rows per
 // expert on average is weight-bandwidth-bound and uses 128-wide tiles, twice
@@ -649,6 +775,8 @@ inline cudaError_t launch_gateup_tc(const __nv_bfloat16* x_perm, const int32_t* 
       !tc::make_map(&m[1], w_gate, (uint64_t)E * F, (uint64_t)d, bn / 2) ||
       !tc::make_map(&m[2], w_up, (uint64_t)E * F, (uint64_t)d, bn / 2))
     return cudaErrorInvalidValue;
+  if (bn == 256 && tc::mcast_enabled())
+    return tc::launch_mcast<true, false>(m[0], m[1], m[2], offsets, R, E, F, d, h, s);
   return tc::launch<true>(m, bn, offsets, R, E, F, d, h, sms, s);
 }
 
@@ -684,11 +812,13 @@ inline cudaError_t launch_down_tc(const __nv_bfloat16* h, const int32_t* offsets
                                   float* y_perm, cudaStream_t s) {
   const int sms = tc::sm_count();
   const int bn = tc::choose_bn(R, E, d, false, sms);
-  CUtensorMap m[3];  // A, B, and B with a half-height box for split tail tiles
+  CUtensorMap m[3];  // A, B, and B with a half-height box (tail halves, multicast halves)
   if (!tc::make_map(&m[0], h, (uint64_t)R, (uint64_t)F, tc::BM) ||
       !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, bn) ||
       !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, bn / 2))
     return cudaErrorInvalidValue;
+  if (bn == 256 && tc::mcast_enabled())
+    return tc::launch_mcast<false, false>(m[0], m[1], m[2], offsets, R, E, d, F, y_perm, s);
   return tc::launch<false>(m, bn, offsets, R, E, d, F, y_perm, sms, s);
 }
 
@@ -705,6 +835,9 @@ inline cudaError_t launch_down_combine_tc(const __nv_bfloat16* h, const int32_t*
       !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, 256) ||
       !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, 128))
     return cudaErrorInvalidValue;
+  if (tc::mcast_enabled())
+    return tc::launch_mcast<false, true>(m[0], m[1], m[2], offsets, R, E, d, F, y, s, perm, topk_w,
+                                         k);
   return tc::launch_bn<false, 256, true>(m[0], m[1], m[2], offsets, R, E, d, F, y, sms, s, perm,
                                          topk_w, k);
 }

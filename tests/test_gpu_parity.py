@@ -382,3 +382,18 @@ def test_gateup_gather_bit_identical(moe, torch, case, tile_n, monkeypatch):
     h_gat = moe.moe_grouped_gateup_swiglu_gather(x, src, div, offsets, w["w_gate"], w["w_up"])
     torch.cuda.synchronize()
     assert torch.equal(h_ref.view(torch.int16), h_gat.view(torch.int16))
+
+
+@pytest.mark.parametrize("k", [2, 4])
+def test_cluster_multicast_path_bit_identical(moe, torch, k, monkeypatch):
+    """Multicasting the weight tiles inside clusters of 2 changes only where operand bytes
+    come from, never the arithmetic: outputs equal the single-CTA path bit for bit."""
+    cfg = synth.small_config("mcast", 4000, 256, 512, 8, k, "bf16", seed=60, x_std=1.0, w_std=0.05)
+    inp = synth.make_inputs(cfg)
+    w = dev_weights(inp)
+    x = to_dev(inp.x)
+    y_mc = moe.moe_layer_forward(x, w, k=k).clone()
+    monkeypatch.setenv("MOE_GROUPED_MCAST", "0")
+    y_one = moe.moe_layer_forward(x, w, k=k)
+    torch.cuda.synchronize()
+    assert torch.equal(y_mc, y_one)
