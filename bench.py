@@ -300,11 +300,16 @@ def launches_per_step(cfg) -> int:
 
 
 def stage_breakdown(moe, torch, cfg, x, w, flush, stream, steps):
-    """Average device ms per stage, timed with events between the entry points."""
+    """Average device ms per stage, timed with events between the entry points.
+
+    A spin kernel at the head of each iteration holds the stream while the host
+    queues every stage, so the events bracket device work only, not the
+    Python-side launch gaps between entry points."""
     names = ["route_ms", "permute_ms", "gateup_ms", "down_ms", "combine_ms", "aux_ms"]
     acc = {n: 0.0 for n in names}
     for i in range(steps + 3):
         flush.fill_(i & 0xFF)
+        torch.cuda._sleep(5_000_000)  # ~2.5-4 ms of device time, longer than the host's queueing
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
         evs[0].record(stream)
         r = moe.moe_route(x, w["w_g"], w["bias"], cfg.k)

@@ -45,9 +45,10 @@ constexpr uint32_t kErrProducer = 1u, kErrMma = 2u, kErrEpilogue = 4u, kErrDrain
 
 // Per-width constants: BN is the MMA N (output columns for down; gate + up
 // halves for gate/up).  Narrow tiles leave room for more stages in flight.
-template <int BN>
+// PAIR: 2-CTA MMA, where each CTA holds only its half (BN / 2 rows) of the B tile.
+template <int BN, bool PAIR = false>
 struct Cfg {
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (192 * 1024) / STAGE_BYTES > 8 ? 8 : (192 * 1024) / STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
@@ -71,9 +72,10 @@ struct Smem {  // lives after the 1024-aligned stage ring
   int off[MOE_MAX_EXPERTS + 1];  // segment offsets
 };
 
-template <int BN>
+template <int BN, bool PAIR = false>
 constexpr size_t smem_bytes() {
-  return (size_t)Cfg<BN>::STAGES * Cfg<BN>::STAGE_BYTES + sizeof(Smem<Cfg<BN>::STAGES>) + 1024;
+  using C = Cfg<BN, PAIR>;
+  return (size_t)C::STAGES * C::STAGE_BYTES + sizeof(Smem<C::STAGES>) + 1024;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -95,17 +97,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, acquiring at cluster scope (arrivals made by the peer CTA).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `parity` to complete.  Gives up (false) when the
 // CTA's abort flag is raised or after kWaitTimeoutNs, recording `code`.
+template <bool CLUSTER_SCOPE = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t code) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  auto ready = [&]() { return CLUSTER_SCOPE ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
+  if (ready()) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(a, parity)) return true;
+      if (ready()) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > kWaitTimeoutNs) {
       record_error(code);
@@ -123,6 +139,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Address, in the cluster's shared window, of this CTA's variable `saddr`
+// as placed in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
@@ -154,6 +184,17 @@ __device__ __forceinline__ void tma_load_2d_mcast(void* dst, const CUtensorMap* 
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::"
       "cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
+
+// 2-CTA form: the completion is signalled on `cluster_bar`, which may be the
+// mbarrier of either CTA of the pair (here always the pair's rank-0 CTA).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t cluster_bar,
+                                                 int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar)
       : "memory");
 }
 
@@ -202,6 +243,27 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Pair forms (cta_group::2), issued by the pair's rank-0 CTA.  One MMA of
+// M = 256 reads A rows 0-127 from this CTA's shared memory and rows 128-255
+// from the peer's (same offset), the first and second halves of B's N rows
+// likewise, and writes each CTA's 128 rows of D into that CTA's TMEM.
+__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair_mcast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
       : "memory");
 }
 
@@ -285,7 +347,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // and multicasts it into both CTAs' shared memory (half the weight-tile L2
 // requests).  A stage is refilled only after both CTAs' MMAs released it: each
 // MMA thread commits to the empty barriers of both CTAs (arrival count 2).
-template <bool GATEUP, int BN, bool COMBINE = false, bool GATHER = false, bool MCAST = false>
+// PAIR: launched in clusters of 2 as one 2-CTA MMA unit (tcgen05 cta_group::2)
+// over 256-row blocks.  Each CTA loads its own 128 A rows and its half of the
+// B tile (gate/up: rank 0 the gate rows, rank 1 the up rows), signalling the
+// full barrier of the rank-0 CTA, whose single thread issues M = 256 MMAs and
+// commits to the empty / accumulator-full barriers of both CTAs.  Each CTA's
+// epilogue drains its own TMEM rows and arrives on rank 0's accumulator-empty
+// barrier (4 warps x 2 CTAs).  Per SM this moves 32 KiB instead of 48 KiB of
+// operands into shared memory per k-block for the same 128 x 256 outputs.
+// PAIRING: 0 single CTA, 1 MCAST, 2 PAIR.
+template <bool GATEUP, int BN, bool COMBINE = false, bool GATHER = false, int PAIRING = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                       const __grid_constant__ CUtensorMap tmB1, const int32_t* __restrict__ offsets,
@@ -294,10 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const float* __restrict__ topk_w = nullptr, int kslots = 1,
                       const __nv_bfloat16* __restrict__ gx = nullptr,
                       const int32_t* __restrict__ gsrc = nullptr, int gdiv = 1) {
-  constexpr int STAGES = Cfg<BN>::STAGES;
-  constexpr int STAGE_BYTES = Cfg<BN>::STAGE_BYTES;
-  constexpr int B_BYTES = Cfg<BN>::B_BYTES;
-  constexpr uint32_t TMEM_COLS = Cfg<BN>::TMEM_COLS;
+  constexpr bool MCAST = PAIRING == 1, PAIR = PAIRING == 2, CL = PAIRING != 0;
+  static_assert(!(PAIR && (GATHER || BN != 256)), "2-CTA MMA: 256-wide tiles without gather");
+  using C = Cfg<BN, PAIR>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int STAGE_BYTES = C::STAGE_BYTES;
+  constexpr int B_BYTES = C::B_BYTES;
+  constexpr uint32_t TMEM_COLS = C::TMEM_COLS;
   using SmemT = Smem<STAGES>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* ring = reinterpret_cast<unsigned char*>(
@@ -307,10 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kTileN = GATEUP ? BN / 2 : BN;  // output columns per tile
-  constexpr int kUnitRows = MCAST ? 2 * BM : BM;  // rows of one work unit (a cluster's)
-  const uint32_t crank = MCAST ? cluster_ctarank() : 0u;
-  const int unit0 = MCAST ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int ustride = MCAST ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  constexpr int kUnitRows = CL ? 2 * BM : BM;  // rows of one work unit (a cluster's)
+  const uint32_t crank = CL ? cluster_ctarank() : 0u;
+  const int unit0 = CL ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustride = CL ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   constexpr uint16_t kPair = 0x3;
   const int n_tiles = (N + kTileN - 1) / kTileN;
   const int num_kb = K / BK;
@@ -324,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.tmem_full[b], 1);
-      mbar_init(&S.tmem_empty[b], 128);
+      mbar_init(&S.tmem_empty[b], PAIR ? 8 : 128);  // PAIR: one arrival per epilogue warp of both CTAs
     }
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -334,11 +408,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (GATEUP) prefetch_tensormap(&tmB1);
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&S.tmem_base)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (PAIR) {  // collective with the peer CTA's warp 1
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(&S.tmem_base)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(&S.tmem_base)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -352,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (MCAST) cluster_sync_all();  // the peer's barriers are initialised before any multicast
+  if (CL) cluster_sync_all();  // the peer's barriers are initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = S.tmem_base;
   // Work units.  A down launch whose last wave would be partly empty splits each
@@ -361,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_tiles = S.cum[E] * n_tiles;
   int full_units = total_tiles, split_tiles = 0;
   if (!GATEUP && !MCAST && BN == 256) {
-    const int rem = total_tiles % (int)gridDim.x;
-    if (rem > 0 && 2 * rem <= (int)gridDim.x) {
+    const int rem = total_tiles % ustride;
+    if (rem > 0 && 2 * rem <= ustride) {
       full_units = total_tiles - rem;
       split_tiles = rem;
     }
@@ -377,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       width = kTileN;
     } else {
       const int v = u - full_units;
-      c = map_tile(S, E, n_tiles, full_units + (v >> 1));
+      c = map_tile(S, E, n_tiles, full_units + (v >> 1), kUnitRows);
+      c.row0 += (int)crank * BM;
       col_off = (v & 1) * (kTileN / 2);
       width = kTileN / 2;
     }
@@ -415,14 +498,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           unsigned char* sB = sA + A_BYTES;
           // a half unit of the down GEMM loads only the 128 B rows it uses (tmB1)
           const bool half_unit = !GATEUP && tile >= full_units;
-          if (lane == 0)
+          if (PAIR) {
+            // both CTAs' loads land on rank 0's full barrier, which expects them all
+            if (lane == 0) {
+              const uint32_t fb = cluster_addr(smem_u32(&S.full[stage]), 0);
+              if (crank == 0)
+                mbar_arrive_expect_tx(&S.full[stage],
+                                      2 * (half_unit ? STAGE_BYTES - B_BYTES / 2 : STAGE_BYTES));
+              tma_load_2d_pair(sA, &tmA, fb, kb * BK, c.row0);
+              if (half_unit)  // down, 128-column half: 64 B rows per CTA (tmB0 has a 64-row box)
+                tma_load_2d_pair(sB, &tmB0, fb, kb * BK, brow + (int)crank * (BN / 4));
+              else
+                tma_load_2d_pair(sB, GATEUP && crank == 0 ? &tmB0 : &tmB1, fb, kb * BK,
+                                 GATEUP ? brow : brow + (int)crank * (BN / 2));
+            }
+          } else if (lane == 0) {
             mbar_arrive_expect_tx(&S.full[stage], half_unit ? STAGE_BYTES - B_BYTES / 2 : STAGE_BYTES);
+          }
           if (GATHER) {
             __syncwarp();  // the expected byte count is set before any gather lands
             tma_gather4(sA + lane * 4 * 128, &tmA, &S.full[stage], kb * BK, tok[0], tok[1], tok[2],
                         tok[3]);
           }
-          if (lane == 0) {
+          if (lane == 0 && !PAIR) {
             if (!GATHER) tma_load_2d(sA, &tmA, &S.full[stage], kb * BK, c.row0);
             if (MCAST) {
               // this CTA's half of B (gate/up: rank 0 the gate rows, rank 1 the up
@@ -446,8 +544,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
       }
-      // drain: every issued load must have landed before the CTA may exit
-      if (lane == 0) {
+      // drain: every issued load must have landed before the CTA may exit.
+      // PAIR, rank 1: its loads complete on rank 0's barriers, which it cannot
+      // poll; on the normal path rank 0's MMAs consumed them all before the
+      // closing cluster barrier.  After an abort it leaves them time to land.
+      if (PAIR && crank != 0) {
+        if (lane == 0 && *abort_flag) {
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 200000ull) {
+          }
+        }
+      } else if (lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
           if (!((issued >> s) & 1u)) continue;
           const uint32_t a = smem_u32(&S.full[s]);
@@ -464,16 +571,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_full = make_idesc_bf16(BM, BN);
-      constexpr uint32_t idesc_half = make_idesc_bf16(BM, BN / 2);
+    // (PAIR: rank 0 only; rank 1's warp 1 just holds its TMEM allocation)
+    if (lane == 0 && (!PAIR || crank == 0)) {
+      constexpr uint32_t idesc_full = make_idesc_bf16(PAIR ? 2 * BM : BM, BN);
+      constexpr uint32_t idesc_half = make_idesc_bf16(PAIR ? 2 * BM : BM, BN / 2);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int tile = unit0; tile < total && !*abort_flag; tile += ustride) {
         const uint32_t idesc = tile < full_units ? idesc_full : idesc_half;
-        if (!mbar_wait(&S.tmem_empty[acc], acc_phase ^ 1u, abort_flag, kErrMma)) break;
+        if (!mbar_wait<PAIR>(&S.tmem_empty[acc], acc_phase ^ 1u, abort_flag, kErrMma)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         bool ok = true;
@@ -487,11 +595,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            tc_mma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
-                       (kb | kk) != 0 ? 1u : 0u);
+            if (PAIR)
+              tc_mma_f16_pair(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                              (kb | kk) != 0 ? 1u : 0u);
+            else
+              tc_mma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                         (kb | kk) != 0 ? 1u : 0u);
           }
-          // frees the smem stage once these MMAs finish (in both CTAs when multicasting)
-          if (MCAST) tc_commit_mcast(&S.empty[stage], kPair);
+          // frees the smem stage once these MMAs finish (in both CTAs when multicasting / paired)
+          if (PAIR) tc_commit_pair_mcast(&S.empty[stage], kPair);
+          else if (MCAST) tc_commit_mcast(&S.empty[stage], kPair);
           else tc_commit(&S.empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -499,14 +612,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        tc_commit(&S.tmem_full[acc]);
+        if (PAIR) tc_commit_pair_mcast(&S.tmem_full[acc], kPair);
+        else tc_commit(&S.tmem_full[acc]);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // drain: all issued MMAs complete before TMEM is released
-      tc_commit(&S.drain);
+      if (PAIR) tc_commit_pair_mcast(&S.drain, 0x1);
+      else tc_commit(&S.drain);
       const uint32_t a = smem_u32(&S.drain);
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(a, 0)) {
@@ -608,7 +723,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&S.tmem_empty[acc]);
+      if (PAIR) {  // one arrival per warp, on rank 0's barrier
+        __syncwarp();
+        if (lane == 0) {
+          if (crank == 0) mbar_arrive(&S.tmem_empty[acc]);
+          else mbar_arrive_cluster(cluster_addr(smem_u32(&S.tmem_empty[acc]), 0));
+        }
+      } else {
+        mbar_arrive(&S.tmem_empty[acc]);
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -618,12 +741,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (MCAST) cluster_sync_all();  // the peer no longer writes here or arrives on our barriers
+  if (CL) cluster_sync_all();  // the peer no longer writes here or arrives on our barriers
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(TMEM_COLS)
-                 : "memory");
+    if (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(TMEM_COLS)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(TMEM_COLS)
+                   : "memory");
   }
 }
 
@@ -687,22 +815,28 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   return cudaGetLastError();
 }
 
-// Cluster-of-2 multicast launch of a 256-wide kernel (MCAST).  The grid is the
-// number of clusters that fit at once (queried once per device), capped by the
-// work, times two.
-inline bool mcast_enabled() {
-  const char* v = getenv("MOE_GROUPED_MCAST");  // "0" turns the cluster path off (tests, A/B)
-  return !(v && v[0] == '0');
+// How 256-wide launches pair CTAs: 2 = 2-CTA MMA (PAIR, the default),
+// 1 = weight-tile multicast (MCAST), 0 = single CTAs.  MOE_GROUPED_CLUSTER in
+// the environment ("pair", "mcast", "none") selects one (tests, A/B timing).
+inline int cluster_mode() {
+  const char* v = getenv("MOE_GROUPED_CLUSTER");
+  if (!v || !*v) return 2;
+  if (v[0] == 'm') return 1;
+  if (v[0] == 'n' || v[0] == '0') return 0;
+  return 2;
 }
 
-template <bool GATEUP, bool COMBINE>
-cudaError_t launch_mcast(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                         const int32_t* offsets, int R, int E, int N, int K, void* out,
-                         cudaStream_t s, const int32_t* perm = nullptr,
-                         const float* topk_w = nullptr, int kslots = 1) {
+// Cluster-of-2 launch of a 256-wide kernel (PAIRING 1 or 2).  The grid is the
+// number of clusters that fit at once (queried once per device and mode),
+// capped by the work, times two.
+template <bool GATEUP, bool COMBINE, int PAIRING>
+cudaError_t launch_cluster(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                           const int32_t* offsets, int R, int E, int N, int K, void* out,
+                           cudaStream_t s, const int32_t* perm = nullptr,
+                           const float* topk_w = nullptr, int kslots = 1) {
   constexpr int BN = 256;
-  constexpr size_t sm = smem_bytes<BN>();
-  auto kern = grouped_tc_kernel<GATEUP, BN, COMBINE, false, true>;
+  constexpr size_t sm = smem_bytes<BN, PAIRING == 2>();
+  auto kern = grouped_tc_kernel<GATEUP, BN, COMBINE, false, PAIRING>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr;
@@ -734,6 +868,16 @@ cudaError_t launch_mcast(const CUtensorMap& a, const CUtensorMap& b0, const CUte
                          (const __nv_bfloat16*)nullptr, (const int32_t*)nullptr, 1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <bool GATEUP, bool COMBINE>
+cudaError_t launch_paired(int mode, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                          const int32_t* offsets, int R, int E, int N, int K, void* out,
+                          cudaStream_t s, const int32_t* perm = nullptr,
+                          const float* topk_w = nullptr, int kslots = 1) {
+  if (mode == 1)
+    return launch_cluster<GATEUP, COMBINE, 1>(a, b0, b1, offsets, R, E, N, K, out, s, perm, topk_w, kslots);
+  return launch_cluster<GATEUP, COMBINE, 2>(a, b0, b1, offsets, R, E, N, K, out, s, perm, topk_w, kslots);
 }
 
 // MMA width for a launch.  256 everywhere it was measured best (both GEMMs
@@ -775,8 +919,8 @@ inline cudaError_t launch_gateup_tc(const __nv_bfloat16* x_perm, const int32_t* 
       !tc::make_map(&m[1], w_gate, (uint64_t)E * F, (uint64_t)d, bn / 2) ||
       !tc::make_map(&m[2], w_up, (uint64_t)E * F, (uint64_t)d, bn / 2))
     return cudaErrorInvalidValue;
-  if (bn == 256 && tc::mcast_enabled())
-    return tc::launch_mcast<true, false>(m[0], m[1], m[2], offsets, R, E, F, d, h, s);
+  if (bn == 256 && tc::cluster_mode() != 0)
+    return tc::launch_paired<true, false>(tc::cluster_mode(), m[0], m[1], m[2], offsets, R, E, F, d, h, s);
   return tc::launch<true>(m, bn, offsets, R, E, F, d, h, sms, s);
 }
 
@@ -812,13 +956,16 @@ inline cudaError_t launch_down_tc(const __nv_bfloat16* h, const int32_t* offsets
                                   float* y_perm, cudaStream_t s) {
   const int sms = tc::sm_count();
   const int bn = tc::choose_bn(R, E, d, false, sms);
-  CUtensorMap m[3];  // A, B, and B with a half-height box (tail halves, multicast halves)
+  const int mode = bn == 256 ? tc::cluster_mode() : 0;
+  // A, and B with a full-tile box and a half-height box (single CTA: tiles and
+  // tail halves; PAIR: quarter box for tail halves, half box for tiles)
+  CUtensorMap m[3];
   if (!tc::make_map(&m[0], h, (uint64_t)R, (uint64_t)F, tc::BM) ||
-      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, bn) ||
+      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, mode == 2 ? bn / 4 : bn) ||
       !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, bn / 2))
     return cudaErrorInvalidValue;
-  if (bn == 256 && tc::mcast_enabled())
-    return tc::launch_mcast<false, false>(m[0], m[1], m[2], offsets, R, E, d, F, y_perm, s);
+  if (mode != 0)
+    return tc::launch_paired<false, false>(mode, m[0], m[1], m[2], offsets, R, E, d, F, y_perm, s);
   return tc::launch<false>(m, bn, offsets, R, E, d, F, y_perm, sms, s);
 }
 
@@ -830,14 +977,15 @@ inline cudaError_t launch_down_combine_tc(const __nv_bfloat16* h, const int32_t*
                                           const int32_t* perm, const float* topk_w, int k, float* y,
                                           cudaStream_t s) {
   const int sms = tc::sm_count();
-  CUtensorMap m[3];  // A, B, and B with a half-height box for split tail tiles
+  const int mode = tc::cluster_mode();
+  CUtensorMap m[3];  // A, and B boxes as in launch_down_tc (256 wide)
   if (!tc::make_map(&m[0], h, (uint64_t)R, (uint64_t)F, tc::BM) ||
-      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, 256) ||
+      !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, mode == 2 ? 64 : 256) ||
       !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, 128))
     return cudaErrorInvalidValue;
-  if (tc::mcast_enabled())
-    return tc::launch_mcast<false, true>(m[0], m[1], m[2], offsets, R, E, d, F, y, s, perm, topk_w,
-                                         k);
+  if (mode != 0)
+    return tc::launch_paired<false, true>(mode, m[0], m[1], m[2], offsets, R, E, d, F, y, s, perm,
+                                          topk_w, k);
   return tc::launch_bn<false, 256, true>(m[0], m[1], m[2], offsets, R, E, d, F, y, sms, s, perm,
                                          topk_w, k);
 }

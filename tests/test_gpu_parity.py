@@ -384,16 +384,54 @@ def test_gateup_gather_bit_identical(moe, torch, case, tile_n, monkeypatch):
     assert torch.equal(h_ref.view(torch.int16), h_gat.view(torch.int16))
 
 
+@pytest.mark.parametrize("mode", ["pair", "mcast"])
 @pytest.mark.parametrize("k", [2, 4])
-def test_cluster_multicast_path_bit_identical(moe, torch, k, monkeypatch):
-    """Multicasting the weight tiles inside clusters of 2 changes only where operand bytes
-    come from, never the arithmetic: outputs equal the single-CTA path bit for bit."""
+def test_cluster_paths_bit_identical(moe, torch, k, mode, monkeypatch):
+    """Clusters of 2 change only where operand bytes come from and which SM issues the
+    MMA (pair: one M = 256 instruction over both CTAs' rows; mcast: weight tiles
+    multicast), never the per-element arithmetic: outputs equal the single-CTA path
+    bit for bit.  Row counts leave partial 256-row blocks and an expert of < 128 rows."""
     cfg = synth.small_config("mcast", 4000, 256, 512, 8, k, "bf16", seed=60, x_std=1.0, w_std=0.05)
     inp = synth.make_inputs(cfg)
     w = dev_weights(inp)
     x = to_dev(inp.x)
-    y_mc = moe.moe_layer_forward(x, w, k=k).clone()
-    monkeypatch.setenv("MOE_GROUPED_MCAST", "0")
-    y_one = moe.moe_layer_forward(x, w, k=k)
+    # outputs start as NaN so that a row a path fails to write cannot match
+    y_cl = torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32, device="cuda")
+    y_one = y_cl.clone()
+    monkeypatch.setenv("MOE_GROUPED_CLUSTER", mode)
+    moe.moe_layer_forward(x, w, k=k, y=y_cl)
+    monkeypatch.setenv("MOE_GROUPED_CLUSTER", "none")
+    moe.moe_layer_forward(x, w, k=k, y=y_one)
     torch.cuda.synchronize()
-    assert torch.equal(y_mc, y_one)
+    assert not torch.isnan(y_cl).any()
+    assert torch.equal(y_cl, y_one)
+
+
+@pytest.mark.parametrize("mode", ["pair", "mcast"])
+def test_cluster_paths_grouped_ragged(moe, torch, mode, monkeypatch):
+    """Both cluster forms of the separate gate/up and down entry points on ragged
+    segments (empty experts, one row, a 128-row half block) against the single-CTA path."""
+    cnts = [300, 0, 1, 128, 129, 700, 0, 255]
+    d, F = 256, 512
+    cfg = synth.small_config("pair_ragged", int(sum(cnts)), d, F, len(cnts), 1, "bf16", seed=61,
+                             x_std=1.0, w_std=0.05)
+    inp = synth.make_inputs(cfg)
+    offsets = torch.from_numpy(np.concatenate([[0], np.cumsum(cnts)]).astype(np.int32)).cuda()
+    w = dev_weights(inp)
+    x = to_dev(inp.x)
+    monkeypatch.setenv("MOE_GROUPED_TILE_N", "256")
+    R = int(sum(cnts))
+    outs = {}
+    for m in (mode, "none"):
+        monkeypatch.setenv("MOE_GROUPED_CLUSTER", m)
+        # outputs start as NaN so that a row a path fails to write cannot match
+        h = torch.full((R, F), float("nan"), dtype=torch.bfloat16, device="cuda")
+        yp = torch.full((R, d), float("nan"), dtype=torch.float32, device="cuda")
+        moe.moe_grouped_gateup_swiglu(x, offsets, w["w_gate"], w["w_up"], h)
+        moe.moe_grouped_down(h, offsets, w["w_down"], yp)
+        outs[m] = (h, yp)
+    torch.cuda.synchronize()
+    (h_cl, yp_cl), (h_one, yp_one) = outs[mode], outs["none"]
+    assert not torch.isnan(yp_cl).any()
+    assert torch.equal(h_cl.view(torch.int16), h_one.view(torch.int16))
+    assert torch.equal(yp_cl, yp_one)
