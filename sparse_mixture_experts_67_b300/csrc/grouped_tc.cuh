@@ -86,10 +86,14 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
+// The waits pass a suspend-time hint of 1 ms: a waiting thread sleeps until
+// the phase completes (or the hint expires) instead of re-polling the barrier.
+// Polling at the default limit cost shared-memory bandwidth that the tensor
+// cores' operand reads need (gate/up GEMM 168 -> 157 us on top2_d1024).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -101,7 +105,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, "
+      "1000000;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -634,9 +639,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // Each warp owns TMEM lane quarter q (tile rows 32q .. 32q+31, thread = row
-    // when reading TMEM).  A 32-column chunk goes through the warp's staging tile
-    // in shared memory and leaves as whole row segments (4-8 rows per store
-    // instruction instead of 32 scattered 16-byte pieces).
+    // when reading TMEM).  A chunk of columns goes through the warp's staging
+    // tile in shared memory and leaves as whole row segments (4-8 rows per store
+    // instruction instead of 32 scattered 16-byte pieces): 64 bf16 columns
+    // (128-byte rows, 16-byte pieces XOR-swizzled by row) for H, 32 fp32 columns
+    // (rows padded to 144 bytes) for Y.  Both staging patterns are free of bank
+    // conflicts.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     float* stg = S.stage_out[q];
     uint32_t* stg_w = reinterpret_cast<uint32_t*>(stg);
@@ -655,32 +663,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = c.nt * kTileN + col_off;
       if (GATEUP) {
         __nv_bfloat16* H = static_cast<__nv_bfloat16*>(out);
+        constexpr int kCh = kTileN >= 64 ? 64 : 32;  // columns per staged chunk
+        uint4* stg16 = reinterpret_cast<uint4*>(stg_w);  // 32 rows x 8 pieces of 16 bytes
 #pragma unroll 1
-        for (int cc = 0; cc < kTileN; cc += 32) {
-          uint32_t g[32], u[32];
-          MOE_TMEM_LD32(taddr + cc, g);
-          MOE_TMEM_LD32(taddr + kTileN + cc, u);
-          tmem_ld_wait();
-          uint32_t p[16];
+        for (int c0 = 0; c0 < kTileN; c0 += kCh) {
+#pragma unroll 1
+          for (int cc = c0; cc < c0 + kCh; cc += 32) {
+            uint32_t g[32], u[32];
+            MOE_TMEM_LD32(taddr + cc, g);
+            MOE_TMEM_LD32(taddr + kTileN + cc, u);
+            tmem_ld_wait();
+            uint32_t p[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-            const float h1 = silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-            p[i] = pack_bf16x2(h0, h1);
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+              const float h1 = silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+              p[i] = pack_bf16x2(h0, h1);
+            }
+            // row `lane`, pieces (cc - c0) / 8 + i, stored at piece ^ (row & 7)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int piece = ((cc - c0) >> 3) + i;
+              stg16[lane * 8 + (piece ^ (lane & 7))] =
+                  make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+            }
           }
-          // stage: row `lane` = 32 bf16 = 64 bytes at a pitch of 80 bytes
-          uint4* srow = reinterpret_cast<uint4*>(stg_w + lane * 20);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) srow[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
           __syncwarp();
-          if (n0 + cc < N) {  // 4 lanes per row, 8 rows per store
+          if (n0 + c0 < N) {
+            constexpr int kLanesPerRow = kCh / 8, kRowsPerStore = 32 / kLanesPerRow;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int r = j * 8 + (lane >> 2), part = lane & 3;
+            for (int j = 0; j < 32 / kRowsPerStore; ++j) {
+              const int r = j * kRowsPerStore + lane / kLanesPerRow, part = lane % kLanesPerRow;
               const int grow = rbase + r;
               if (grow < c.row_end)
-                *reinterpret_cast<uint4*>(H + (size_t)grow * N + n0 + cc + part * 8) =
-                    *reinterpret_cast<const uint4*>(stg_w + r * 20 + part * 4);
+                *reinterpret_cast<uint4*>(H + (size_t)grow * N + n0 + c0 + part * 8) =
+                    stg16[r * 8 + (part ^ (r & 7))];
             }
           }
           __syncwarp();
