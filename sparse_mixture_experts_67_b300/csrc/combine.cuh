@@ -22,6 +22,7 @@ constexpr int kCombineThreads = 256;
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const float4* __restrict__ y_perm, const int32_t* __restrict__ inv_perm,
                    const float* __restrict__ w, int T, int d4, int k, float4* __restrict__ y) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (kCombineThreads / 32);
   for (int t = blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5); t < T; t += warps) {
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     ec_combine_kernel(const float4* __restrict__ y_perm, const int32_t* __restrict__ pos,
                       const float* __restrict__ score, int T, int d4, int E,
                       float4* __restrict__ y) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (kCombineThreads / 32);
   for (int t = blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5); t < T; t += warps) {
@@ -101,6 +103,7 @@ __global__ void __launch_bounds__(kCombineThreads)
 // (blocks of tok tokens).
 __global__ void probs_partials_kernel(const float* __restrict__ probs, int T, int E, int tok,
                                       float* __restrict__ partials) {
+  pdl_begin();
   const int t0 = blockIdx.x * tok;
   const int t1 = min(T, t0 + tok);
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -117,6 +120,7 @@ __global__ void __launch_bounds__(kAuxThreads)
     aux_finalize_kernel(const float* __restrict__ partials, int rows, const int32_t* __restrict__ counts,
                         int T, int E, float* __restrict__ f, float* __restrict__ p,
                         float* __restrict__ loss) {
+  pdl_begin();
   __shared__ float s[MOE_MAX_EXPERTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int nwarps = kAuxThreads / 32;

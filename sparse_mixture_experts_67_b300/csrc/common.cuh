@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "../../include/moe.h"
 
@@ -22,6 +23,51 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Programmatic dependent launch.  Every kernel here calls pdl_begin() before
+// its first global-memory access: it waits until the previous kernel in the
+// stream has completed with its memory visible, then lets the next kernel be
+// scheduled.  Launched with programmatic stream serialization (launch_k, when
+// enabled), a kernel's CTAs thus start, and run their prologue (barrier setup,
+// TMEM allocation), while the previous kernel drains its last CTAs; without
+// the launch attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// The attribute is off unless MOE_PDL=1 is set in the environment.  Measured
+// on top2_d1024: CUDA-graph replay of the layer 0.294 -> 0.300 ms with it (the
+// graph already removes the launch gaps), eager launches 0.317 -> 0.313 ms.
+inline bool pdl_enabled() {
+  const char* v = getenv("MOE_PDL");
+  return v && v[0] == '1';
+}
+
+// Launch with programmatic stream serialization (see pdl_begin) and optional
+// extra attributes (a cluster shape).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     const cudaLaunchAttribute* extra, int n_extra, Args&&... args) {
+  cudaLaunchAttribute attrs[4];
+  int n = 0;
+  for (int i = 0; i < n_extra && n < 3; ++i) attrs[n++] = extra[i];
+  if (pdl_enabled()) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 template <typename T>

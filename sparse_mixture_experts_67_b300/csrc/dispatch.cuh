@@ -28,6 +28,7 @@ inline int dispatch_tiles(long long A, int tile) { return A == 0 ? 0 : ceil_div(
 __global__ void __launch_bounds__(kDispatchThreads)
     dispatch_hist_kernel(const int32_t* __restrict__ idx, int A, int E, int tile,
                          int32_t* __restrict__ tile_counts) {
+  pdl_begin();
   __shared__ int cnt[MOE_MAX_EXPERTS];
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(kScanThreads)
     dispatch_scan_kernel(const int32_t* __restrict__ tile_counts, int tiles, int E, int A,
                          int32_t* __restrict__ tile_base, int32_t* __restrict__ counts,
                          int32_t* __restrict__ offsets) {
+  pdl_begin();
   __shared__ int s_tot[MOE_MAX_EXPERTS];
   __shared__ int s_off[MOE_MAX_EXPERTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
                             const float* __restrict__ aux_partials, int T, float* __restrict__ f,
                             float* __restrict__ p, float* __restrict__ loss,
                             float4* __restrict__ y_zero, int d4, int tokens_per_tile) {
+  pdl_begin();
   __shared__ int running[MOE_MAX_EXPERTS];
   __shared__ int s_tot[MOE_MAX_EXPERTS];
   __shared__ int wcnt[kDispatchWarps][MOE_MAX_EXPERTS];
@@ -268,6 +271,7 @@ constexpr int kGatherThreads = 256;
 __global__ void __launch_bounds__(kGatherThreads)
     gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ src, int R, int div,
                        int vec_per_row, uint4* __restrict__ out) {
+  pdl_begin();
   const int lane = threadIdx.x & 31;
   const int warps = gridDim.x * (kGatherThreads / 32);
   for (int r = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); r < R; r += warps) {
@@ -293,6 +297,7 @@ namespace moe {
 
 // Expert-choice segments are uniform: offsets[e] = e * C, e = 0..E.
 __global__ void uniform_offsets_kernel(int32_t* __restrict__ offsets, int E, int C) {
+  pdl_begin();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = e * C;
 }
 

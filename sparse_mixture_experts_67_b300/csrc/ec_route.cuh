@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kEcThreads)
     ec_route_kernel(const float* __restrict__ logits, int T, int E, int C, int c_pow2,
                     int32_t* __restrict__ ec_idx, float* __restrict__ ec_score,
                     int32_t* __restrict__ pos) {
+  pdl_begin();
   extern __shared__ __align__(16) unsigned char ec_smem[];
   uint32_t* s_key = reinterpret_cast<uint32_t*>(ec_smem);  // ascending = descending logit
   unsigned long long* s_sel = reinterpret_cast<unsigned long long*>(

@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kSimtThreads)
     grouped_simt_kernel(const TIn* __restrict__ A, const int32_t* __restrict__ offsets,
                         const TIn* __restrict__ B0, const TIn* __restrict__ B1, int N, int K, int E,
                         void* __restrict__ out) {
+  pdl_begin();
   __shared__ __align__(16) float As[kSimtBK][kSimtBM + 4];
   __shared__ __align__(16) float Bs0[kSimtBK][kSimtBN + 4];
   __shared__ __align__(16) float Bs1[GATEUP ? kSimtBK : 1][kSimtBN + 4];
@@ -152,8 +153,8 @@ template <typename TIn, bool GATEUP>
 cudaError_t launch_grouped_simt(const TIn* A, const int32_t* offsets, const TIn* B0, const TIn* B1,
                                 int R, int N, int K, int E, void* out, cudaStream_t st) {
   dim3 grid(ceil_div(R, kSimtBM) + E, ceil_div(N, kSimtBN));
-  grouped_simt_kernel<TIn, GATEUP><<<grid, kSimtThreads, 0, st>>>(A, offsets, B0, B1, N, K, E, out);
-  return cudaGetLastError();
+  return launch_k(grouped_simt_kernel<TIn, GATEUP>, grid, dim3(kSimtThreads), 0, st, nullptr, 0, A,
+                  offsets, B0, B1, N, K, E, out);
 }
 
 }  // namespace moe

@@ -101,6 +101,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Without the hint: the wait returns at the hardware's default limit, for
+// latency-critical chains of short waits.
+__device__ __forceinline__ bool mbar_try_wait_short(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // As mbar_try_wait, acquiring at cluster scope (arrivals made by the peer CTA).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -116,11 +129,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 
 // Waits for the phase of `parity` to complete.  Gives up (false) when the
 // CTA's abort flag is raised or after kWaitTimeoutNs, recording `code`.
-template <bool CLUSTER_SCOPE = false>
+template <bool CLUSTER_SCOPE = false, bool SHORT = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t code) {
   const uint32_t a = smem_u32(bar);
-  auto ready = [&]() { return CLUSTER_SCOPE ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
+  auto ready = [&]() {
+    return CLUSTER_SCOPE ? mbar_try_wait_cluster(a, parity)
+                         : (SHORT ? mbar_try_wait_short(a, parity) : mbar_try_wait(a, parity));
+  };
   if (ready()) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -394,8 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (N + kTileN - 1) / kTileN;
   const int num_kb = K / BK;
 
-  // --- setup
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) S.off[i] = min(max(offsets[i], 0), R);
+  // --- setup (barriers and TMEM first: this part may overlap the previous kernel)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&S.full[s], 1);
@@ -427,6 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
   }
+  pdl_begin();  // the segment offsets come from the previous kernel
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) S.off[i] = min(max(offsets[i], 0), R);
   __syncthreads();
   if (threadIdx.x == 0) {
     int cum = 0;
@@ -827,9 +844,9 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   constexpr int tile_n = GATEUP ? BN / 2 : BN;
   const long long max_tiles = (long long)((R + BM - 1) / BM + E) * ((N + tile_n - 1) / tile_n);
   const int grid = (int)std::min<long long>(sms, max_tiles);
-  grouped_tc_kernel<GATEUP, BN, COMBINE, GATHER><<<grid, kThreads, sm, s>>>(
-      a, b0, b1, offsets, R, E, N, K, out, perm, topk_w, kslots, gx, gsrc, gdiv);
-  return cudaGetLastError();
+  return launch_k(grouped_tc_kernel<GATEUP, BN, COMBINE, GATHER>, dim3(grid), dim3(kThreads), sm, s,
+                  nullptr, 0, a, b0, b1, offsets, R, E, N, K, out, perm, topk_w, kslots, gx, gsrc,
+                  gdiv);
 }
 
 // How 256-wide launches pair CTAs: 2 = 2-CTA MMA (PAIR, the default),
@@ -880,11 +897,9 @@ cudaError_t launch_cluster(const CUtensorMap& a, const CUtensorMap& b0, const CU
   constexpr int tile_n = GATEUP ? BN / 2 : BN;
   const long long units = (long long)((R + 2 * BM - 1) / (2 * BM) + E) * ((N + tile_n - 1) / tile_n);
   const int clusters = (int)std::min<long long>(max_clusters[dev], units);
-  cfg.gridDim = dim3(2 * clusters, 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, a, b0, b1, offsets, R, E, N, K, out, perm, topk_w, kslots,
-                         (const __nv_bfloat16*)nullptr, (const int32_t*)nullptr, 1);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_k(kern, dim3(2 * clusters), dim3(kThreads), sm, s, &attr, 1, a, b0, b1, offsets, R,
+                  E, N, K, out, perm, topk_w, kslots, (const __nv_bfloat16*)nullptr,
+                  (const int32_t*)nullptr, 1);
 }
 
 template <bool GATEUP, bool COMBINE>

@@ -10,6 +10,7 @@
 #include "grouped_simt.cuh"
 #include "grouped_tc.cuh"
 #include "router.cuh"
+#include "router_tc.cuh"
 
 using namespace moe;
 
@@ -116,8 +117,8 @@ moe_status moe_expert_choice_route(const void* x, const void* w_g, const float* 
   const size_t sm = ec_route_smem(T, C > 0 ? C : 1);
   e = cudaFuncSetAttribute(ec_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  ec_route_kernel<<<E, kEcThreads, sm, s>>>(logits, T, E, C, c2, ec_idx, ec_score, pos);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(ec_route_kernel, dim3(E), dim3(kEcThreads), sm, s, nullptr, 0, logits,
+                              T, E, C, c2, ec_idx, ec_score, pos));
 }
 
 size_t moe_permute_workspace_size(int T, int E, int k) {
@@ -136,9 +137,9 @@ moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, in
   if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_UNSUPPORTED;
   const int vec = (int)(d * elt_size(dt) / 16);
   const int grid = min(ceil_div(R, kGatherThreads / 32), 148 * 16);
-  gather_rows_kernel<<<grid, kGatherThreads, 0, (cudaStream_t)stream>>>(
-      static_cast<const uint4*>(x), src, R, div, vec, static_cast<uint4*>(x_perm));
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(gather_rows_kernel, dim3(grid), dim3(kGatherThreads), 0,
+                              (cudaStream_t)stream, nullptr, 0, static_cast<const uint4*>(x), src, R,
+                              div, vec, static_cast<uint4*>(x_perm)));
 }
 
 // Dispatch: (histogram when the counts are not ready) + scatter with the row
@@ -155,21 +156,26 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
                                   float* y_zero = nullptr) {
   const long long A = (long long)T * k;
   const int tiles = dispatch_tiles(A, tile);
+  cudaError_t e = cudaSuccess;
   if (!counts_ready)
-    dispatch_hist_kernel<<<tiles, kDispatchThreads, 0, s>>>(topk_idx, (int)A, E, tile, tile_counts);
+    e = launch_k(dispatch_hist_kernel, dim3(tiles), dim3(kDispatchThreads), 0, s, nullptr, 0,
+                 topk_idx, (int)A, E, tile, tile_counts);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
   const bool separate_scan = (long long)tiles * tiles * E > kFusedScanMaxReads;
   if (separate_scan) {
-    dispatch_scan_kernel<<<1, kScanThreads, 0, s>>>(tile_counts, tiles, E, (int)A, tile_base,
-                                                    counts, offsets);
-    if (aux_partials)
-      aux_finalize_kernel<<<1, kAuxThreads, 0, s>>>(aux_partials, tiles, counts, T, E, f, p, loss);
+    e = launch_k(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, nullptr, 0, tile_counts,
+                 tiles, E, (int)A, tile_base, counts, offsets);
+    if (e == cudaSuccess && aux_partials)
+      e = launch_k(aux_finalize_kernel, dim3(1), dim3(kAuxThreads), 0, s, nullptr, 0, aux_partials,
+                   tiles, counts, T, E, f, p, loss);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
-  dispatch_scatter_kernel<<<tiles, kDispatchThreads, 0, s>>>(
-      topk_idx, (int)A, E, k, tile, tile_counts, separate_scan ? tile_base : nullptr, tiles, perm,
-      inv_perm, counts, offsets, static_cast<const uint4*>(x), (int)(d * elt_size(dt) / 16),
-      static_cast<uint4*>(x_perm), aux_partials, T, f, p, loss,
-      reinterpret_cast<float4*>(y_zero), d / 4, tile / k);
-  return cuda_status(cudaGetLastError());
+  const int32_t* base = separate_scan ? tile_base : nullptr;
+  return cuda_status(launch_k(
+      dispatch_scatter_kernel, dim3(tiles), dim3(kDispatchThreads), 0, s, nullptr, 0, topk_idx,
+      (int)A, E, k, tile, tile_counts, base, tiles, perm, inv_perm, counts, offsets,
+      static_cast<const uint4*>(x), (int)(d * elt_size(dt) / 16), static_cast<uint4*>(x_perm),
+      aux_partials, T, f, p, loss, reinterpret_cast<float4*>(y_zero), d / 4, tile / k));
 }
 
 static moe_status check_permute(const void* x, const void* x_perm, int T, int d, int E, int k,
@@ -284,10 +290,10 @@ moe_status moe_combine(const float* y_perm, const int32_t* inv_perm, const float
   if (!y_perm || !inv_perm || !topk_w || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
   const int grid = min(ceil_div(T, kCombineThreads / 32), 148 * 8);
-  combine_kernel<<<grid, kCombineThreads, 0, (cudaStream_t)stream>>>(
-      reinterpret_cast<const float4*>(y_perm), inv_perm, topk_w, T, d / 4, k,
-      reinterpret_cast<float4*>(y));
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(combine_kernel, dim3(grid), dim3(kCombineThreads), 0,
+                              (cudaStream_t)stream, nullptr, 0,
+                              reinterpret_cast<const float4*>(y_perm), inv_perm, topk_w, T, d / 4,
+                              k, reinterpret_cast<float4*>(y)));
 }
 
 moe_status moe_ec_combine(const float* y_perm, const int32_t* pos, const float* ec_score, int T,
@@ -298,10 +304,10 @@ moe_status moe_ec_combine(const float* y_perm, const int32_t* pos, const float* 
   if (!pos || !y || (C > 0 && (!y_perm || !ec_score))) return MOE_ERR_INVALID_ARG;
   if ((y_perm && !aligned16(y_perm)) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
   const int grid = min(ceil_div(T, kCombineThreads / 32), 148 * 8);
-  ec_combine_kernel<<<grid, kCombineThreads, 0, (cudaStream_t)stream>>>(
-      reinterpret_cast<const float4*>(y_perm), pos, ec_score, T, d / 4, E,
-      reinterpret_cast<float4*>(y));
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(ec_combine_kernel, dim3(grid), dim3(kCombineThreads), 0,
+                              (cudaStream_t)stream, nullptr, 0,
+                              reinterpret_cast<const float4*>(y_perm), pos, ec_score, T, d / 4, E,
+                              reinterpret_cast<float4*>(y)));
 }
 
 moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int32_t* counts, int T,
@@ -315,10 +321,12 @@ moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int
   if (probs) {
     // probs given: rebuild the per-block partial sums in place of the router's
     if (!aux_partials) return MOE_ERR_INVALID_ARG;
-    probs_partials_kernel<<<rows, 256, 0, s>>>(probs, T, E, tok, const_cast<float*>(aux_partials));
+    cudaError_t e = launch_k(probs_partials_kernel, dim3(rows), dim3(256), 0, s, nullptr, 0, probs, T,
+                             E, tok, const_cast<float*>(aux_partials));
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
-  aux_finalize_kernel<<<1, kAuxThreads, 0, s>>>(aux_partials, rows, counts, T, E, f, p, loss);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(aux_finalize_kernel, dim3(1), dim3(kAuxThreads), 0, s, nullptr, 0,
+                              aux_partials, rows, counts, T, E, f, p, loss));
 }
 
 size_t moe_layer_workspace_size(const moe_layer_desc* desc) {
@@ -403,8 +411,9 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
     if (st != MOE_OK) return st;
     if (R > 0) {
       // expert e owns dispatch rows [e*C, (e+1)*C)
-      uniform_offsets_kernel<<<1, MOE_MAX_EXPERTS + 1, 0, s>>>(offsets, D.E, C);
-      if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+      if (launch_k(uniform_offsets_kernel, dim3(1), dim3(MOE_MAX_EXPERTS + 1), 0, s, nullptr, 0,
+                   offsets, D.E, C) != cudaSuccess)
+        return MOE_ERR_CUDA;
       st = moe_gather_rows(x, ec_idx, (int)R, 1, D.T, D.d, D.dtype, x_perm, stream);
       if (st != MOE_OK) return st;
       st = moe_experts_swiglu(x_perm, offsets, w->w_gate, w->w_up, w->w_down, (int)R, D.d, D.F,

@@ -49,20 +49,25 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, cons
 }
 
 // Thread-per-token epilogue over the logits tile S[TOK][ldS] (bias not yet
-// added; S is modified).  k == 0 writes logits only (expert-choice pre-pass).
-// s_m / s_inv: TOK floats each of shared scratch; s_cnt: MOE_MAX_EXPERTS ints;
-// s_part: blockDim.x floats.
-// tile_counts (nullable): this CTA's row of per-expert selection counts, the
-// dispatch histogram of its TOK*k assignments.
-template <int TOK>
+// added, when given; S is modified).  k == 0 writes logits only (expert-choice
+// pre-pass).  The CTA's tokens form TOK / SUB dispatch tiles of SUB tokens,
+// numbered from tile0: each gets its own row of aux partial sums (aux_rows,
+// the row of tile0, nullable) and of per-expert selection counts (tile_counts,
+// the dispatch histogram of its SUB*k assignments, nullable).
+// Shared scratch: s_m / s_inv TOK floats each; s_cnt (TOK / SUB) *
+// MOE_MAX_EXPERTS ints; s_part max(blockDim.x, E) floats.
+template <int TOK, int SUB = TOK>
 __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k,
                                 const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                                 float* __restrict__ w_out, float* __restrict__ logits_out,
-                                float* __restrict__ probs_out, float* __restrict__ aux_row,
-                                int32_t* __restrict__ tile_counts, float* s_m, float* s_inv,
-                                int* s_cnt, float* s_part) {
+                                float* __restrict__ probs_out, float* __restrict__ aux_rows,
+                                int32_t* __restrict__ tile_counts, int tile0, float* s_m,
+                                float* s_inv, int* s_cnt, float* s_part) {
+  static_assert(TOK % SUB == 0, "dispatch tiles split the CTA's tokens");
+  constexpr int NSUB = TOK / SUB;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int ntok = min(TOK, T - tok0);
+  const int nsub = (ntok + SUB - 1) / SUB;  // dispatch tiles holding tokens
   if (bias) {
     for (int i = tid; i < ntok * E; i += nthr) {
       const int r = i / E, e = i - r * E;
@@ -92,22 +97,27 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
   }
   if (k == 0) return;
   if (tile_counts)
-    for (int e = tid; e < E; e += nthr) s_cnt[e] = 0;
-  if (aux_row) {
-    // column sums of g over this CTA's tokens: G row groups per expert sum
-    // strided rows, then one thread per expert adds the G partials in order
+    for (int i = tid; i < NSUB * MOE_MAX_EXPERTS; i += nthr) s_cnt[i] = 0;
+  if (aux_rows) {
+    // column sums of g over each dispatch tile's tokens: G row groups per
+    // expert sum strided rows, then one thread per expert adds the G partials
+    // in order
     const int G = max(1, nthr / E);
-    if (tid < G * E) {
-      const int e = tid % E, gi = tid / E;
-      float acc = 0.f;
-      for (int r = gi; r < ntok; r += G) acc += expf(S[r * ldS + e] - s_m[r]) * s_inv[r];
-      s_part[gi * E + e] = acc;
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += nthr) {
-      float acc = 0.f;
-      for (int gi = 0; gi < G; ++gi) acc += s_part[gi * E + e];
-      aux_row[e] = acc;
+    for (int st = 0; st < nsub; ++st) {
+      const int r0 = st * SUB, r1 = min(ntok, r0 + SUB);
+      for (int c = tid; c < G * E; c += nthr) {
+        const int e = c % E, gi = c / E;
+        float acc = 0.f;
+        for (int r = r0 + gi; r < r1; r += G) acc += expf(S[r * ldS + e] - s_m[r]) * s_inv[r];
+        s_part[gi * E + e] = acc;
+      }
+      __syncthreads();
+      for (int e = tid; e < E; e += nthr) {
+        float acc = 0.f;
+        for (int gi = 0; gi < G; ++gi) acc += s_part[gi * E + e];
+        aux_rows[(size_t)st * E + e] = acc;
+      }
+      __syncthreads();
     }
   }
   __syncthreads();  // the top-k below overwrites selected entries of S
@@ -126,19 +136,26 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
           bi = e;
         }
       }
+      if (bi < 0) {  // only for non-finite logits (NaN / -inf everywhere): stay in range
+        bi = j;
+        best = row[bi];
+      }
       row[bi] = -INFINITY;  // taken (logits are finite)
       const float gsel = expf(best - m) * inv;  // same arithmetic as probs
       selsum += gsel;
       idx_out[(size_t)t * k + j] = bi;
       w_out[(size_t)t * k + j] = gsel;
-      if (tile_counts) atomicAdd(&s_cnt[bi], 1);
+      if (tile_counts) atomicAdd(&s_cnt[(tid / SUB) * MOE_MAX_EXPERTS + bi], 1);
     }
     const float rs = 1.0f / selsum;
     for (int j = 0; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
   }
   if (tile_counts) {
     __syncthreads();
-    for (int e = tid; e < E; e += nthr) tile_counts[(size_t)blockIdx.x * E + e] = s_cnt[e];
+    for (int i = tid; i < nsub * E; i += nthr) {
+      const int st = i / E, e = i - st * E;
+      tile_counts[(size_t)(tile0 + st) * E + e] = s_cnt[st * MOE_MAX_EXPERTS + e];
+    }
   }
 }
 
@@ -186,6 +203,7 @@ __global__ void __launch_bounds__(kRouterThreadsBf16)
                        int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                        float* __restrict__ logits_out, float* __restrict__ probs_out,
                        float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts) {
+  pdl_begin();
   using C = RouterBf16<NT, TOK>;
   constexpr int EP = C::EP, LD = C::LD, SBK = C::SBK, STAGES = C::STAGES;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -290,6 +308,7 @@ __global__ void __launch_bounds__(kRouterThreadsBf16)
   __syncthreads();
   router_epilogue<TOK>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
+                       blockIdx.x,
                        s_m, s_inv, s_cnt, s_part);
 }
 
@@ -300,7 +319,9 @@ constexpr size_t router_smem_bytes_f32() {
   constexpr size_t ld = kRouterBKf + 1;
   constexpr size_t tiles = (size_t)(TOK + 8 * NT) * ld * 4;
   constexpr size_t acc = (size_t)TOK * (8 * NT + 1) * 4;
-  return tiles + acc + 2 * TOK * 4 + MOE_MAX_EXPERTS * 4 + 2 * TOK * 4;
+  // s_m, s_inv; s_cnt; s_part (max(threads, E) floats)
+  return tiles + acc + 2 * TOK * 4 + MOE_MAX_EXPERTS * 4 +
+         (2 * TOK > MOE_MAX_EXPERTS ? 2 * TOK : MOE_MAX_EXPERTS) * 4;
 }
 
 template <int NT, int TOK>
@@ -310,6 +331,7 @@ __global__ void __launch_bounds__(2 * TOK)
                       int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                       float* __restrict__ logits_out, float* __restrict__ probs_out,
                       float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts) {
+  pdl_begin();
   constexpr int EP = 8 * NT;
   constexpr int ld = kRouterBKf + 1;
   constexpr int ldS = EP + 1;
@@ -352,6 +374,7 @@ __global__ void __launch_bounds__(2 * TOK)
   __syncthreads();
   router_epilogue<TOK>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
+                       blockIdx.x,
                        s_m, s_inv, s_cnt, s_part);
 }
 
@@ -371,22 +394,22 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     cudaError_t e = cudaFuncSetAttribute(router_bf16_kernel<NT, TOK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    router_bf16_kernel<NT, TOK><<<grid, kRouterThreadsBf16, sm, st>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wg), bias, T, d,
-        E, k, idx, w, logits, probs, aux, tile_counts);
+    return launch_k(router_bf16_kernel<NT, TOK>, dim3(grid), dim3(kRouterThreadsBf16), sm, st,
+                    nullptr, 0, static_cast<const __nv_bfloat16*>(x),
+                    static_cast<const __nv_bfloat16*>(wg), bias, T, d, E, k, idx, w, logits, probs,
+                    aux, tile_counts);
   } else {
     const size_t sm = router_smem_bytes_f32<NT, TOK>();
     cudaError_t e = cudaFuncSetAttribute(router_f32_kernel<NT, TOK>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    router_f32_kernel<NT, TOK><<<grid, 2 * TOK, sm, st>>>(
-        static_cast<const float*>(x), static_cast<const float*>(wg), bias, T, d, E, k, idx, w,
-        logits, probs, aux, tile_counts);
+    return launch_k(router_f32_kernel<NT, TOK>, dim3(grid), dim3(2 * TOK), sm, st, nullptr, 0,
+                    static_cast<const float*>(x), static_cast<const float*>(wg), bias, T, d, E, k,
+                    idx, w, logits, probs, aux, tile_counts);
   }
-  return cudaGetLastError();
 }
 
-inline cudaError_t launch_router(const void* x, const void* wg, const float* bias, int T, int d,
+inline cudaError_t launch_router_mma(const void* x, const void* wg, const float* bias, int T, int d,
                                  int E, int k, bool bf16, int32_t* idx, float* w, float* logits,
                                  float* probs, float* aux, cudaStream_t st,
                                  int32_t* tile_counts = nullptr) {

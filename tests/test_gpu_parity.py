@@ -47,12 +47,22 @@ ROUTER_CASES = [
     ("dense_bf16_e5", 64, 64, 5, 5, "bf16", None),
     ("single_f32_e1", 33, 16, 1, 1, "f32", None),
     ("one_token_f32", 1, 8, 4, 2, "f32", None),
+    ("wide_f32_e200", 100, 64, 200, 4, "f32", None),
+    # several 128-token CTAs of the tensor-core router, ragged last CTA and dispatch tile
+    ("multi_bf16_e16", 1000, 512, 16, 2, "bf16", None),
+    ("multi_bf16_e64", 1000, 512, 64, 4, "bf16", "zipf"),
+    ("multi_bf16_e128", 333, 256, 128, 6, "bf16", None),
 ]
 
 
+@pytest.mark.parametrize("router", ["auto", "warp_mma", "tcgen05"])
 @pytest.mark.parametrize("case", ROUTER_CASES, ids=[c[0] for c in ROUTER_CASES])
-def test_router_parity(moe, torch, case):
+def test_router_parity(moe, torch, case, router, monkeypatch):
     name, T, d, E, k, dt, bias = case
+    if router != "auto":
+        if dt != "bf16":
+            pytest.skip("the bf16 routers only")
+        monkeypatch.setenv("MOE_ROUTER_TC", "1" if router == "tcgen05" else "0")
     cfg = synth.small_config(name, T, d, 64, E, k, dt, seed=zlib.crc32(name.encode()) % 1000, wg_std=0.1,
                              bias="zipf" if bias else "none")
     x, w_g, b = synth.make_x(cfg), synth.make_router_weight(cfg), synth.router_bias(cfg)
@@ -228,9 +238,15 @@ def test_layer_tiny_fp32(moe, torch):
     _check_topk_layer(moe, torch, synth.CONFIGS["tiny_fp32"])
 
 
-def test_layer_small_bf16_multi_tile(moe, torch):
-    cfg = synth.small_config("small_bf16", 1000, 256, 384, 8, 2, "bf16", seed=21, x_std=1.0,
-                             w_std=0.02, wg_std=0.1)
+@pytest.mark.parametrize("router", ["auto", "warp_mma", "tcgen05"])
+@pytest.mark.parametrize("E,k", [(8, 2), (40, 4)])
+def test_layer_small_bf16_multi_tile(moe, torch, E, k, router, monkeypatch):
+    """Several router CTAs and dispatch tiles (32 or 64 tokens per tile, four or two per
+    tensor-core router CTA) with a ragged last one, through the whole layer."""
+    if router != "auto":
+        monkeypatch.setenv("MOE_ROUTER_TC", "1" if router == "tcgen05" else "0")
+    cfg = synth.small_config(f"small_bf16_e{E}", 1000, 256, 384, E, k, "bf16", seed=21 + E,
+                             x_std=1.0, w_std=0.02, wg_std=0.1)
     _check_topk_layer(moe, torch, cfg)
 
 
@@ -435,3 +451,26 @@ def test_cluster_paths_grouped_ragged(moe, torch, mode, monkeypatch):
     assert not torch.isnan(yp_cl).any()
     assert torch.equal(h_cl.view(torch.int16), h_one.view(torch.int16))
     assert torch.equal(yp_cl, yp_one)
+
+
+@pytest.mark.parametrize("k", [2, 4])
+def test_programmatic_dependent_launch_bit_identical(moe, torch, k, monkeypatch):
+    """With programmatic dependent launch each kernel starts under the tail of the previous
+    one but waits for its completion before touching memory: outputs equal the plainly
+    stream-ordered launches bit for bit, over back-to-back layer calls."""
+    cfg = synth.small_config("pdl", 3000, 256, 512, 8, k, "bf16", seed=62, x_std=1.0, w_std=0.05)
+    inp = synth.make_inputs(cfg)
+    w = dev_weights(inp)
+    x = to_dev(inp.x)
+    outs = {}
+    for flag in ("0", "1"):
+        monkeypatch.setenv("MOE_PDL", flag)
+        ys = [torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32, device="cuda")
+              for _ in range(3)]
+        for y in ys:  # back to back on one stream: each call reuses the previous call's buffers
+            moe.moe_layer_forward(x, w, k=k, y=y)
+        outs[flag] = ys
+    torch.cuda.synchronize()
+    for y in outs["0"] + outs["1"]:
+        assert not torch.isnan(y).any()
+        assert torch.equal(y, outs["0"][0])
