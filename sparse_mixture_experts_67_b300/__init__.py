@@ -23,7 +23,7 @@ __all__ = [
     "moe_grouped_gateup_swiglu_gather",
     "moe_grouped_down", "moe_experts_swiglu", "moe_combine", "moe_ec_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_layer_workspace_size", "moe_route_aux_rows", "moe_device_error",
-    "MoELayer",
+    "MoELayer", "HostPipeline",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -407,3 +407,57 @@ class MoELayer:
     def __call__(self, x: torch.Tensor, outputs=None, y=None) -> torch.Tensor:
         return moe_layer_forward(x, self.weights, self.k, self.routing, self.capacity_factor,
                                  outputs=outputs, workspace=self.workspace(x), y=y)
+
+
+class HostPipeline:
+    """Runs a MoELayer over batches held in pinned host memory with the copies
+    overlapped: while batch i runs on the current stream, the host-to-device
+    copy of batch i+1 runs on one copy stream and the device-to-host copy of
+    batch i-1 on another.  Device buffers are double-buffered; every hazard
+    between the three streams is ordered with CUDA events, so results equal
+    those of copying, running and copying back one batch at a time."""
+
+    def __init__(self, layer: MoELayer, T: int, d: int, dtype: torch.dtype,
+                 device: Optional[torch.device] = None, depth: int = 2):
+        if depth < 1:
+            raise ValueError("depth must be >= 1")
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.layer, self.depth = layer, depth
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.xd = [torch.empty((T, d), dtype=dtype, device=dev) for _ in range(depth)]
+        self.yd = [torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(depth)]
+        ev = lambda: [torch.cuda.Event() for _ in range(depth)]  # noqa: E731
+        self._x_ready, self._done, self._y_copied = ev(), ev(), ev()
+        self._used = [False] * depth
+
+    def run(self, xs_host: List[torch.Tensor], ys_host: List[torch.Tensor]) -> None:
+        """ys_host[i] <- layer(xs_host[i]) for every i; enqueue only (synchronise on the
+        current stream, or on the returned work, before reading ys_host).  xs_host[i] are
+        pinned [T, d] tensors of the layer's dtype, ys_host[i] pinned [T, d] fp32."""
+        if len(xs_host) != len(ys_host):
+            raise ValueError("one output per input batch")
+        compute = torch.cuda.current_stream(self.xd[0].device)
+        start = torch.cuda.Event()
+        start.record(compute)
+        self.h2d.wait_event(start)
+        self.d2h.wait_event(start)
+        for i, (xh, yh) in enumerate(zip(xs_host, ys_host)):
+            b = i % self.depth
+            if self._used[b]:
+                self.h2d.wait_event(self._done[b])       # batch i-depth finished reading xd[b]
+                compute.wait_event(self._y_copied[b])    # and its result left yd[b]
+            with torch.cuda.stream(self.h2d):
+                self.xd[b].copy_(xh, non_blocking=True)
+                self._x_ready[b].record(self.h2d)
+            compute.wait_event(self._x_ready[b])
+            self.layer(self.xd[b], y=self.yd[b])
+            self._done[b].record(compute)
+            self.d2h.wait_event(self._done[b])
+            with torch.cuda.stream(self.d2h):
+                yh.copy_(self.yd[b], non_blocking=True)
+                self._y_copied[b].record(self.d2h)
+            self._used[b] = True
+        for b in range(self.depth):  # the current stream ends after every copy back
+            if self._used[b]:
+                compute.wait_event(self._y_copied[b])

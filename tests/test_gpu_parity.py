@@ -474,3 +474,24 @@ def test_programmatic_dependent_launch_bit_identical(moe, torch, k, monkeypatch)
     for y in outs["0"] + outs["1"]:
         assert not torch.isnan(y).any()
         assert torch.equal(y, outs["0"][0])
+
+
+def test_host_pipeline_matches_batchwise(moe, torch):
+    """HostPipeline overlaps each batch's copies with its neighbours' forwards; every output
+    equals copying in, running and copying back that batch alone, bit for bit."""
+    cfg = synth.small_config("pipe", 700, 256, 384, 8, 2, "bf16", seed=63, x_std=1.0, w_std=0.05)
+    inp = synth.make_inputs(cfg)
+    w = dev_weights(inp)
+    layer = moe.MoELayer(w, k=2)
+    rng = np.random.default_rng(5)
+    xs = []
+    for _ in range(5):
+        bits = synth.round_to_bf16_bits(rng.standard_normal((cfg.T, cfg.d)))
+        xs.append(torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory())
+    ys = [torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32).pin_memory() for _ in xs]
+    pipe = moe.HostPipeline(layer, cfg.T, cfg.d, torch.bfloat16)
+    pipe.run(xs, ys)
+    torch.cuda.synchronize()
+    for xh, yh in zip(xs, ys):
+        ref = layer(xh.cuda()).cpu()
+        assert torch.equal(yh, ref)
