@@ -79,12 +79,15 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, or None if the kernel changed since."""
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the kernel changed
+    since or the capture was of another workload."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh)[kernel]
+        if rec.get("workload") != workload:
+            return None
         with open(os.path.join(ROOT, rec["source"]), "rb") as fh:
             sha = hashlib.sha256(fh.read()).hexdigest()
         return rec if sha == rec["source_sha256"] else None
@@ -239,7 +242,8 @@ def run_gpu(args, cfg):
     eager_ms = sum(a.elapsed_time(b) for a, b in eager) / len(eager)
 
     # per-stage breakdown through the individual entry points (same kernels)
-    stages = stage_breakdown(moe, torch, cfg, x, w, flush, stream, min(K, 50)) if not ec else {}
+    stages = (stage_breakdown_ec if ec else stage_breakdown)(moe, torch, cfg, x, w, flush, stream,
+                                                             min(K, 50))
     # end to end through the public API with host buffers
     e2e = run_e2e(moe, torch, layer, inp.x, cfg, dev, min(K, 50))
     clk = clocks.stop()
@@ -277,7 +281,7 @@ def run_gpu(args, cfg):
         gu_ms = stages.get("gateup_ms")
         gu_flops = 4.0 * cfg.R * cfg.d * cfg.F
         achieved = gu_flops / (gu_ms / 1e3) / 1e12
-        traffic = recorded_traffic("gateup")
+        traffic = recorded_traffic("gateup", cfg.name)
         # the kernel is timed alone (events around its launch) for ~0.2 ms at a time:
         # the burst figure is its denominator; the sustained one is reported beside it
         line["roofline"] = {
@@ -326,6 +330,34 @@ def stage_breakdown(moe, torch, cfg, x, w, flush, stream, steps):
         evs[5].record(stream)
         moe.moe_aux_loss(p["counts"], cfg.T, cfg.k, aux_partials=r["aux_partials"])
         evs[6].record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            for j, n in enumerate(names):
+                acc[n] += evs[j].elapsed_time(evs[j + 1])
+    return {n: v / steps for n, v in acc.items()}
+
+
+def stage_breakdown_ec(moe, torch, cfg, x, w, flush, stream, steps):
+    """Expert-choice stages, timed as in stage_breakdown."""
+    names = ["route_ms", "gather_ms", "gateup_ms", "down_ms", "combine_ms"]
+    acc = {n: 0.0 for n in names}
+    for i in range(steps + 3):
+        flush.fill_(i & 0xFF)
+        torch.cuda._sleep(5_000_000)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        evs[0].record(stream)
+        r = moe.moe_expert_choice_route(x, w["w_g"], w["bias"], cfg.capacity_factor)
+        evs[1].record(stream)
+        C = r["C"]
+        offsets = torch.arange(cfg.E + 1, device=x.device, dtype=torch.int32) * C
+        xp = moe.moe_gather_rows(x, r["ec_idx"].view(-1), 1)
+        evs[2].record(stream)
+        h = moe.moe_grouped_gateup_swiglu(xp, offsets, w["w_gate"], w["w_up"])
+        evs[3].record(stream)
+        yp = moe.moe_grouped_down(h, offsets, w["w_down"])
+        evs[4].record(stream)
+        moe.moe_ec_combine(yp, r["pos"], r["ec_score"])
+        evs[5].record(stream)
         torch.cuda.synchronize()
         if i >= 3:
             for j, n in enumerate(names):
