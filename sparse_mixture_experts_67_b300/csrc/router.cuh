@@ -48,15 +48,21 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, cons
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Thread-per-token epilogue over the logits tile S[TOK][ldS] (bias not yet
-// added, when given; S is modified).  k == 0 writes logits only (expert-choice
-// pre-pass).  The CTA's tokens form TOK / SUB dispatch tiles of SUB tokens,
-// numbered from tile0: each gets its own row of aux partial sums (aux_rows,
-// the row of tile0, nullable) and of per-expert selection counts (tile_counts,
-// the dispatch histogram of its SUB*k assignments, nullable).
+// Epilogue over the logits tile S[TOK][ldS] (bias not yet added, when given;
+// S is modified) with P adjacent threads per token (threads past TOK * P only
+// join the cooperative loops): thread r * P + q owns the experts
+// e = q, q + P, ... of token row r; row max,
+// sum and the top-k arg-max are reduced over the P threads with shuffles (the
+// top-k compares (logit desc, index asc), so ties still go to the lower
+// index).  ldS = P (mod 32) keeps those reads free of bank conflicts.
+// k == 0 writes logits only (expert-choice pre-pass).  The CTA's tokens form
+// TOK / SUB dispatch tiles of SUB tokens, numbered from tile0: each gets its
+// own row of aux partial sums (aux_rows, the row of tile0, nullable) and of
+// per-expert selection counts (tile_counts, the dispatch histogram of its
+// SUB*k assignments, nullable).
 // Shared scratch: s_m / s_inv TOK floats each; s_cnt (TOK / SUB) *
 // MOE_MAX_EXPERTS ints; s_part max(blockDim.x, E) floats.
-template <int TOK, int SUB = TOK>
+template <int TOK, int SUB = TOK, int P = 1>
 __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k,
                                 const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                                 float* __restrict__ w_out, float* __restrict__ logits_out,
@@ -64,35 +70,46 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
                                 int32_t* __restrict__ tile_counts, int tile0, float* s_m,
                                 float* s_inv, int* s_cnt, float* s_part) {
   static_assert(TOK % SUB == 0, "dispatch tiles split the CTA's tokens");
+  static_assert(P >= 1 && P <= 32 && (P & (P - 1)) == 0, "threads per token: a power of two");
   constexpr int NSUB = TOK / SUB;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int ntok = min(TOK, T - tok0);
   const int nsub = (ntok + SUB - 1) / SUB;  // dispatch tiles holding tokens
+  const int r = tid / P, q = tid % P;       // this thread's token row and expert phase
+  const bool live = r < ntok;
   if (bias) {
     for (int i = tid; i < ntok * E; i += nthr) {
-      const int r = i / E, e = i - r * E;
-      S[r * ldS + e] += bias[e];
+      const int ri = i / E, e = i - ri * E;
+      S[ri * ldS + e] += bias[e];
     }
     __syncthreads();
   }
-  if (k > 0 && tid < ntok) {
-    const float* row = S + tid * ldS;
-    float m = row[0];
-    for (int e = 1; e < E; ++e) m = fmaxf(m, row[e]);
+  if (k > 0) {
+    const float* row = S + r * ldS;
+    float m = -INFINITY;
+    if (live)
+      for (int e = q; e < E; e += P) m = fmaxf(m, row[e]);
+#pragma unroll
+    for (int o = 1; o < P; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
     float sum = 0.f;
-    for (int e = 0; e < E; ++e) sum += expf(row[e] - m);
-    s_m[tid] = m;
-    s_inv[tid] = 1.0f / sum;
+    if (live)
+      for (int e = q; e < E; e += P) sum += expf(row[e] - m);
+#pragma unroll
+    for (int o = 1; o < P; o <<= 1) sum += __shfl_xor_sync(kFullMask, sum, o);
+    if (live && q == 0) {
+      s_m[r] = m;
+      s_inv[r] = 1.0f / sum;
+    }
   }
   __syncthreads();
   // coalesced optional outputs: element i of the CTA's [ntok, E] block
   if (logits_out || probs_out) {
     const size_t base = (size_t)tok0 * E;
     for (int i = tid; i < ntok * E; i += nthr) {
-      const int r = i / E, e = i - r * E;
-      const float v = S[r * ldS + e];
+      const int ri = i / E, e = i - ri * E;
+      const float v = S[ri * ldS + e];
       if (logits_out) logits_out[base + i] = v;
-      if (probs_out) probs_out[base + i] = expf(v - s_m[r]) * s_inv[r];
+      if (probs_out) probs_out[base + i] = expf(v - s_m[ri]) * s_inv[ri];
     }
   }
   if (k == 0) return;
@@ -108,7 +125,7 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
       for (int c = tid; c < G * E; c += nthr) {
         const int e = c % E, gi = c / E;
         float acc = 0.f;
-        for (int r = r0 + gi; r < r1; r += G) acc += expf(S[r * ldS + e] - s_m[r]) * s_inv[r];
+        for (int ri = r0 + gi; ri < r1; ri += G) acc += expf(S[ri * ldS + e] - s_m[ri]) * s_inv[ri];
         s_part[gi * E + e] = acc;
       }
       __syncthreads();
@@ -121,34 +138,48 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
     }
   }
   __syncthreads();  // the top-k below overwrites selected entries of S
-  if (tid < ntok) {
-    float* row = S + tid * ldS;
-    const float m = s_m[tid], inv = s_inv[tid];
-    const int t = tok0 + tid;
+  {
+    float* row = S + r * ldS;
+    const float m = live ? s_m[r] : 0.f, inv = live ? s_inv[r] : 0.f;
+    const int t = tok0 + r;
     float selsum = 0.f;
     for (int j = 0; j < k; ++j) {
-      float best = 0.f;
+      float best = -INFINITY;
       int bi = -1;
-      for (int e = 0; e < E; ++e) {  // ascending e + strict '>' keeps the lower index on ties
-        const float v = row[e];
-        if (bi < 0 ? v > -INFINITY : v > best) {
-          best = v;
-          bi = e;
+      if (live)
+        for (int e = q; e < E; e += P) {  // ascending e + strict '>': lower index on ties
+          const float v = row[e];
+          if (bi < 0 ? v > -INFINITY : v > best) {
+            best = v;
+            bi = e;
+          }
+        }
+#pragma unroll
+      for (int o = 1; o < P; o <<= 1) {  // (larger logit, then lower index); none loses
+        const float ob = __shfl_xor_sync(kFullMask, best, o);
+        const int oi = __shfl_xor_sync(kFullMask, bi, o);
+        if (oi >= 0 && (bi < 0 || ob > best || (ob == best && oi < bi))) {
+          best = ob;
+          bi = oi;
         }
       }
       if (bi < 0) {  // only for non-finite logits (NaN / -inf everywhere): stay in range
         bi = j;
-        best = row[bi];
+        best = live ? row[bi] : 0.f;
       }
-      row[bi] = -INFINITY;  // taken (logits are finite)
+      if (live && bi % P == q) row[bi] = -INFINITY;  // taken; only this thread reads it again
       const float gsel = expf(best - m) * inv;  // same arithmetic as probs
       selsum += gsel;
-      idx_out[(size_t)t * k + j] = bi;
-      w_out[(size_t)t * k + j] = gsel;
-      if (tile_counts) atomicAdd(&s_cnt[(tid / SUB) * MOE_MAX_EXPERTS + bi], 1);
+      if (live && q == 0) {
+        idx_out[(size_t)t * k + j] = bi;
+        w_out[(size_t)t * k + j] = gsel;
+        if (tile_counts) atomicAdd(&s_cnt[(r / SUB) * MOE_MAX_EXPERTS + bi], 1);
+      }
     }
-    const float rs = 1.0f / selsum;
-    for (int j = 0; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
+    if (live && q == 0) {
+      const float rs = 1.0f / selsum;
+      for (int j = 0; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
+    }
   }
   if (tile_counts) {
     __syncthreads();
@@ -183,7 +214,10 @@ struct RouterBf16 {
   static constexpr int STAGES =
       FIT2 >= 3 ? (FIT2 > 8 ? 8 : (int)FIT2) : (FIT1 >= 3 ? 3 : (FIT1 < 2 ? 2 : (int)FIT1));
   static constexpr size_t RING = (size_t)STAGES * STAGE_BYTES;
-  static constexpr int LDS = EP + 1;
+  // epilogue threads per token: 4 from E > 16 on (TOK = 64; measured 44.8 -> 39.2 us at
+  // T=16384, E=64), 1 below (TOK = 32; 4-8 threads per token measured slower at E=8)
+  static constexpr int P = TOK == 64 ? 4 : 1;
+  static constexpr int LDS = ((EP + 31) / 32) * 32 + P;  // = P (mod 32): conflict-free epilogue
   static constexpr size_t PART = (size_t)KG * TOK * LDS * 4;  // per-K-group partial logits
   static constexpr size_t TILE = (size_t)TOK * LDS * 4;
   static constexpr size_t MAIN = RING > PART + TILE ? RING : PART + TILE;
@@ -306,7 +340,7 @@ __global__ void __launch_bounds__(kRouterThreadsBf16)
     S[r * ldS + e] = v;
   }
   __syncthreads();
-  router_epilogue<TOK>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
+  router_epilogue<TOK, TOK, C::P>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
                        blockIdx.x,
                        s_m, s_inv, s_cnt, s_part);
@@ -318,7 +352,7 @@ template <int NT, int TOK>
 constexpr size_t router_smem_bytes_f32() {
   constexpr size_t ld = kRouterBKf + 1;
   constexpr size_t tiles = (size_t)(TOK + 8 * NT) * ld * 4;
-  constexpr size_t acc = (size_t)TOK * (8 * NT + 1) * 4;
+  constexpr size_t acc = (size_t)TOK * (((8 * NT + 31) / 32) * 32 + (TOK == 64 ? 2 : 1)) * 4;  // S
   // s_m, s_inv; s_cnt; s_part (max(threads, E) floats)
   return tiles + acc + 2 * TOK * 4 + MOE_MAX_EXPERTS * 4 +
          (2 * TOK > MOE_MAX_EXPERTS ? 2 * TOK : MOE_MAX_EXPERTS) * 4;
@@ -334,7 +368,8 @@ __global__ void __launch_bounds__(2 * TOK)
   pdl_begin();
   constexpr int EP = 8 * NT;
   constexpr int ld = kRouterBKf + 1;
-  constexpr int ldS = EP + 1;
+  constexpr int kPf = TOK == 64 ? 2 : 1;               // epilogue threads per token
+  constexpr int ldS = ((EP + 31) / 32) * 32 + kPf;  // = kPf (mod 32)
   extern __shared__ __align__(16) unsigned char smem[];
   float* xs = reinterpret_cast<float*>(smem);
   constexpr int kThr = 2 * TOK;
@@ -372,7 +407,7 @@ __global__ void __launch_bounds__(2 * TOK)
 #pragma unroll
   for (int i = 0; i < 4 * NT; ++i) S[tt * ldS + eh + 2 * i] = acc[i];
   __syncthreads();
-  router_epilogue<TOK>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
+  router_epilogue<TOK, TOK, kPf>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
                        blockIdx.x,
                        s_m, s_inv, s_cnt, s_part);

@@ -4,17 +4,18 @@
 // tcgen05 with the tokens as the MMA's M, followed by the same softmax,
 // top-k, renormalisation and aux partial sums as the warp-MMA router.
 //
-// One CTA of 4 warps owns 128 tokens:
+// One CTA of 16 warps owns 128 tokens:
 //   - one thread streams [128 x 64] x tiles and [EN x 64] W_g tiles (EN = E
 //     rounded up to 16 .. 256; rows past E read as zero) with 2-D TMA into a
 //     shared-memory ring;
 //   - one thread issues tcgen05.mma kind::f16 (M = 128, N = EN, K = 16,
 //     fp32 accumulate) into TMEM, freeing each stage by tcgen05.commit;
-//   - every thread then reads its own token's row of logits from TMEM (TMEM
-//     lane = token), adds the bias and stores the row to shared memory, where
-//     the thread-per-token epilogue of the warp-MMA router runs.  The 128
-//     tokens form 128 / SUB dispatch tiles (SUB = 32 or 64 tokens, the tile
-//     the dispatch histogram and the aux partial rows are kept per).
+//   - the first 4 warps then read one token's row of logits each from TMEM
+//     (TMEM lane = token), add the bias and store the rows to shared memory,
+//     where the epilogue of the warp-MMA router runs with 4 threads per token
+//     (E > 16) over all 16 warps.  The 128 tokens form 128 / SUB dispatch tiles (SUB =
+//     32 or 64 tokens, the tile the dispatch histogram and the aux partial
+//     rows are kept per).
 // Every barrier wait is bounded; on expiry the kernel records an error code,
 // drains its copies and MMAs, frees TMEM and returns without outputs.
 #pragma once
@@ -26,15 +27,18 @@ namespace moe {
 namespace rtc {
 
 constexpr int kTok = 128;      // tokens per CTA: the MMA's M
-constexpr int kThreads = 128;  // thread = token = TMEM lane in the epilogue
+constexpr int kThreads = 512;  // 16 warps: warps 0-3 read TMEM (thread = token = lane)
 constexpr int kBK = 64;        // K per stage: one 128-byte swizzled row per token
 
 template <int EN>
 struct Cfg {
+  // epilogue threads per token: 4 (measured 34.8 -> 30.6 us at T=16384, E=64);
+  // 1 for E <= 16, where wider groups measured slower
+  static constexpr int P = EN > 16 ? kThreads / kTok : 1;
   static constexpr int A_BYTES = kTok * kBK * 2;  // 16 KiB
   static constexpr int B_BYTES = EN * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int LDS = EN + 1;  // fp32 logits tile pitch (odd: conflict-free rows)
+  static constexpr int LDS = ((EN + 31) / 32) * 32 + P;  // logits tile pitch, = P (mod 32)
   static constexpr int S_BYTES = kTok * LDS * 4;
   // about 192 KiB of ring (one CTA per SM; measured 6% faster than 96 KiB at
   // E = 64); the logits tile reuses the ring once the MMAs are done
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();  // loads landed and MMAs done: the ring may hold the logits tile
   const bool aborted = *abort_flag != 0;
   float* Sx = reinterpret_cast<float*>(ring);  // [kTok][LDS]
-  if (!aborted) {
+  if (!aborted && warp < 4) {
     tc_fence_after();
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
     float* row = Sx + threadIdx.x * C::LDS;
@@ -196,7 +200,7 @@ __global__ void __launch_bounds__(kThreads)
   if (aborted) return;
   constexpr int kSubTiles = kTok / SUB;
   const int tile0 = blockIdx.x * kSubTiles;
-  router_epilogue<kTok, SUB>(Sx, C::LDS, tok0, T, E, k, nullptr, idx_out, w_out, logits_out,
+  router_epilogue<kTok, SUB, C::P>(Sx, C::LDS, tok0, T, E, k, nullptr, idx_out, w_out, logits_out,
                              probs_out, aux_partials ? aux_partials + (size_t)tile0 * E : nullptr,
                              tile_counts, tile0, S.s_m, S.s_inv, S.s_cnt, S.s_part);
 }
