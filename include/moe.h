@@ -102,7 +102,10 @@ moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, i
  *   ec_idx [E,C] int32 token ids, ec_score [E,C] fp32 scores,
  *   pos [E,T] int32: e*C + c where token t is expert e's c-th pick, else -1
  *     (the non-zero pattern of the page's dispatch mask; dispatch row of a pick),
- *   logits [T,E] fp32: required (it is also the kernel's scratch).
+ *   logits [T,E] fp32: required.
+ * pos doubles as scratch: the router stores the logits there transposed
+ * ([E,T] fp32 bits) and the selection of expert e reads row e once, coalesced,
+ * before writing the position map over it.
  * Limits: T <= 16384 (one expert's keys are sorted in shared memory),
  *         C <= T, E <= 256.                                                  */
 int moe_expert_choice_capacity(int T, int E, float capacity_factor);

@@ -11,7 +11,10 @@
 //     equal to it, the lowest token ids (ties go to the lower token);
 //   - only the C picks are sorted (bitonic, in shared memory) by descending
 //     logit then ascending token, the output order.
-// The logits come from the router kernel run in logits-only mode.
+// The logits come from the router kernel run in logits-only mode, which also
+// writes them transposed into pos ([E, T], as fp32 bits): CTA e reads its row
+// there once, coalesced, keeps the order-preserving keys in shared memory and
+// only then overwrites the row with the position map.
 #pragma once
 
 #include <float.h>
@@ -55,6 +58,11 @@ __device__ __forceinline__ uint32_t float_order_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Inverse of float_order_key (exact; -0 comes back as +0).
+__device__ __forceinline__ float order_key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 inline int next_pow2_host(int v) {
   int p = 1;
   while (p < v) p <<= 1;
@@ -95,9 +103,8 @@ inline size_t ec_route_smem(int T, int C) {
 }
 
 __global__ void __launch_bounds__(kEcThreads)
-    ec_route_kernel(const float* __restrict__ logits, int T, int E, int C, int c_pow2,
-                    int32_t* __restrict__ ec_idx, float* __restrict__ ec_score,
-                    int32_t* __restrict__ pos) {
+    ec_route_kernel(int T, int E, int C, int c_pow2, int32_t* __restrict__ ec_idx,
+                    float* __restrict__ ec_score, int32_t* __restrict__ pos) {
   pdl_begin();
   extern __shared__ __align__(16) unsigned char ec_smem[];
   uint32_t* s_key = reinterpret_cast<uint32_t*>(ec_smem);  // ascending = descending logit
@@ -112,17 +119,20 @@ __global__ void __launch_bounds__(kEcThreads)
   const int per = (T + kEcThreads - 1) / kEcThreads;
   const int t0 = min(T, threadIdx.x * per), t1 = min(T, t0 + per);
 
+  int32_t* prow = pos + (size_t)e * T;  // on entry: this expert's logits (fp32 bits)
   float m = -FLT_MAX;
-  for (int t = t0; t < t1; ++t) {
-    const float v = logits[(size_t)t * E + e];
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {  // coalesced
+    const float v = __int_as_float(prow[t]);
     m = fmaxf(m, v);
     s_key[t] = ~float_order_key(v);
-    pos[(size_t)e * T + t] = -1;
   }
-  m = block_reduce_max(m, scratch);
+  m = block_reduce_max(m, scratch);  // every read of the row is done past this barrier
   float sum = 0.f;
-  for (int t = t0; t < t1; ++t) sum += expf(logits[(size_t)t * E + e] - m);
-  sum = block_reduce_sum(sum, scratch);  // also publishes s_key / pos writes to the CTA
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    sum += expf(order_key_float(~s_key[t]) - m);
+    prow[t] = -1;
+  }
+  sum = block_reduce_sum(sum, scratch);  // also publishes the pos writes to the CTA
   if (C <= 0) return;
 
   // radix select: the C-th smallest key K* and how many keys equal to it to take
@@ -208,7 +218,7 @@ __global__ void __launch_bounds__(kEcThreads)
   const float inv = 1.0f / sum;
   for (int c = threadIdx.x; c < C; c += blockDim.x) {
     const int t = (int)(s_sel[c] & 0xffffffffu);
-    const float v = logits[(size_t)t * E + e];
+    const float v = order_key_float((uint32_t)(s_sel[c] >> 32) ^ 0xffffffffu);
     ec_idx[(size_t)e * C + c] = t;
     ec_score[(size_t)e * C + c] = expf(v - m) * inv;
     pos[(size_t)e * T + t] = e * C + c;

@@ -110,15 +110,16 @@ moe_status moe_expert_choice_route(const void* x, const void* w_g, const float* 
   if (!x || !w_g || !pos || !logits || (C > 0 && (!ec_idx || !ec_score))) return MOE_ERR_INVALID_ARG;
   if (dt == MOE_BF16 && (!aligned16(x) || !aligned16(w_g))) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
+  // logits [T, E] for the caller, and transposed into pos for the selection
   cudaError_t e = launch_router(x, w_g, bias, T, d, E, /*k=*/0, dt == MOE_BF16, nullptr, nullptr,
-                                logits, nullptr, nullptr, s);
+                                logits, nullptr, nullptr, s, nullptr, reinterpret_cast<float*>(pos));
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const int c2 = next_pow2(C > 0 ? C : 1);
   const size_t sm = ec_route_smem(T, C > 0 ? C : 1);
   e = cudaFuncSetAttribute(ec_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_k(ec_route_kernel, dim3(E), dim3(kEcThreads), sm, s, nullptr, 0, logits,
-                              T, E, C, c2, ec_idx, ec_score, pos));
+  return cuda_status(launch_k(ec_route_kernel, dim3(E), dim3(kEcThreads), sm, s, nullptr, 0, T, E, C,
+                              c2, ec_idx, ec_score, pos));
 }
 
 size_t moe_permute_workspace_size(int T, int E, int k) {

@@ -62,13 +62,16 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, cons
 // SUB*k assignments, nullable).
 // Shared scratch: s_m / s_inv TOK floats each; s_cnt (TOK / SUB) *
 // MOE_MAX_EXPERTS ints; s_part max(blockDim.x, E) floats.
+// logitsT_out (nullable): the logits once more, transposed to [E, T] (row e is
+// what the expert-choice selection of expert e reads).
 template <int TOK, int SUB = TOK, int P = 1>
 __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k,
                                 const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                                 float* __restrict__ w_out, float* __restrict__ logits_out,
                                 float* __restrict__ probs_out, float* __restrict__ aux_rows,
                                 int32_t* __restrict__ tile_counts, int tile0, float* s_m,
-                                float* s_inv, int* s_cnt, float* s_part) {
+                                float* s_inv, int* s_cnt, float* s_part,
+                                float* __restrict__ logitsT_out = nullptr) {
   static_assert(TOK % SUB == 0, "dispatch tiles split the CTA's tokens");
   static_assert(P >= 1 && P <= 32 && (P & (P - 1)) == 0, "threads per token: a power of two");
   constexpr int NSUB = TOK / SUB;
@@ -110,6 +113,12 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
       const float v = S[ri * ldS + e];
       if (logits_out) logits_out[base + i] = v;
       if (probs_out) probs_out[base + i] = expf(v - s_m[ri]) * s_inv[ri];
+    }
+  }
+  if (logitsT_out) {  // element i of the CTA's [E, ntok] block, tokens fastest
+    for (int i = tid; i < ntok * E; i += nthr) {
+      const int e = i / ntok, ri = i - e * ntok;
+      logitsT_out[(size_t)e * T + tok0 + ri] = S[ri * ldS + e];
     }
   }
   if (k == 0) return;
@@ -236,7 +245,8 @@ __global__ void __launch_bounds__(kRouterThreadsBf16)
                        const float* __restrict__ bias, int T, int d, int E, int k,
                        int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                        float* __restrict__ logits_out, float* __restrict__ probs_out,
-                       float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts) {
+                       float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts,
+                       float* __restrict__ logitsT) {
   pdl_begin();
   using C = RouterBf16<NT, TOK>;
   constexpr int EP = C::EP, LD = C::LD, SBK = C::SBK, STAGES = C::STAGES;
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(kRouterThreadsBf16)
   router_epilogue<TOK, TOK, C::P>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
                        blockIdx.x,
-                       s_m, s_inv, s_cnt, s_part);
+                       s_m, s_inv, s_cnt, s_part, logitsT);
 }
 
 // fp32 router: FFMA over 32-wide d chunks, same epilogue.
@@ -364,7 +374,8 @@ __global__ void __launch_bounds__(2 * TOK)
                       const float* __restrict__ bias, int T, int d, int E, int k,
                       int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                       float* __restrict__ logits_out, float* __restrict__ probs_out,
-                      float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts) {
+                      float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts,
+                      float* __restrict__ logitsT) {
   pdl_begin();
   constexpr int EP = 8 * NT;
   constexpr int ld = kRouterBKf + 1;
@@ -410,7 +421,7 @@ __global__ void __launch_bounds__(2 * TOK)
   router_epilogue<TOK, TOK, kPf>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
                        blockIdx.x,
-                       s_m, s_inv, s_cnt, s_part);
+                       s_m, s_inv, s_cnt, s_part, logitsT);
 }
 
 inline int router_nt(int E) {
@@ -422,7 +433,7 @@ inline int router_nt(int E) {
 template <int NT, int TOK>
 cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, int T, int d, int E,
                              int k, bool bf16, int32_t* idx, float* w, float* logits, float* probs,
-                             float* aux, int32_t* tile_counts, cudaStream_t st) {
+                             float* aux, int32_t* tile_counts, float* logitsT, cudaStream_t st) {
   const int grid = ceil_div(T, TOK);
   if (bf16) {
     const size_t sm = router_smem_bytes_bf16<NT, TOK>();
@@ -432,7 +443,7 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     return launch_k(router_bf16_kernel<NT, TOK>, dim3(grid), dim3(kRouterThreadsBf16), sm, st,
                     nullptr, 0, static_cast<const __nv_bfloat16*>(x),
                     static_cast<const __nv_bfloat16*>(wg), bias, T, d, E, k, idx, w, logits, probs,
-                    aux, tile_counts);
+                    aux, tile_counts, logitsT);
   } else {
     const size_t sm = router_smem_bytes_f32<NT, TOK>();
     cudaError_t e = cudaFuncSetAttribute(router_f32_kernel<NT, TOK>,
@@ -440,21 +451,21 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     if (e != cudaSuccess) return e;
     return launch_k(router_f32_kernel<NT, TOK>, dim3(grid), dim3(2 * TOK), sm, st, nullptr, 0,
                     static_cast<const float*>(x), static_cast<const float*>(wg), bias, T, d, E, k,
-                    idx, w, logits, probs, aux, tile_counts);
+                    idx, w, logits, probs, aux, tile_counts, logitsT);
   }
 }
 
 inline cudaError_t launch_router_mma(const void* x, const void* wg, const float* bias, int T, int d,
                                  int E, int k, bool bf16, int32_t* idx, float* w, float* logits,
                                  float* probs, float* aux, cudaStream_t st,
-                                 int32_t* tile_counts = nullptr) {
+                                 int32_t* tile_counts = nullptr, float* logitsT = nullptr) {
 #define MOE_ROUTER_CASE(NT_)                                                                     \
   case NT_:                                                                                      \
     return router_tokens(E) == 32                                                                \
                ? launch_router_nt<NT_, 32>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, \
-                                           aux, tile_counts, st)                                 \
+                                           aux, tile_counts, logitsT, st)                                 \
                : launch_router_nt<NT_, 64>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, \
-                                           aux, tile_counts, st);
+                                           aux, tile_counts, logitsT, st);
   switch (router_nt(E)) {
     MOE_ROUTER_CASE(1)
     MOE_ROUTER_CASE(2)
@@ -463,7 +474,7 @@ inline cudaError_t launch_router_mma(const void* x, const void* wg, const float*
     MOE_ROUTER_CASE(16)
     default:
       return launch_router_nt<32, 64>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux,
-                                      tile_counts, st);
+                                      tile_counts, logitsT, st);
   }
 #undef MOE_ROUTER_CASE
 }
