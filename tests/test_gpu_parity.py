@@ -318,6 +318,35 @@ def test_layer_expert_choice_fp32(moe, torch):
     _check_ec_layer(moe, torch, cfg)
 
 
+@pytest.mark.parametrize("T,E,cf", [(6000, 2, 1.0), (40, 4, 2.0), (40, 4, 1.0), (2000, 3, 1.7)],
+                         ids=["C3000_several_per_thread", "C20", "C10", "C1133"])
+def test_layer_expert_choice_capacities(moe, torch, T, E, cf):
+    """Capacities below a warp, between a warp and the CTA, and above the CTA's thread
+    count (several sorted picks per thread), through the whole layer."""
+    cfg = synth.LayerConfig(f"ec_T{T}_E{E}", T=T, d=64, F=64, E=E, k=0, dtype="bf16", x_std=1.0,
+                            w_std=0.05, wg_std=0.1, seed=34, routing="expert_choice",
+                            capacity_factor=cf)
+    _check_ec_layer(moe, torch, cfg)
+
+
+def test_expert_choice_route_exact_ties(moe, torch):
+    """Tokens with identical rows tie exactly on every expert's logit: the selection keeps
+    the lower token ids and orders equal scores by token, as the oracle does."""
+    cfg = synth.small_config("ec_ties", 1200, 64, 64, 5, 1, "bf16", seed=35, wg_std=0.1)
+    x = synth.make_x(cfg)
+    x = np.ascontiguousarray(np.tile(x[:16], (cfg.T // 16, 1)))  # 16 distinct rows, repeated
+    w_g = synth.make_router_weight(cfg)
+    cf = 1.25  # exact in fp32: the capacity is floor(T * cf / E) of the fp32 factor
+    r = moe.moe_expert_choice_route(to_dev(x), to_dev(w_g), None, cf)
+    torch.cuda.synchronize()
+    s_gpu = _np(r["logits"]).astype(np.float64)
+    C_ref, idx_g, sc_g, pos_g = oracle.expert_choice_route(s_gpu, cf)
+    assert C_ref == r["C"]
+    np.testing.assert_array_equal(_np(r["ec_idx"]), idx_g)
+    np.testing.assert_array_equal(_np(r["pos"]), pos_g)
+    np.testing.assert_allclose(_np(r["ec_score"]), sc_g, rtol=1e-5, atol=1e-9)
+
+
 @pytest.mark.slow
 def test_layer_ec_e16(moe, torch):
     _check_ec_layer(moe, torch, synth.CONFIGS["ec_e16"])
