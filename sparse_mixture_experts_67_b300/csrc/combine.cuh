@@ -71,21 +71,40 @@ __global__ void __launch_bounds__(kCombineThreads)
         const int e = e0 + lane;
         const int p = (e < E) ? pos[(size_t)e * T + t] : -1;
         unsigned hit = __ballot_sync(kFullMask, p >= 0);
-        while (hit) {  // ascending expert order
-          const int src_lane = __ffs(hit) - 1;
+        while (hit) {  // ascending expert order, two experts' rows in flight at a time
+          const int la = __ffs(hit) - 1;
           hit &= hit - 1;
-          const int row = __shfl_sync(kFullMask, p, src_lane);
-          const float s = score[row];
-          const float4* src = y_perm + (size_t)row * d4;
+          const int lb = hit ? __ffs(hit) - 1 : -1;
+          if (hit) hit &= hit - 1;
+          const int ra = __shfl_sync(kFullMask, p, la);
+          const int rb = __shfl_sync(kFullMask, p, lb < 0 ? la : lb);
+          const float sa = score[ra];
+          const float sb = lb < 0 ? 0.f : score[rb];
+          const float4* srca = y_perm + (size_t)ra * d4;
+          const float4* srcb = y_perm + (size_t)rb * d4;
+          float4 va[8], vb[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int c = c0 + lane + 32 * i;
             if (c < d4) {
-              const float4 v = __ldg(src + c);
-              acc[i].x = fmaf(s, v.x, acc[i].x);
-              acc[i].y = fmaf(s, v.y, acc[i].y);
-              acc[i].z = fmaf(s, v.z, acc[i].z);
-              acc[i].w = fmaf(s, v.w, acc[i].w);
+              va[i] = __ldg(srca + c);
+              if (lb >= 0) vb[i] = __ldg(srcb + c);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c = c0 + lane + 32 * i;
+            if (c < d4) {
+              acc[i].x = fmaf(sa, va[i].x, acc[i].x);
+              acc[i].y = fmaf(sa, va[i].y, acc[i].y);
+              acc[i].z = fmaf(sa, va[i].z, acc[i].z);
+              acc[i].w = fmaf(sa, va[i].w, acc[i].w);
+              if (lb >= 0) {
+                acc[i].x = fmaf(sb, vb[i].x, acc[i].x);
+                acc[i].y = fmaf(sb, vb[i].y, acc[i].y);
+                acc[i].z = fmaf(sb, vb[i].z, acc[i].z);
+                acc[i].w = fmaf(sb, vb[i].w, acc[i].w);
+              }
             }
           }
         }
