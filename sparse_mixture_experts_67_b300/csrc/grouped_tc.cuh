@@ -475,7 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // unit -> tile coordinates, first output column inside the tile, column count
   auto unit_at = [&](int u, TileCoord& c, int& col_off, int& width) {
     if (u < full_units) {
-      c = map_tile(S, E, n_tiles, u, kUnitRows);
+      // down: the last experts first, whose H rows the gate/up kernel wrote last
+      // (still in L2 when this kernel starts)
+      c = map_tile(S, E, n_tiles, GATEUP ? u : full_units - 1 - u, kUnitRows);
       c.row0 += (int)crank * BM;  // this CTA's half of the cluster's rows
       col_off = 0;
       width = kTileN;
