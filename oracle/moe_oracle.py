@@ -17,7 +17,10 @@ Readings of points the pages leave open (each also listed in the design notes):
   * selection is made on the logits (softmax is monotone within a row), ties go
     to the lower expert index; slot 0 holds the largest weight;
   * the selected weights are renormalised to sum to 1 (code on every page);
-  * f_i = count_i / T, so sum(f) = k, loss = E * sum(f * p) (unweighted);
+    without renormalisation (the equations of [moe-intro] and [sparse-moe]) they
+    are the selected softmax probabilities as they are;
+  * f_i = count_i / T, so sum(f) = k, loss = E * sum(f * p) (unweighted); in the
+    convention of [sparse-moe] f_i = count_i / (T k), so sum(f) = 1;
   * the router bias, when present, is added to the logits before the softmax;
   * expert choice selects per expert on the logit column (same order as the
     softmax over tokens), ties to the lower token index, output in descending
@@ -67,18 +70,21 @@ def topk_select(s: Array, k: int) -> Array:
     return np.argsort(-s, axis=1, kind="stable")[:, :k].astype(np.int64)
 
 
-def topk_route(s: Array, k: int) -> Tuple[Array, Array, Array]:
+def topk_route(s: Array, k: int, renormalize: bool = True) -> Tuple[Array, Array, Array]:
     """(idx [T,k], w [T,k], g [T,E]) with w the renormalised selected probabilities.
 
     [moe-theory] MoELayer.route: g = softmax(s); select top-k; w_j = g_{i_j} / sum_sel g.
     [sparse-moe] TopKGating.forward does the same with torch.topk.
+    renormalize=False: w_j = g_{i_j} as it is, the gate of the equations in
+    [moe-intro] "ゲート / ルーターって何者？" (y = sum over TopK of g_i E_i(x)) and of the
+    top-k gating formula in [sparse-moe].
     """
     g = softmax(s, axis=1)
     idx = topk_select(s, k)
     w = np.zeros(idx.shape, np.float64)
     for t in range(s.shape[0]):
         sel = g[t, idx[t]]
-        w[t] = sel / np.sum(sel)
+        w[t] = sel / np.sum(sel) if renormalize else sel
     return idx, w, g
 
 
@@ -98,6 +104,22 @@ def aux_stats(g: Array, idx: Array, E: int) -> Tuple[Array, Array, Array, float]
     p = np.mean(g, axis=0)
     loss = float(E * np.sum(f * p))
     return counts, f, p, loss
+
+
+def aux_stats_fraction(g: Array, idx: Array, E: int) -> Tuple[Array, float]:
+    """(f [E], loss) in the convention of [sparse-moe] compute_load_balancing_loss:
+    f_i is the fraction of the T*k assignments routed to expert i (sum f = 1),
+    p_i the mean routing probability, loss = E * sum_i f_i p_i (balanced routing
+    gives 1).
+    """
+    T, k = idx.shape
+    counts = np.zeros(E, np.int64)
+    for t in range(T):
+        for j in range(k):
+            counts[idx[t, j]] += 1
+    f = counts.astype(np.float64) / (T * k)
+    p = np.mean(g, axis=0)
+    return f, float(E * np.sum(f * p))
 
 
 def dispatch(idx: Array, E: int) -> Tuple[Array, Array, Array, Array]:

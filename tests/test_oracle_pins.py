@@ -147,6 +147,62 @@ def pin_all_ties(orc):
         assert abs(loss - k) < 1e-12
 
 
+def pin_unrenormalised_route(orc):
+    """Without renormalisation the weights are the selected softmax probabilities of the
+    equations ([moe-intro], [sparse-moe]): hand values, the same selection, the same
+    ratios, and all of g back when k = E."""
+    g = _golden()
+    case = g["route_three_experts_top2"]
+    x = np.asarray(case["x"], np.float64)
+    w_g = np.vectorize(_log_entry)(np.asarray(case["w_g_log"], np.float64))
+    s = orc.router_logits(x, w_g)
+    idx, w, probs = orc.topk_route(s, case["k"], renormalize=False)
+    assert idx.tolist() == case["idx"]
+    g_hand = _frac(case["g"])
+    np.testing.assert_allclose(w, np.take_along_axis(g_hand, np.asarray(case["idx"]), axis=1),
+                               rtol=0, atol=1e-15)
+    # W_g = 0, E = 8, k = 2: every probability is 1/8
+    s0 = orc.router_logits(np.ones((3, 4)), np.zeros((8, 4)))
+    _, w0, _ = orc.topk_route(s0, 2, renormalize=False)
+    np.testing.assert_allclose(w0, 1.0 / 8, rtol=0, atol=1e-16)
+    rng = np.random.default_rng(21)
+    s = rng.normal(0, 2.0, (40, 7))
+    for k in (1, 3, 7):
+        idx_n, w_n, g_n = orc.topk_route(s, k, renormalize=False)
+        idx_r, w_r, _ = orc.topk_route(s, k)
+        np.testing.assert_array_equal(idx_n, idx_r)
+        assert np.all(w_n.sum(axis=1) <= 1.0 + 1e-15)
+        np.testing.assert_allclose(w_n / w_n.sum(axis=1, keepdims=True), w_r, rtol=1e-14, atol=0)
+        if k == 7:  # every expert selected: the weights are the whole softmax row
+            np.testing.assert_allclose(w_n.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+            np.testing.assert_allclose(np.sort(w_n, axis=1), np.sort(g_n, axis=1), rtol=0, atol=0)
+
+
+def pin_aux_fraction_convention(orc):
+    """[sparse-moe] compute_load_balancing_loss: f sums to 1 and balanced routing gives 1;
+    the hand case's counts give f = counts / (T k)."""
+    case = _golden()["route_two_tokens"]
+    x = np.asarray(case["x"], np.float64)
+    w_g = np.vectorize(_log_entry)(np.asarray(case["w_g_log"], np.float64))
+    idx, _, probs = orc.topk_route(orc.router_logits(x, w_g), case["k"])
+    f, loss = orc.aux_stats_fraction(probs, idx, 2)
+    T, k = idx.shape
+    np.testing.assert_allclose(f, np.asarray(case["counts"], np.float64) / (T * k), rtol=0, atol=0)
+    assert abs(loss - float(Fraction(case["loss"])) / k) < 1e-15
+    # W_g = 0: the first k experts each take 1/k of the assignments, p = 1/E, loss = 1
+    for E, k in ((8, 2), (6, 6), (64, 4)):
+        s = orc.router_logits(np.ones((5, 3)), np.zeros((E, 3)))
+        idx, _, g = orc.topk_route(s, k)
+        f, loss = orc.aux_stats_fraction(g, idx, E)
+        np.testing.assert_allclose(f, [1.0 / k] * k + [0.0] * (E - k), rtol=0, atol=1e-16)
+        assert abs(loss - 1.0) < 1e-12
+    rng = np.random.default_rng(22)
+    s = rng.normal(0, 1.0, (50, 9))
+    idx, _, g = orc.topk_route(s, 3)
+    f, _ = orc.aux_stats_fraction(g, idx, 9)
+    assert abs(f.sum() - 1.0) < 1e-15
+
+
 def pin_bias_only(orc):
     """x = 0: the logits are the bias ([zh-moe] GatingNetwork adds b)."""
     b = np.array([1.5 * math.log(1.0 / (e + 1)) for e in range(6)])
@@ -363,20 +419,20 @@ def _mutant(**overrides):
     return ns
 
 
-def _no_renorm(s, k):
+def _no_renorm(s, k, renormalize=True):
     g = oracle.softmax(s, axis=1)
     idx = oracle.topk_select(s, k)
     return idx, np.take_along_axis(g, idx, axis=1), g
 
 
-def _smallest(s, k):
+def _smallest(s, k, renormalize=True):
     g = oracle.softmax(s, axis=1)
     idx = np.argsort(s, axis=1, kind="stable")[:, :k]
     sel = np.take_along_axis(g, idx, axis=1)
     return idx, sel / sel.sum(axis=1, keepdims=True), g
 
 
-def _ties_high(s, k):
+def _ties_high(s, k, renormalize=True):
     g = oracle.softmax(s, axis=1)
     idx = (s.shape[1] - 1 - np.argsort(-s[:, ::-1], axis=1, kind="stable"))[:, :k]
     sel = np.take_along_axis(g, idx, axis=1)
@@ -424,6 +480,15 @@ def _forward_unweighted(x, idx, w, experts, round_h=None):
     return oracle.moe_forward(x, idx, np.ones_like(w), experts, round_h)
 
 
+def _always_renormalise(s, k, renormalize=True):
+    return oracle.topk_route(s, k)
+
+
+def _fraction_over_T(g, idx, E):
+    counts, f, p, loss = oracle.aux_stats(g, idx, E)
+    return f, loss
+
+
 def _silu_sign(a):
     return a / (1.0 + np.exp(a))
 
@@ -445,6 +510,8 @@ MUTANTS = {
     "forward_ignores_weights": dict(moe_forward=_forward_unweighted),
     "silu_sign": dict(silu=_silu_sign),
     "bias_dropped": dict(router_logits=_no_bias),
+    "unrenormalised_flag_ignored": dict(topk_route=_always_renormalise),
+    "fraction_convention_over_T": dict(aux_stats_fraction=_fraction_over_T),
 }
 
 
