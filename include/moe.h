@@ -60,6 +60,14 @@ typedef enum { MOE_ROUTING_TOPK = 0, MOE_ROUTING_EXPERT_CHOICE = 1 } moe_routing
 /* Largest expert count any call accepts. */
 #define MOE_MAX_EXPERTS 256
 
+/* Routing flags (moe_route flags, moe_layer_desc.flags).
+ * MOE_ROUTE_NO_RENORM: the combine weights are the selected probabilities
+ * g[t,idx] as they are, the gate of the equations in [moe-intro] ("ゲート /
+ * ルーターって何者？", y = sum over TopK of g_i E_i(x)) and [sparse-moe] (top-k
+ * gating formula); without it they are renormalised to sum to 1, as the code
+ * on every page does. */
+#define MOE_ROUTE_NO_RENORM 1
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* moe_status_string(moe_status status);
 
@@ -77,7 +85,8 @@ moe_status moe_device_error(uint32_t* word, int clear);
  *   topk_idx[t,j], j < k: the k largest s[t,:], slot 0 largest, ties to the
  *             lower expert index (selection on the logits: the softmax is
  *             monotone in a row, so this is the same set)
- *   topk_w[t,j] = g[t,idx] / sum_{j'} g[t,idx_j']            (sums to 1)
+ *   topk_w[t,j] = g[t,idx] / sum_{j'} g[t,idx_j']            (sums to 1),
+ *             or g[t,idx] itself with flags & MOE_ROUTE_NO_RENORM
  * Arguments
  *   x [T,d] (dt), w_g [E,d] (dt), bias [E] fp32 or NULL
  *   topk_idx [T,k] int32, topk_w [T,k] fp32             (required outputs)
@@ -90,7 +99,7 @@ moe_status moe_device_error(uint32_t* word, int clear);
 size_t moe_route_aux_rows(int T);
 moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, int d, int E,
                      int k, moe_dtype dt, int32_t* topk_idx, float* topk_w, float* logits,
-                     float* probs, float* aux_partials, moe_stream_t stream);
+                     float* probs, float* aux_partials, int flags, moe_stream_t stream);
 
 /* -------------------------------------------------- expert-choice router
  * [sparse-moe] ExpertChoiceGating.forward:
@@ -212,12 +221,16 @@ moe_status moe_ec_combine(const float* y_perm, const int32_t* pos, const float* 
  * [moe-theory] MoELayer.load_balancing_loss:
  *   f[e] = counts[e] / T (sum f = k);  p[e] = mean_t g[t,e];
  *   loss = E * sum_e f[e] p[e]     (unweighted; balanced routing gives k)
+ * [sparse-moe] compute_load_balancing_loss convention (optional outputs):
+ *   f_frac[e] = counts[e] / (T k) (sum 1);  loss_frac = E * sum_e f_frac[e] p[e]
+ *   (= loss / k; balanced routing gives 1)
  * p comes from probs [T,E] when probs != NULL, else from aux_partials
  * ([moe_route_aux_rows(T), E], written by moe_route); one must be given.
+ * f, p, loss, f_frac, loss_frac: each may be NULL.
  * Fixed-order reductions: deterministic.                                    */
 moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int32_t* counts,
-                        int T, int E, int k, float* f, float* p, float* loss,
-                        moe_stream_t stream);
+                        int T, int E, int k, float* f, float* p, float* loss, float* f_frac,
+                        float* loss_frac, moe_stream_t stream);
 
 /* ---------------------------------------------------------- whole layer */
 typedef struct {
@@ -225,6 +238,7 @@ typedef struct {
   moe_routing routing;
   float capacity_factor;   /* expert choice only */
   moe_dtype dtype;         /* x and weights */
+  int flags;               /* routing flags (MOE_ROUTE_NO_RENORM), top-k only */
 } moe_layer_desc;
 
 typedef struct {
@@ -248,6 +262,8 @@ typedef struct {
   int32_t* ec_idx;         /* [E,C]  expert choice only */
   float* ec_score;         /* [E,C]  expert choice only */
   int32_t* pos;            /* [E,T]  expert choice only */
+  float* f_frac;           /* [E]    top-k only: counts / (T k) */
+  float* loss_frac;        /* [1]    top-k only: loss / k */
 } moe_layer_outputs;
 
 /* Bytes of scratch moe_layer_forward needs for `desc` (0 on invalid desc). */

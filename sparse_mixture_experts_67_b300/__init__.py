@@ -31,6 +31,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
 MOE_F32, MOE_BF16 = 0, 1
+MOE_ROUTE_NO_RENORM = 1
 MOE_ROUTING_TOPK, MOE_ROUTING_EXPERT_CHOICE = 0, 1
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
            4: "MOE_ERR_CUDA"}
@@ -45,7 +46,7 @@ class MoEError(RuntimeError):
 class _Desc(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("d", ctypes.c_int), ("F", ctypes.c_int), ("E", ctypes.c_int),
                 ("k", ctypes.c_int), ("routing", ctypes.c_int), ("capacity_factor", ctypes.c_float),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("flags", ctypes.c_int)]
 
 
 class _Weights(ctypes.Structure):
@@ -53,7 +54,7 @@ class _Weights(ctypes.Structure):
 
 
 _OUT_FIELDS = ("topk_idx", "topk_w", "logits", "counts", "offsets", "f", "p", "loss", "ec_idx",
-               "ec_score", "pos")
+               "ec_score", "pos", "f_frac", "loss_frac")
 
 
 class _Outputs(ctypes.Structure):
@@ -67,7 +68,7 @@ _SIGS = {
     "moe_status_string": ([_I], ctypes.c_char_p),
     "moe_device_error": ([ctypes.POINTER(ctypes.c_uint32), _I], _I),
     "moe_route_aux_rows": ([_I], _Z),
-    "moe_route": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "moe_route": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P], _I),
     "moe_expert_choice_capacity": ([_I, _I, _F], _I),
     "moe_expert_choice_route": ([_P, _P, _P, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _Z),
@@ -81,7 +82,7 @@ _SIGS = {
     "moe_experts_swiglu": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_ec_combine": ([_P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
-    "moe_aux_loss": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
+    "moe_aux_loss": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
     "moe_layer_workspace_size": ([ctypes.POINTER(_Desc)], _Z),
     "moe_layer_forward": ([ctypes.POINTER(_Desc), ctypes.POINTER(_Weights), _P, _P,
                            ctypes.POINTER(_Outputs), _P, _Z, _P], _I),
@@ -169,8 +170,9 @@ def moe_expert_choice_capacity(T: int, E: int, capacity_factor: float) -> int:
 
 def moe_route(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[torch.Tensor], k: int,
               want_logits: bool = False, want_probs: bool = False,
-              want_aux: bool = True) -> Dict[str, torch.Tensor]:
-    """Top-k router: returns topk_idx [T,k] int32, topk_w [T,k] fp32 and the optional outputs."""
+              want_aux: bool = True, renormalize: bool = True) -> Dict[str, torch.Tensor]:
+    """Top-k router: returns topk_idx [T,k] int32, topk_w [T,k] fp32 and the optional outputs.
+    renormalize=False keeps the selected probabilities as the weights (MOE_ROUTE_NO_RENORM)."""
     _dev(x, w_g, bias)
     T, d = x.shape
     E = w_g.shape[0]
@@ -184,7 +186,7 @@ def moe_route(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[torch.Tensor], 
     _check("moe_route", lib().moe_route(
         _ptr(x), _ptr(w_g), _ptr(bias), T, d, E, k, _dtype(x), _ptr(out["topk_idx"]),
         _ptr(out["topk_w"]), _ptr(out.get("logits")), _ptr(out.get("probs")),
-        _ptr(out.get("aux_partials")), _stream()))
+        _ptr(out.get("aux_partials")), 0 if renormalize else MOE_ROUTE_NO_RENORM, _stream()))
     return out
 
 
@@ -335,21 +337,24 @@ def moe_ec_combine(y_perm: torch.Tensor, pos: torch.Tensor, ec_score: torch.Tens
 
 def moe_aux_loss(counts: torch.Tensor, T: int, k: int, aux_partials: Optional[torch.Tensor] = None,
                  probs: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
-    """f [E], p [E], loss [1] from router partial sums (or from probs [T,E])."""
+    """f [E], p [E], loss [1] from router partial sums (or from probs [T,E]), and the
+    fraction-of-assignments convention f_frac [E] = counts / (T k), loss_frac [1] = loss / k."""
     _dev(counts, aux_partials, probs)
     E = counts.numel()
     if probs is not None and aux_partials is None:
         aux_partials = _empty((max(1, moe_route_aux_rows(T)), E), torch.float32, counts)
     out = {"f": _empty((E,), torch.float32, counts), "p": _empty((E,), torch.float32, counts),
-           "loss": _empty((1,), torch.float32, counts)}
+           "loss": _empty((1,), torch.float32, counts),
+           "f_frac": _empty((E,), torch.float32, counts),
+           "loss_frac": _empty((1,), torch.float32, counts)}
     _check("moe_aux_loss", lib().moe_aux_loss(
         _ptr(probs), _ptr(aux_partials), _ptr(counts), T, E, k, _ptr(out["f"]), _ptr(out["p"]),
-        _ptr(out["loss"]), _stream()))
+        _ptr(out["loss"]), _ptr(out["f_frac"]), _ptr(out["loss_frac"]), _stream()))
     return out
 
 
-def _desc(T, d, F, E, k, routing, capacity_factor, dtype) -> _Desc:
-    return _Desc(T, d, F, E, k, routing, capacity_factor, dtype)
+def _desc(T, d, F, E, k, routing, capacity_factor, dtype, flags=0) -> _Desc:
+    return _Desc(T, d, F, E, k, routing, capacity_factor, dtype, flags)
 
 
 def moe_layer_workspace_size(T: int, d: int, F: int, E: int, k: int, routing: int = 0,
@@ -362,14 +367,16 @@ def moe_layer_forward(x: torch.Tensor, weights: Dict[str, torch.Tensor], k: int 
                       routing: int = MOE_ROUTING_TOPK, capacity_factor: float = 0.0,
                       outputs: Optional[Dict[str, torch.Tensor]] = None,
                       workspace: Optional[torch.Tensor] = None,
-                      y: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Whole layer forward.  weights: w_g [E,d], bias [E] or None, w_gate/w_up [E,F,d], w_down [E,d,F]."""
+                      y: Optional[torch.Tensor] = None, renormalize: bool = True) -> torch.Tensor:
+    """Whole layer forward.  weights: w_g [E,d], bias [E] or None, w_gate/w_up [E,F,d], w_down [E,d,F].
+    renormalize=False: top-k combine weights are the selected probabilities (MOE_ROUTE_NO_RENORM)."""
     w_g, bias = weights["w_g"], weights.get("bias")
     w_gate, w_up, w_down = weights["w_gate"], weights["w_up"], weights["w_down"]
     _dev(x, w_g, bias, w_gate, w_up, w_down, y, workspace)
     T, d = x.shape
     E, F, _ = w_gate.shape
-    desc = _desc(T, d, F, E, k, routing, capacity_factor, _dtype(x))
+    desc = _desc(T, d, F, E, k, routing, capacity_factor, _dtype(x),
+                 0 if renormalize else MOE_ROUTE_NO_RENORM)
     need = int(lib().moe_layer_workspace_size(ctypes.byref(desc)))
     if workspace is None or workspace.numel() < need:
         workspace = _empty((max(need, 1),), torch.uint8, x)
@@ -391,9 +398,10 @@ class MoELayer:
     """Holds device weights and a workspace; calls moe_layer_forward."""
 
     def __init__(self, weights: Dict[str, torch.Tensor], k: int = 2, routing: int = MOE_ROUTING_TOPK,
-                 capacity_factor: float = 0.0):
+                 capacity_factor: float = 0.0, renormalize: bool = True):
         self.weights = weights
         self.k, self.routing, self.capacity_factor = k, routing, capacity_factor
+        self.renormalize = renormalize
         self._ws: Optional[torch.Tensor] = None
 
     def workspace(self, x: torch.Tensor) -> torch.Tensor:
@@ -406,7 +414,8 @@ class MoELayer:
 
     def __call__(self, x: torch.Tensor, outputs=None, y=None) -> torch.Tensor:
         return moe_layer_forward(x, self.weights, self.k, self.routing, self.capacity_factor,
-                                 outputs=outputs, workspace=self.workspace(x), y=y)
+                                 outputs=outputs, workspace=self.workspace(x), y=y,
+                                 renormalize=self.renormalize)
 
 
 class HostPipeline:

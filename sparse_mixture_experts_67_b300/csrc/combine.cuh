@@ -8,7 +8,9 @@
 // ascending expert order, weighted by the raw dispatch-mask score.
 //
 // Aux: f_e = count_e / T, p_e = mean_t g[t,e], loss = E * sum_e f_e p_e, the
-// load_balancing_loss of the first page.  p is reduced from per-block partial
+// load_balancing_loss of the first page; optionally also the convention of
+// compute_load_balancing_loss in the second: f_frac_e = count_e / (T k),
+// loss_frac = loss / k.  p is reduced from per-block partial
 // sums in a fixed order, so the result does not depend on scheduling.
 #pragma once
 
@@ -137,8 +139,9 @@ __global__ void probs_partials_kernel(const float* __restrict__ probs, int T, in
 constexpr int kAuxThreads = 256;
 __global__ void __launch_bounds__(kAuxThreads)
     aux_finalize_kernel(const float* __restrict__ partials, int rows, const int32_t* __restrict__ counts,
-                        int T, int E, float* __restrict__ f, float* __restrict__ p,
-                        float* __restrict__ loss) {
+                        int T, int E, int k, float* __restrict__ f, float* __restrict__ p,
+                        float* __restrict__ loss, float* __restrict__ f_frac,
+                        float* __restrict__ loss_frac) {
   pdl_begin();
   __shared__ float s[MOE_MAX_EXPERTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(kAuxThreads)
       const float fe = (float)counts[e] / (float)T;
       if (p) p[e] = pe;
       if (f) f[e] = fe;
+      if (f_frac) f_frac[e] = (float)counts[e] / ((float)T * (float)k);
       s[e] = fe * pe;
     }
   }
@@ -164,6 +168,7 @@ __global__ void __launch_bounds__(kAuxThreads)
     __syncthreads();
   }
   if (threadIdx.x == 0 && loss) *loss = (float)E * s[0];
+  if (threadIdx.x == 0 && loss_frac) *loss_frac = (float)E * s[0] / (float)k;
 }
 
 }  // namespace moe

@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
                             const uint4* __restrict__ x, int vec_per_row, uint4* __restrict__ x_perm,
                             const float* __restrict__ aux_partials, int T, float* __restrict__ f,
                             float* __restrict__ p, float* __restrict__ loss,
+                            float* __restrict__ f_frac, float* __restrict__ loss_frac,
                             float4* __restrict__ y_zero, int d4, int tokens_per_tile) {
   pdl_begin();
   __shared__ int running[MOE_MAX_EXPERTS];
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
       const float fe = (float)s_tot[e] / (float)T;
       if (p) p[e] = pe;
       if (f) f[e] = fe;
+      if (f_frac) f_frac[e] = (float)s_tot[e] / ((float)T * (float)k);
       s_fp[e] = fe * pe;
     }
   }
@@ -264,6 +266,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
     __syncthreads();
   }
   if (threadIdx.x == 0 && loss) *loss = (float)E * s_fp[0];
+  if (threadIdx.x == 0 && loss_frac) *loss_frac = (float)E * s_fp[0] / (float)k;
 }
 
 // x_perm[r,:] = x[src[r] / div, :]; one warp per row, 16-byte vectors.

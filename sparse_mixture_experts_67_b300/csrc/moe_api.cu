@@ -80,15 +80,17 @@ size_t moe_route_aux_rows(int T) { return T <= 0 ? 0 : (size_t)ceil_div(T, kRout
 
 moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, int d, int E, int k,
                      moe_dtype dt, int32_t* topk_idx, float* topk_w, float* logits, float* probs,
-                     float* aux_partials, moe_stream_t stream) {
+                     float* aux_partials, int flags, moe_stream_t stream) {
   if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (flags & ~MOE_ROUTE_NO_RENORM) return MOE_ERR_INVALID_ARG;
   moe_status st = check_dims(d, dt);
   if (st != MOE_OK) return st;
   if (T == 0) return MOE_OK;
   if (!x || !w_g || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   if (dt == MOE_BF16 && (!aligned16(x) || !aligned16(w_g))) return MOE_ERR_UNSUPPORTED;
   return cuda_status(launch_router(x, w_g, bias, T, d, E, k, dt == MOE_BF16, topk_idx, topk_w,
-                                   logits, probs, aux_partials, (cudaStream_t)stream));
+                                   logits, probs, aux_partials, (cudaStream_t)stream, nullptr,
+                                   nullptr, flags));
 }
 
 int moe_expert_choice_capacity(int T, int E, float capacity_factor) {
@@ -154,7 +156,8 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
                                   int32_t* tile_base, int tile, bool counts_ready, cudaStream_t s,
                                   const float* aux_partials = nullptr, float* f = nullptr,
                                   float* p = nullptr, float* loss = nullptr,
-                                  float* y_zero = nullptr) {
+                                  float* y_zero = nullptr, float* f_frac = nullptr,
+                                  float* loss_frac = nullptr) {
   const long long A = (long long)T * k;
   const int tiles = dispatch_tiles(A, tile);
   cudaError_t e = cudaSuccess;
@@ -168,7 +171,7 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
                  tiles, E, (int)A, tile_base, counts, offsets);
     if (e == cudaSuccess && aux_partials)
       e = launch_k(aux_finalize_kernel, dim3(1), dim3(kAuxThreads), 0, s, nullptr, 0, aux_partials,
-                   tiles, counts, T, E, f, p, loss);
+                   tiles, counts, T, E, k, f, p, loss, f_frac, loss_frac);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   const int32_t* base = separate_scan ? tile_base : nullptr;
@@ -176,7 +179,8 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
       dispatch_scatter_kernel, dim3(tiles), dim3(kDispatchThreads), 0, s, nullptr, 0, topk_idx,
       (int)A, E, k, tile, tile_counts, base, tiles, perm, inv_perm, counts, offsets,
       static_cast<const uint4*>(x), (int)(d * elt_size(dt) / 16), static_cast<uint4*>(x_perm),
-      aux_partials, T, f, p, loss, reinterpret_cast<float4*>(y_zero), d / 4, tile / k));
+      aux_partials, T, f, p, loss, f_frac, loss_frac, reinterpret_cast<float4*>(y_zero), d / 4,
+      tile / k));
 }
 
 static moe_status check_permute(const void* x, const void* x_perm, int T, int d, int E, int k,
@@ -312,7 +316,8 @@ moe_status moe_ec_combine(const float* y_perm, const int32_t* pos, const float* 
 }
 
 moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int32_t* counts, int T,
-                        int E, int k, float* f, float* p, float* loss, moe_stream_t stream) {
+                        int E, int k, float* f, float* p, float* loss, float* f_frac,
+                        float* loss_frac, moe_stream_t stream) {
   if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!counts || (!probs && !aux_partials)) return MOE_ERR_INVALID_ARG;
@@ -327,7 +332,7 @@ moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return cuda_status(launch_k(aux_finalize_kernel, dim3(1), dim3(kAuxThreads), 0, s, nullptr, 0,
-                              aux_partials, rows, counts, T, E, f, p, loss));
+                              aux_partials, rows, counts, T, E, k, f, p, loss, f_frac, loss_frac));
 }
 
 size_t moe_layer_workspace_size(const moe_layer_desc* desc) {
@@ -377,6 +382,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   if (D.routing != MOE_ROUTING_TOPK && !ec) return MOE_ERR_INVALID_ARG;
   if (D.T < 0 || D.E < 1 || D.E > MOE_MAX_EXPERTS || D.F <= 0) return MOE_ERR_INVALID_ARG;
   if (!ec && (D.k < 1 || D.k > D.E)) return MOE_ERR_INVALID_ARG;
+  if (D.flags & ~MOE_ROUTE_NO_RENORM) return MOE_ERR_INVALID_ARG;
   if (ec && !(D.capacity_factor > 0.f)) return MOE_ERR_INVALID_ARG;
   moe_status st = check_experts(0, D.d, D.F, D.E, D.dtype);
   if (st != MOE_OK) return st;
@@ -453,7 +459,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   int32_t* tile_base = reinterpret_cast<int32_t*>(static_cast<char*>(pw) +
                                                   align256((size_t)tiles * D.E * sizeof(int32_t)));
   if (launch_router(x, w->w_g, w->bias, D.T, D.d, D.E, k, D.dtype == MOE_BF16, idx, tw, O.logits,
-                    nullptr, aux, s, tile_counts) != cudaSuccess)
+                    nullptr, aux, s, tile_counts, nullptr, D.flags) != cudaSuccess)
     return MOE_ERR_CUDA;
   // k <= 2 (bf16): the down GEMM accumulates the combine into y, zeroed by the scatter
   const bool fused_combine = D.dtype == MOE_BF16 && k <= 2;
@@ -464,7 +470,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   st = dispatch_launch(x, idx, D.T, D.d, D.E, k, D.dtype, x_perm, counts, offsets, perm, inv_perm,
                        tile_counts, tile_base, tile, true, s, aux, O.f ? O.f : fpl,
                        O.p ? O.p : fpl + D.E, O.loss ? O.loss : fpl + 2 * D.E,
-                       fused_combine ? y : nullptr);
+                       fused_combine ? y : nullptr, O.f_frac, O.loss_frac);
   if (st != MOE_OK) return st;
   if (fused_combine) {
     // down projection with the combine in its epilogue (deterministic for k <= 2)

@@ -64,6 +64,7 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, cons
 // MOE_MAX_EXPERTS ints; s_part max(blockDim.x, E) floats.
 // logitsT_out (nullable): the logits once more, transposed to [E, T] (row e is
 // what the expert-choice selection of expert e reads).
+// flags & MOE_ROUTE_NO_RENORM: the weights stay the selected probabilities.
 template <int TOK, int SUB = TOK, int P = 1>
 __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k,
                                 const float* __restrict__ bias, int32_t* __restrict__ idx_out,
@@ -71,7 +72,7 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
                                 float* __restrict__ probs_out, float* __restrict__ aux_rows,
                                 int32_t* __restrict__ tile_counts, int tile0, float* s_m,
                                 float* s_inv, int* s_cnt, float* s_part,
-                                float* __restrict__ logitsT_out = nullptr) {
+                                float* __restrict__ logitsT_out = nullptr, int flags = 0) {
   static_assert(TOK % SUB == 0, "dispatch tiles split the CTA's tokens");
   static_assert(P >= 1 && P <= 32 && (P & (P - 1)) == 0, "threads per token: a power of two");
   constexpr int NSUB = TOK / SUB;
@@ -185,7 +186,7 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
         if (tile_counts) atomicAdd(&s_cnt[(r / SUB) * MOE_MAX_EXPERTS + bi], 1);
       }
     }
-    if (live && q == 0) {
+    if (live && q == 0 && !(flags & MOE_ROUTE_NO_RENORM)) {
       const float rs = 1.0f / selsum;
       for (int j = 0; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
     }
@@ -246,7 +247,7 @@ __global__ void __launch_bounds__(kRouterThreadsBf16)
                        int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                        float* __restrict__ logits_out, float* __restrict__ probs_out,
                        float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts,
-                       float* __restrict__ logitsT) {
+                       float* __restrict__ logitsT, int flags) {
   pdl_begin();
   using C = RouterBf16<NT, TOK>;
   constexpr int EP = C::EP, LD = C::LD, SBK = C::SBK, STAGES = C::STAGES;
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kRouterThreadsBf16)
   router_epilogue<TOK, TOK, C::P>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
                        blockIdx.x,
-                       s_m, s_inv, s_cnt, s_part, logitsT);
+                       s_m, s_inv, s_cnt, s_part, logitsT, flags);
 }
 
 // fp32 router: FFMA over 32-wide d chunks, same epilogue.
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(2 * TOK)
                       int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                       float* __restrict__ logits_out, float* __restrict__ probs_out,
                       float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts,
-                      float* __restrict__ logitsT) {
+                      float* __restrict__ logitsT, int flags) {
   pdl_begin();
   constexpr int EP = 8 * NT;
   constexpr int ld = kRouterBKf + 1;
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(2 * TOK)
   router_epilogue<TOK, TOK, kPf>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
                        blockIdx.x,
-                       s_m, s_inv, s_cnt, s_part, logitsT);
+                       s_m, s_inv, s_cnt, s_part, logitsT, flags);
 }
 
 inline int router_nt(int E) {
@@ -433,7 +434,8 @@ inline int router_nt(int E) {
 template <int NT, int TOK>
 cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, int T, int d, int E,
                              int k, bool bf16, int32_t* idx, float* w, float* logits, float* probs,
-                             float* aux, int32_t* tile_counts, float* logitsT, cudaStream_t st) {
+                             float* aux, int32_t* tile_counts, float* logitsT, int flags,
+                             cudaStream_t st) {
   const int grid = ceil_div(T, TOK);
   if (bf16) {
     const size_t sm = router_smem_bytes_bf16<NT, TOK>();
@@ -443,7 +445,7 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     return launch_k(router_bf16_kernel<NT, TOK>, dim3(grid), dim3(kRouterThreadsBf16), sm, st,
                     nullptr, 0, static_cast<const __nv_bfloat16*>(x),
                     static_cast<const __nv_bfloat16*>(wg), bias, T, d, E, k, idx, w, logits, probs,
-                    aux, tile_counts, logitsT);
+                    aux, tile_counts, logitsT, flags);
   } else {
     const size_t sm = router_smem_bytes_f32<NT, TOK>();
     cudaError_t e = cudaFuncSetAttribute(router_f32_kernel<NT, TOK>,
@@ -451,21 +453,22 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     if (e != cudaSuccess) return e;
     return launch_k(router_f32_kernel<NT, TOK>, dim3(grid), dim3(2 * TOK), sm, st, nullptr, 0,
                     static_cast<const float*>(x), static_cast<const float*>(wg), bias, T, d, E, k,
-                    idx, w, logits, probs, aux, tile_counts, logitsT);
+                    idx, w, logits, probs, aux, tile_counts, logitsT, flags);
   }
 }
 
 inline cudaError_t launch_router_mma(const void* x, const void* wg, const float* bias, int T, int d,
                                  int E, int k, bool bf16, int32_t* idx, float* w, float* logits,
                                  float* probs, float* aux, cudaStream_t st,
-                                 int32_t* tile_counts = nullptr, float* logitsT = nullptr) {
+                                 int32_t* tile_counts = nullptr, float* logitsT = nullptr,
+                                 int flags = 0) {
 #define MOE_ROUTER_CASE(NT_)                                                                     \
   case NT_:                                                                                      \
     return router_tokens(E) == 32                                                                \
                ? launch_router_nt<NT_, 32>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, \
-                                           aux, tile_counts, logitsT, st)                                 \
+                                           aux, tile_counts, logitsT, flags, st)                                 \
                : launch_router_nt<NT_, 64>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, \
-                                           aux, tile_counts, logitsT, st);
+                                           aux, tile_counts, logitsT, flags, st);
   switch (router_nt(E)) {
     MOE_ROUTER_CASE(1)
     MOE_ROUTER_CASE(2)
@@ -474,7 +477,7 @@ inline cudaError_t launch_router_mma(const void* x, const void* wg, const float*
     MOE_ROUTER_CASE(16)
     default:
       return launch_router_nt<32, 64>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux,
-                                      tile_counts, logitsT, st);
+                                      tile_counts, logitsT, flags, st);
   }
 #undef MOE_ROUTER_CASE
 }

@@ -91,9 +91,19 @@ def test_router_parity(moe, torch, case, router, monkeypatch):
     np.testing.assert_allclose(_np(aux["f"]), f_ref, rtol=1e-7, atol=0)
     np.testing.assert_allclose(_np(aux["p"]), p_ref, rtol=0, atol=2e-6)
     assert abs(float(_np(aux["loss"])[0]) - loss_ref) <= 1e-5 * max(1.0, loss_ref)
+    f_frac_ref, loss_frac_ref = oracle.aux_stats_fraction(g_ref, idx_ref, E)
+    np.testing.assert_allclose(_np(aux["f_frac"]), f_frac_ref, rtol=1e-7, atol=0)
+    assert abs(float(_np(aux["loss_frac"])[0]) - loss_frac_ref) <= 1e-5 * max(1.0, loss_frac_ref)
     aux2 = moe.moe_aux_loss(counts, T, k, probs=out["probs"])
     torch.cuda.synchronize()
     np.testing.assert_allclose(_np(aux2["p"]), p_ref, rtol=0, atol=2e-6)
+    # without renormalisation: same selection, the selected probabilities as weights
+    out_n = moe.moe_route(to_dev(x), to_dev(w_g), None if b is None else to_dev(b), k,
+                          want_logits=True, renormalize=False)
+    torch.cuda.synchronize()
+    idx_n, w_n, _ = oracle.topk_route(_np(out_n["logits"]).astype(np.float64), k, renormalize=False)
+    np.testing.assert_array_equal(_np(out_n["topk_idx"]), idx_n)
+    np.testing.assert_allclose(_np(out_n["topk_w"]), w_n, rtol=0, atol=2e-6)
 
 
 PERMUTE_CASES = [
@@ -177,7 +187,7 @@ def test_grouped_experts_parity(moe, torch, case, tile_n, monkeypatch):
     assert_close_output(_np(y_perm), y_ref, dt, f"y_perm[{name}]", ref_bf16_h=y_ref_h if dt == "bf16" else None)
 
 
-def _run_layer(moe, torch, inp, outputs_spec):
+def _run_layer(moe, torch, inp, outputs_spec, renormalize=True):
     cfg = inp.cfg
     w = dev_weights(inp)
     x = to_dev(inp.x)
@@ -187,7 +197,7 @@ def _run_layer(moe, torch, inp, outputs_spec):
     if cfg.routing == "expert_choice":
         y = moe.moe_layer_forward(x, w, k=0, routing=1, capacity_factor=cfg.capacity_factor, outputs=outs)
     else:
-        y = moe.moe_layer_forward(x, w, k=cfg.k, outputs=outs)
+        y = moe.moe_layer_forward(x, w, k=cfg.k, outputs=outs, renormalize=renormalize)
     torch.cuda.synchronize()
     return y, outs
 
@@ -197,16 +207,17 @@ def _topk_outputs(torch, cfg):
     return {"topk_idx": ((T, k), torch.int32), "topk_w": ((T, k), torch.float32),
             "logits": ((T, E), torch.float32), "counts": ((E,), torch.int32),
             "offsets": ((E + 1,), torch.int32), "f": ((E,), torch.float32),
-            "p": ((E,), torch.float32), "loss": ((1,), torch.float32)}
+            "p": ((E,), torch.float32), "loss": ((1,), torch.float32),
+            "f_frac": ((E,), torch.float32), "loss_frac": ((1,), torch.float32)}
 
 
-def _check_topk_layer(moe, torch, cfg, sample=None):
+def _check_topk_layer(moe, torch, cfg, sample=None, renormalize=True):
     inp = cached_inputs(cfg)
-    y, outs = _run_layer(moe, torch, inp, _topk_outputs(torch, cfg))
+    y, outs = _run_layer(moe, torch, inp, _topk_outputs(torch, cfg), renormalize=renormalize)
     x64 = synth.to_f64(inp.x)
     s_gpu = _np(outs["logits"]).astype(np.float64)
     # routing, dispatch and aux: full size, same-precision decisions
-    idx_g, w_g, g_g = oracle.topk_route(s_gpu, cfg.k)
+    idx_g, w_g, g_g = oracle.topk_route(s_gpu, cfg.k, renormalize=renormalize)
     np.testing.assert_array_equal(_np(outs["topk_idx"]), idx_g)
     np.testing.assert_allclose(_np(outs["topk_w"]), w_g, rtol=0, atol=2e-6)
     counts, offsets, _, _ = oracle.dispatch(idx_g, cfg.E)
@@ -216,9 +227,12 @@ def _check_topk_layer(moe, torch, cfg, sample=None):
     np.testing.assert_allclose(_np(outs["f"]), f_ref, rtol=1e-6, atol=0)
     np.testing.assert_allclose(_np(outs["p"]), p_ref, rtol=0, atol=1e-5)
     assert abs(float(_np(outs["loss"])[0]) - loss_ref) <= 1e-4 * max(1.0, loss_ref)
+    f_frac_ref, loss_frac_ref = oracle.aux_stats_fraction(g_g, idx_g, cfg.E)
+    np.testing.assert_allclose(_np(outs["f_frac"]), f_frac_ref, rtol=1e-6, atol=0)
+    assert abs(float(_np(outs["loss_frac"])[0]) - loss_frac_ref) <= 1e-4 * max(1.0, loss_frac_ref)
     # end-to-end routing against fp64 logits
     s64 = oracle.router_logits(x64, synth.to_f64(inp.w_g), inp.bias)
-    idx64, w64, g64 = oracle.topk_route(s64, cfg.k)
+    idx64, w64, g64 = oracle.topk_route(s64, cfg.k, renormalize=renormalize)
     agree = check_routing_agreement(_np(outs["topk_idx"]), idx64, g64)
     # outputs (sampled at full size) against the fp64 oracle with its own routing
     tokens = np.arange(cfg.T) if sample is None else np.sort(
@@ -248,6 +262,15 @@ def test_layer_small_bf16_multi_tile(moe, torch, E, k, router, monkeypatch):
     cfg = synth.small_config(f"small_bf16_e{E}", 1000, 256, 384, E, k, "bf16", seed=21 + E,
                              x_std=1.0, w_std=0.02, wg_std=0.1)
     _check_topk_layer(moe, torch, cfg)
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (16, 4), (40, 1)])
+def test_layer_without_renormalisation(moe, torch, E, k):
+    """MOE_ROUTE_NO_RENORM: the combine weights are the selected probabilities themselves
+    (fused down+combine for k <= 2, the separate combine above; both routers)."""
+    cfg = synth.small_config(f"norenorm_e{E}", 900, 256, 384, E, k, "bf16", seed=40 + E, x_std=1.0,
+                             w_std=0.02, wg_std=0.1)
+    _check_topk_layer(moe, torch, cfg, renormalize=False)
 
 
 @pytest.mark.slow
