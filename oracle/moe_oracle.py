@@ -25,7 +25,9 @@ Readings of points the pages leave open (each also listed in the design notes):
   * expert choice selects per expert on the logit column (same order as the
     softmax over tokens), ties to the lower token index, output in descending
     score order; the combine weight is the raw score (no renormalisation);
-  * dispatch order inside an expert segment is ascending assignment id t*k+j.
+  * dispatch order inside an expert segment is ascending assignment id t*k+j;
+  * capacity-limited token choice keeps, per expert, its first `capacity`
+    assignments in token order (the greedy loop of [zh-moe]).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 closed forms, invariants, brute force and library special cases.
@@ -193,6 +195,44 @@ def dense_mixture(x: Array, g: Array, experts: Sequence) -> Array:
     for e in range(len(experts)):
         y += g[:, e:e + 1] * swiglu_expert(x, *experts[e])
     return y
+
+
+def token_capacity(T: int, E: int, capacity_factor: float, k: int) -> int:
+    """Assignments one expert may take: int((T / E) * capacity_factor * k).
+    [zh-moe] expert_capacity_routing (capacity = tokens per expert x factor x top_k)."""
+    return int(math.floor((T / E) * capacity_factor * k))
+
+
+def capacity_route(s: Array, k: int, capacity_factor: float):
+    """Token choice with a per-expert capacity, [zh-moe] expert_capacity_routing:
+    tokens in ascending order take their top-k experts while the expert still has
+    room (its load below the capacity), the others are dropped; the kept
+    probabilities of a token are renormalised over its kept slots (a token with
+    none kept gets zero weights).
+
+    The k experts of one token are distinct, so the order of its slots does not
+    change which assignments are kept; the selection itself is topk_route's.
+    Returns (idx [T,k], w [T,k] with 0 on dropped slots, kept [T,k] bool,
+    dropped count, load [E], capacity).
+    """
+    T, E = s.shape
+    cap = token_capacity(T, E, capacity_factor, k)
+    idx, _, g = topk_route(s, k)
+    load = np.zeros(E, np.int64)
+    kept = np.zeros(idx.shape, bool)
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            if load[e] < cap:
+                kept[t, j] = True
+                load[e] += 1
+    w = np.zeros(idx.shape, np.float64)
+    for t in range(T):
+        sel = np.where(kept[t], g[t, idx[t]], 0.0)
+        total = np.sum(sel)
+        if total > 0:
+            w[t] = sel / total
+    return idx, w, kept, int(np.sum(~kept)), load, cap
 
 
 def expert_choice_capacity(T: int, E: int, capacity_factor: float) -> int:

@@ -203,6 +203,49 @@ def pin_aux_fraction_convention(orc):
     assert abs(f.sum() - 1.0) < 1e-15
 
 
+def pin_capacity_route(orc):
+    """[zh-moe] expert_capacity_routing: the hand case, then on random logits the greedy
+    rule in closed form (each expert keeps its first `capacity` tokens in order), the
+    drop count, per-token renormalisation of the kept weights, and no drops at all
+    when the capacity covers every assignment."""
+    case = _golden()["capacity_three_tokens_top2"]
+    x = np.asarray(case["x"], np.float64)
+    w_g = np.vectorize(_log_entry)(np.asarray(case["w_g_log"], np.float64))
+    s = orc.router_logits(x, w_g)
+    idx, w, kept, dropped, load, cap = orc.capacity_route(s, case["k"], case["capacity_factor"])
+    assert cap == case["capacity"] and dropped == case["dropped"]
+    assert idx.tolist() == case["idx"] and kept.tolist() == case["kept"]
+    assert load.tolist() == case["load"]
+    np.testing.assert_allclose(w, _frac(case["w"]), rtol=0, atol=1e-15)
+    rng = np.random.default_rng(23)
+    T, E = 60, 6
+    s = rng.normal(0, 1.5, (T, E))
+    s[:, 2] += 2.0  # one popular expert, so its capacity binds
+    for k, cf in ((1, 1.0), (2, 0.7), (3, 1.25)):
+        idx, w, kept, dropped, load, cap = orc.capacity_route(s, k, cf)
+        assert cap == int(math.floor(T / E * cf * k))
+        idx_r, w_r, _ = orc.topk_route(s, k)
+        np.testing.assert_array_equal(idx, idx_r)
+        counts = np.bincount(idx.ravel(), minlength=E)
+        np.testing.assert_array_equal(load, np.minimum(counts, cap))
+        assert dropped == int(np.sum(np.maximum(counts - cap, 0)))
+        for e in range(E):
+            tok = [t for t in range(T) for j in range(k) if idx[t, j] == e]  # ascending t
+            kept_tok = [t for t in range(T) for j in range(k) if idx[t, j] == e and kept[t, j]]
+            assert kept_tok == tok[:cap]
+        for t in range(T):
+            if kept[t].any():
+                assert abs(w[t].sum() - 1.0) < 1e-15
+                np.testing.assert_array_equal(w[t][~kept[t]], 0.0)
+                ratio = w[t][kept[t]] / w_r[t][kept[t]]
+                np.testing.assert_allclose(ratio, ratio[0], rtol=1e-14)
+            else:
+                np.testing.assert_array_equal(w[t], 0.0)
+    idx, w, kept, dropped, load, cap = orc.capacity_route(s, 2, float(E))  # capacity 2T
+    assert dropped == 0 and kept.all()
+    np.testing.assert_allclose(w, orc.topk_route(s, 2)[1], rtol=0, atol=0)
+
+
 def pin_bias_only(orc):
     """x = 0: the logits are the bias ([zh-moe] GatingNetwork adds b)."""
     b = np.array([1.5 * math.log(1.0 / (e + 1)) for e in range(6)])
@@ -489,6 +532,39 @@ def _fraction_over_T(g, idx, E):
     return f, loss
 
 
+def _capacity_without_k(s, k, cf):
+    T, E = s.shape
+    cap = int(math.floor(T / E * cf))
+    return _greedy(s, k, cap, order=range(T))
+
+
+def _greedy(s, k, cap, order, renorm=True):
+    T, E = s.shape
+    idx, _, g = oracle.topk_route(s, k)
+    load = np.zeros(E, np.int64)
+    kept = np.zeros(idx.shape, bool)
+    for t in order:
+        for j in range(k):
+            if load[idx[t, j]] < cap:
+                kept[t, j] = True
+                load[idx[t, j]] += 1
+    w = np.where(kept, np.take_along_axis(g, idx, axis=1), 0.0)
+    if renorm:
+        tot = w.sum(axis=1, keepdims=True)
+        w = np.divide(w, tot, out=np.zeros_like(w), where=tot > 0)
+    return idx, w, kept, int(np.sum(~kept)), load, cap
+
+
+def _capacity_last_tokens_first(s, k, cf):
+    T, E = s.shape
+    return _greedy(s, k, oracle.token_capacity(T, E, cf, k), order=range(T - 1, -1, -1))
+
+
+def _capacity_no_renorm(s, k, cf):
+    T, E = s.shape
+    return _greedy(s, k, oracle.token_capacity(T, E, cf, k), order=range(T), renorm=False)
+
+
 def _silu_sign(a):
     return a / (1.0 + np.exp(a))
 
@@ -512,6 +588,9 @@ MUTANTS = {
     "bias_dropped": dict(router_logits=_no_bias),
     "unrenormalised_flag_ignored": dict(topk_route=_always_renormalise),
     "fraction_convention_over_T": dict(aux_stats_fraction=_fraction_over_T),
+    "capacity_without_k": dict(capacity_route=_capacity_without_k),
+    "capacity_last_tokens_first": dict(capacity_route=_capacity_last_tokens_first),
+    "capacity_kept_not_renormalised": dict(capacity_route=_capacity_no_renorm),
 }
 
 
