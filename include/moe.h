@@ -67,6 +67,15 @@ typedef enum { MOE_ROUTING_TOPK = 0, MOE_ROUTING_EXPERT_CHOICE = 1 } moe_routing
  * gating formula); without it they are renormalised to sum to 1, as the code
  * on every page does. */
 #define MOE_ROUTE_NO_RENORM 1
+/* MOE_ROUTE_CAPACITY (moe_layer_desc.flags, top-k): capacity-limited token
+ * choice of [zh-moe] expert_capacity_routing.  Each expert takes at most
+ * capacity = int(T / E * capacity_factor * k) assignments (computed in double,
+ * in this order), the first ones in token order; the others are dropped (no
+ * dispatch row, inv_perm -1) and each token's kept weights are renormalised
+ * over its kept slots (all 0 when none is kept).  Needs capacity_factor > 0;
+ * not combinable with MOE_ROUTE_NO_RENORM.  counts, f and p describe the
+ * routing before the drops; offsets the kept segments. */
+#define MOE_ROUTE_CAPACITY 2
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* moe_status_string(moe_status status);
@@ -236,9 +245,9 @@ moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int
 typedef struct {
   int T, d, F, E, k;       /* k ignored for expert choice */
   moe_routing routing;
-  float capacity_factor;   /* expert choice only */
+  float capacity_factor;   /* expert choice; top-k with MOE_ROUTE_CAPACITY */
   moe_dtype dtype;         /* x and weights */
-  int flags;               /* routing flags (MOE_ROUTE_NO_RENORM), top-k only */
+  int flags;               /* routing flags (MOE_ROUTE_NO_RENORM, MOE_ROUTE_CAPACITY), top-k */
 } moe_layer_desc;
 
 typedef struct {
@@ -264,6 +273,7 @@ typedef struct {
   int32_t* pos;            /* [E,T]  expert choice only */
   float* f_frac;           /* [E]    top-k only: counts / (T k) */
   float* loss_frac;        /* [1]    top-k only: loss / k */
+  int32_t* dropped;        /* [1]    top-k with MOE_ROUTE_CAPACITY: dropped assignments */
 } moe_layer_outputs;
 
 /* Bytes of scratch moe_layer_forward needs for `desc` (0 on invalid desc). */

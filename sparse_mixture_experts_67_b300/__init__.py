@@ -31,7 +31,7 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
 MOE_F32, MOE_BF16 = 0, 1
-MOE_ROUTE_NO_RENORM = 1
+MOE_ROUTE_NO_RENORM, MOE_ROUTE_CAPACITY = 1, 2
 MOE_ROUTING_TOPK, MOE_ROUTING_EXPERT_CHOICE = 0, 1
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
            4: "MOE_ERR_CUDA"}
@@ -54,7 +54,7 @@ class _Weights(ctypes.Structure):
 
 
 _OUT_FIELDS = ("topk_idx", "topk_w", "logits", "counts", "offsets", "f", "p", "loss", "ec_idx",
-               "ec_score", "pos", "f_frac", "loss_frac")
+               "ec_score", "pos", "f_frac", "loss_frac", "dropped")
 
 
 class _Outputs(ctypes.Structure):
@@ -367,16 +367,19 @@ def moe_layer_forward(x: torch.Tensor, weights: Dict[str, torch.Tensor], k: int 
                       routing: int = MOE_ROUTING_TOPK, capacity_factor: float = 0.0,
                       outputs: Optional[Dict[str, torch.Tensor]] = None,
                       workspace: Optional[torch.Tensor] = None,
-                      y: Optional[torch.Tensor] = None, renormalize: bool = True) -> torch.Tensor:
+                      y: Optional[torch.Tensor] = None, renormalize: bool = True,
+                      capacity: bool = False) -> torch.Tensor:
     """Whole layer forward.  weights: w_g [E,d], bias [E] or None, w_gate/w_up [E,F,d], w_down [E,d,F].
-    renormalize=False: top-k combine weights are the selected probabilities (MOE_ROUTE_NO_RENORM)."""
+    renormalize=False: top-k combine weights are the selected probabilities (MOE_ROUTE_NO_RENORM).
+    capacity=True: top-k with at most int(T / E * capacity_factor * k) assignments per expert
+    (MOE_ROUTE_CAPACITY); outputs["dropped"] ([1] int32) receives the number dropped."""
     w_g, bias = weights["w_g"], weights.get("bias")
     w_gate, w_up, w_down = weights["w_gate"], weights["w_up"], weights["w_down"]
     _dev(x, w_g, bias, w_gate, w_up, w_down, y, workspace)
     T, d = x.shape
     E, F, _ = w_gate.shape
-    desc = _desc(T, d, F, E, k, routing, capacity_factor, _dtype(x),
-                 0 if renormalize else MOE_ROUTE_NO_RENORM)
+    flags = (0 if renormalize else MOE_ROUTE_NO_RENORM) | (MOE_ROUTE_CAPACITY if capacity else 0)
+    desc = _desc(T, d, F, E, k, routing, capacity_factor, _dtype(x), flags)
     need = int(lib().moe_layer_workspace_size(ctypes.byref(desc)))
     if workspace is None or workspace.numel() < need:
         workspace = _empty((max(need, 1),), torch.uint8, x)
@@ -398,10 +401,10 @@ class MoELayer:
     """Holds device weights and a workspace; calls moe_layer_forward."""
 
     def __init__(self, weights: Dict[str, torch.Tensor], k: int = 2, routing: int = MOE_ROUTING_TOPK,
-                 capacity_factor: float = 0.0, renormalize: bool = True):
+                 capacity_factor: float = 0.0, renormalize: bool = True, capacity: bool = False):
         self.weights = weights
         self.k, self.routing, self.capacity_factor = k, routing, capacity_factor
-        self.renormalize = renormalize
+        self.renormalize, self.capacity = renormalize, capacity
         self._ws: Optional[torch.Tensor] = None
 
     def workspace(self, x: torch.Tensor) -> torch.Tensor:
@@ -415,7 +418,7 @@ class MoELayer:
     def __call__(self, x: torch.Tensor, outputs=None, y=None) -> torch.Tensor:
         return moe_layer_forward(x, self.weights, self.k, self.routing, self.capacity_factor,
                                  outputs=outputs, workspace=self.workspace(x), y=y,
-                                 renormalize=self.renormalize)
+                                 renormalize=self.renormalize, capacity=self.capacity)
 
 
 class HostPipeline:

@@ -4,8 +4,10 @@
 // MoELayer.forward in "Mixture of Experts（MoE）の理論と実装" and of
 // MoELayerWithAuxLoss.forward in "Sparse Mixture of Experts(MoE) 아키텍처 심층
 // 분석".  One warp per token, float4 columns, slots summed in order j = 0..k-1
-// (deterministic).  Expert choice sums the experts that picked the token in
-// ascending expert order, weighted by the raw dispatch-mask score.
+// (deterministic), skipping slots without a dispatch row (inv_perm < 0:
+// dropped by capacity-limited routing).  Expert choice sums the experts that
+// picked the token in ascending expert order, weighted by the raw
+// dispatch-mask score.
 //
 // Aux: f_e = count_e / T, p_e = mean_t g[t,e], loss = E * sum_e f_e p_e, the
 // load_balancing_loss of the first page; optionally also the convention of
@@ -34,6 +36,7 @@ __global__ void __launch_bounds__(kCombineThreads)
       for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int j = 0; j < k; ++j) {
         const int row = inv_perm[(size_t)t * k + j];
+        if (row < 0) continue;  // dropped by the expert's capacity
         const float wj = w[(size_t)t * k + j];
         const float4* src = y_perm + (size_t)row * d4;
 #pragma unroll

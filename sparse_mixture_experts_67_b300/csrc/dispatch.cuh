@@ -53,18 +53,29 @@ __global__ void __launch_bounds__(kDispatchThreads)
 // the tiles before its own), warp per expert, lanes over tiles; the expert
 // offsets are the exclusive scan of the totals, and CTA 0 also writes counts /
 // offsets and, given aux_partials, the load-balancing statistics (same
-// reduction order as aux_finalize_kernel).  Optional extras:
+// reduction order as aux_finalize_kernel).
+// cap (capacity-limited token choice; INT_MAX: none): an expert's segment
+// holds its first cap assignments in assignment order, i.e. in token order;
+// later ones are dropped (inv_perm -1, no row).  With w_cap != nullptr the
+// [T, k] weights of the tile's tokens are then renormalised over their kept
+// slots in place (0 on dropped slots; all 0 for a token with none kept).
+// dropped (nullable, CTA 0) gets the number of dropped assignments.
+// Optional extras:
 // x != nullptr copies x[a / k] into x_perm[row] (16-byte vectors, warp per
 // row); y_zero != nullptr zeroes the y rows of the tile's tokens
 // (tokens_per_tile of them) for an accumulating combine downstream.
 // Large count matrices: one CTA computes every tile's first dispatch row per
 // expert (tile_base), the counts and the offsets; the scatter CTAs then read
 // their row of tile_base instead of reducing the whole matrix each.
+// cap: per-expert capacity (INT_MAX: none).  Segments hold min(count, cap)
+// rows; tile_base[t, e] is the segment start plus the expert's assignments in
+// tiles before t, so a row at or past segment start + cap is a dropped one;
+// dropped (nullable) gets the number of dropped assignments.
 constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads)
     dispatch_scan_kernel(const int32_t* __restrict__ tile_counts, int tiles, int E, int A,
                          int32_t* __restrict__ tile_base, int32_t* __restrict__ counts,
-                         int32_t* __restrict__ offsets) {
+                         int32_t* __restrict__ offsets, int cap, int32_t* __restrict__ dropped) {
   pdl_begin();
   __shared__ int s_tot[MOE_MAX_EXPERTS];
   __shared__ int s_off[MOE_MAX_EXPERTS];
@@ -82,7 +93,7 @@ __global__ void __launch_bounds__(kScanThreads)
     constexpr int per = MOE_MAX_EXPERTS / 32;
     const int e0 = lane * per;
     int run = 0;
-    for (int e = e0; e < min(E, e0 + per); ++e) run += s_tot[e];
+    for (int e = e0; e < min(E, e0 + per); ++e) run += min(s_tot[e], cap);
     int incl = run;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -92,7 +103,11 @@ __global__ void __launch_bounds__(kScanThreads)
     int ex = incl - run;
     for (int e = e0; e < min(E, e0 + per); ++e) {
       s_off[e] = ex;
-      ex += s_tot[e];
+      ex += min(s_tot[e], cap);
+    }
+    if (lane == 31) {
+      offsets[E] = ex;  // rows kept
+      if (dropped) *dropped = A - ex;
     }
   }
   __syncthreads();
@@ -115,7 +130,6 @@ __global__ void __launch_bounds__(kScanThreads)
       offsets[e] = s_off[e];
     }
   }
-  if (threadIdx.x == 0) offsets[E] = A;
 }
 
 // The in-CTA reduction reads tiles * E counts per CTA; above this many
@@ -132,10 +146,12 @@ __global__ void __launch_bounds__(kDispatchThreads)
                             const float* __restrict__ aux_partials, int T, float* __restrict__ f,
                             float* __restrict__ p, float* __restrict__ loss,
                             float* __restrict__ f_frac, float* __restrict__ loss_frac,
-                            float4* __restrict__ y_zero, int d4, int tokens_per_tile) {
+                            float4* __restrict__ y_zero, int d4, int tokens_per_tile, int cap,
+                            float* __restrict__ w_cap, int32_t* __restrict__ dropped) {
   pdl_begin();
   __shared__ int running[MOE_MAX_EXPERTS];
   __shared__ int s_tot[MOE_MAX_EXPERTS];
+  __shared__ int s_seg[MOE_MAX_EXPERTS];  // segment start of each expert
   __shared__ int wcnt[kDispatchWarps][MOE_MAX_EXPERTS];
   __shared__ int s_row[kDispatchThreads];
   __shared__ int s_tok[kDispatchThreads];
@@ -143,8 +159,10 @@ __global__ void __launch_bounds__(kDispatchThreads)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int me = blockIdx.x;
   const bool fused_scan = tile_base == nullptr;
-  for (int e = fused_scan ? E : threadIdx.x; e < E; e += blockDim.x)
+  for (int e = fused_scan ? E : threadIdx.x; e < E; e += blockDim.x) {
     running[e] = tile_base[(size_t)me * E + e];
+    s_seg[e] = offsets[e];  // written by dispatch_scan_kernel
+  }
   for (int e = fused_scan ? warp : E; e < E; e += kDispatchWarps) {
     int tot = 0, pre = 0;
     for (int t = lane; t < tiles; t += 32) {
@@ -169,7 +187,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
     constexpr int per = MOE_MAX_EXPERTS / 32;
     const int e0 = lane * per;
     int run = 0;
-    for (int e = e0; e < min(E, e0 + per); ++e) run += s_tot[e];
+    for (int e = e0; e < min(E, e0 + per); ++e) run += min(s_tot[e], cap);
     int incl = run;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -183,10 +201,14 @@ __global__ void __launch_bounds__(kDispatchThreads)
         counts[e] = v;
         offsets[e] = ex;
       }
+      s_seg[e] = ex;
       running[e] += ex;
-      ex += v;
+      ex += min(v, cap);
     }
-    if (me == 0 && lane == 31) offsets[E] = A;
+    if (me == 0 && lane == 31) {
+      offsets[E] = ex;  // rows kept
+      if (dropped) *dropped = A - ex;
+    }
   }
   if (y_zero != nullptr) {
     const int tk0 = me * tokens_per_tile;
@@ -208,9 +230,14 @@ __global__ void __launch_bounds__(kDispatchThreads)
     if (valid) {
       int row = running[e] + rank;
       for (int w = 0; w < warp; ++w) row += wcnt[w][e];
-      perm[row] = a;
-      inv_perm[a] = row;
-      s_row[threadIdx.x] = row;
+      if (row - s_seg[e] < cap) {
+        perm[row] = a;
+        inv_perm[a] = row;
+        s_row[threadIdx.x] = row;
+      } else {  // past the expert's capacity: dropped
+        inv_perm[a] = -1;
+        s_row[threadIdx.x] = -1;
+      }
       s_tok[threadIdx.x] = a / k;
     }
     __syncthreads();
@@ -226,6 +253,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
     if (x != nullptr) {  // copy this round's rows, one warp per row
       const int nvalid = min(kDispatchThreads, a1 - base);
       for (int i = warp; i < nvalid; i += kDispatchWarps) {
+        if (s_row[i] < 0) continue;  // dropped assignment: no row
         const uint4* src = x + (size_t)s_tok[i] * vec_per_row;
         uint4* dst = x_perm + (size_t)s_row[i] * vec_per_row;
         int v = lane;
@@ -241,6 +269,17 @@ __global__ void __launch_bounds__(kDispatchThreads)
       }
     }
     __syncthreads();
+  }
+  if (w_cap != nullptr) {  // renormalise the kept weights of this tile's tokens
+    for (int t = a0 / k + threadIdx.x; t < (a1 + k - 1) / k; t += blockDim.x) {
+      float sum = 0.f;
+      for (int j = 0; j < k; ++j)
+        if (inv_perm[(size_t)t * k + j] >= 0) sum += w_cap[(size_t)t * k + j];
+      for (int j = 0; j < k; ++j) {
+        const size_t a = (size_t)t * k + j;
+        w_cap[a] = (inv_perm[a] >= 0 && sum > 0.f) ? w_cap[a] / sum : 0.f;
+      }
+    }
   }
   if (me != 0 || aux_partials == nullptr || !fused_scan) return;
   // CTA 0: aux statistics from the router's per-tile partial sums of g

@@ -1,5 +1,6 @@
 // C ABI of the MoE layer forward: argument checks, workspace carving and the
 // launch sequence.  Every entry point only enqueues on the caller's stream.
+#include <limits.h>
 #include <math.h>
 #include <string.h>
 
@@ -157,7 +158,8 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
                                   const float* aux_partials = nullptr, float* f = nullptr,
                                   float* p = nullptr, float* loss = nullptr,
                                   float* y_zero = nullptr, float* f_frac = nullptr,
-                                  float* loss_frac = nullptr) {
+                                  float* loss_frac = nullptr, int cap = INT_MAX,
+                                  float* w_cap = nullptr, int32_t* dropped = nullptr) {
   const long long A = (long long)T * k;
   const int tiles = dispatch_tiles(A, tile);
   cudaError_t e = cudaSuccess;
@@ -168,7 +170,7 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
   const bool separate_scan = (long long)tiles * tiles * E > kFusedScanMaxReads;
   if (separate_scan) {
     e = launch_k(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, nullptr, 0, tile_counts,
-                 tiles, E, (int)A, tile_base, counts, offsets);
+                 tiles, E, (int)A, tile_base, counts, offsets, cap, dropped);
     if (e == cudaSuccess && aux_partials)
       e = launch_k(aux_finalize_kernel, dim3(1), dim3(kAuxThreads), 0, s, nullptr, 0, aux_partials,
                    tiles, counts, T, E, k, f, p, loss, f_frac, loss_frac);
@@ -180,7 +182,7 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
       (int)A, E, k, tile, tile_counts, base, tiles, perm, inv_perm, counts, offsets,
       static_cast<const uint4*>(x), (int)(d * elt_size(dt) / 16), static_cast<uint4*>(x_perm),
       aux_partials, T, f, p, loss, f_frac, loss_frac, reinterpret_cast<float4*>(y_zero), d / 4,
-      tile / k));
+      tile / k, cap, w_cap, dropped));
 }
 
 static moe_status check_permute(const void* x, const void* x_perm, int T, int d, int E, int k,
@@ -382,7 +384,10 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   if (D.routing != MOE_ROUTING_TOPK && !ec) return MOE_ERR_INVALID_ARG;
   if (D.T < 0 || D.E < 1 || D.E > MOE_MAX_EXPERTS || D.F <= 0) return MOE_ERR_INVALID_ARG;
   if (!ec && (D.k < 1 || D.k > D.E)) return MOE_ERR_INVALID_ARG;
-  if (D.flags & ~MOE_ROUTE_NO_RENORM) return MOE_ERR_INVALID_ARG;
+  if (D.flags & ~(MOE_ROUTE_NO_RENORM | MOE_ROUTE_CAPACITY)) return MOE_ERR_INVALID_ARG;
+  const bool capacity = (D.flags & MOE_ROUTE_CAPACITY) != 0;
+  if (capacity && (ec || (D.flags & MOE_ROUTE_NO_RENORM) || !(D.capacity_factor > 0.f)))
+    return MOE_ERR_INVALID_ARG;
   if (ec && !(D.capacity_factor > 0.f)) return MOE_ERR_INVALID_ARG;
   moe_status st = check_experts(0, D.d, D.F, D.E, D.dtype);
   if (st != MOE_OK) return st;
@@ -467,10 +472,19 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   // the scatter also copies the x rows into dispatch order: contiguous row blocks
   // keep the gate/up operand loads full-width TMA boxes (gathering rows inside
   // the GEMM re-fetches them once per n-block and measured several times slower)
+  // capacity-limited token choice: each expert keeps its first `cap` assignments
+  // in token order, cap = int(T / E * capacity_factor * k) (double, this order)
+  int cap = INT_MAX;
+  if (capacity) {
+    const double capd =
+        floor((double)D.T / (double)D.E * (double)D.capacity_factor * (double)k);
+    cap = capd >= (double)A ? (int)A : (int)capd;
+  }
   st = dispatch_launch(x, idx, D.T, D.d, D.E, k, D.dtype, x_perm, counts, offsets, perm, inv_perm,
                        tile_counts, tile_base, tile, true, s, aux, O.f ? O.f : fpl,
                        O.p ? O.p : fpl + D.E, O.loss ? O.loss : fpl + 2 * D.E,
-                       fused_combine ? y : nullptr, O.f_frac, O.loss_frac);
+                       fused_combine ? y : nullptr, O.f_frac, O.loss_frac, cap,
+                       capacity ? tw : nullptr, O.dropped);
   if (st != MOE_OK) return st;
   if (fused_combine) {
     // down projection with the combine in its epilogue (deterministic for k <= 2)

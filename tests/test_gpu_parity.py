@@ -273,6 +273,46 @@ def test_layer_without_renormalisation(moe, torch, E, k):
     _check_topk_layer(moe, torch, cfg, renormalize=False)
 
 
+@pytest.mark.parametrize("E,k,cf", [(8, 2, 1.0), (16, 4, 0.8), (8, 1, 0.5), (6, 2, 0.001)],
+                         ids=["e8_k2_fused", "e16_k4", "e8_k1_heavy", "capacity_zero"])
+def test_layer_capacity_limited(moe, torch, E, k, cf):
+    """MOE_ROUTE_CAPACITY against the oracle's capacity_route on the device logits: the
+    selection, the kept segments, the drop count, the kept-renormalised weights and y
+    (the fused down+combine for k <= 2, the separate combine above; all dropped at cf 0.001)."""
+    cfg = synth.small_config(f"cap_e{E}_k{k}", 1000, 256, 384, E, k, "bf16", seed=50 + E + k,
+                             x_std=1.0, w_std=0.02, wg_std=0.1, bias="zipf")
+    inp = cached_inputs(cfg)
+    w = dev_weights(inp)
+    x = to_dev(inp.x)
+    T = cfg.T
+    outs = {"topk_idx": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+            "topk_w": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+            "logits": torch.empty((T, E), dtype=torch.float32, device="cuda"),
+            "counts": torch.empty((E,), dtype=torch.int32, device="cuda"),
+            "offsets": torch.empty((E + 1,), dtype=torch.int32, device="cuda"),
+            "dropped": torch.full((1,), -7, dtype=torch.int32, device="cuda")}
+    y = moe.moe_layer_forward(x, w, k=k, capacity_factor=cf, outputs=outs, capacity=True)
+    torch.cuda.synchronize()
+    s_gpu = _np(outs["logits"]).astype(np.float64)
+    cf32 = float(np.float32(cf))
+    idx_g, w_cap, kept, dropped, load, cap = oracle.capacity_route(s_gpu, k, cf32)
+    np.testing.assert_array_equal(_np(outs["topk_idx"]), idx_g)
+    np.testing.assert_array_equal(_np(outs["counts"]), np.bincount(idx_g.ravel(), minlength=E))
+    np.testing.assert_array_equal(_np(outs["offsets"]), np.concatenate([[0], np.cumsum(load)]))
+    assert int(_np(outs["dropped"])[0]) == dropped
+    if cf >= 0.5:
+        assert dropped > 0  # the capacity binds on these inputs
+    np.testing.assert_allclose(_np(outs["topk_w"]), w_cap, rtol=0, atol=2e-6)
+    x64 = synth.to_f64(inp.x)
+    experts = synth.ExpertsF64(inp.w_gate, inp.w_up, inp.w_down)
+    y_ref = oracle.moe_forward(x64, idx_g, w_cap, experts)
+    y_ref_h = oracle.moe_forward(x64, idx_g, w_cap, experts, round_h=oracle.bf16_round)
+    if dropped == T * k:
+        assert np.all(_np(y) == 0)
+    else:
+        assert_close_output(_np(y), y_ref, "bf16", what=f"y[{cfg.name}]", ref_bf16_h=y_ref_h)
+
+
 @pytest.mark.slow
 def test_layer_top2_d1024(moe, torch):
     _check_topk_layer(moe, torch, synth.CONFIGS["top2_d1024"], sample=1024)
