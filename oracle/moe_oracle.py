@@ -124,6 +124,16 @@ def aux_stats_fraction(g: Array, idx: Array, E: int) -> Tuple[Array, float]:
     return f, float(E * np.sum(f * p))
 
 
+def router_z_loss(s: Array) -> float:
+    """mean_t (log sum_e exp s[t, e])^2, the ST-MoE style router z-loss of
+    [sparse-moe] router_z_loss (logsumexp over the experts, squared, averaged
+    over the tokens); the log-sum-exp is taken with the row max subtracted."""
+    s = np.asarray(s, np.float64)
+    m = np.max(s, axis=1)
+    log_z = m + np.log(np.sum(np.exp(s - m[:, None]), axis=1))
+    return float(np.mean(log_z ** 2))
+
+
 def dispatch(idx: Array, E: int) -> Tuple[Array, Array, Array, Array]:
     """(counts [E], offsets [E+1], perm [T*k], inv_perm [T*k]).
 

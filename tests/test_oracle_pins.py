@@ -246,6 +246,22 @@ def pin_capacity_route(orc):
     np.testing.assert_allclose(w, orc.topk_route(s, 2)[1], rtol=0, atol=0)
 
 
+def pin_router_z_loss(orc):
+    """[sparse-moe] router_z_loss: closed forms (equal logits c over E experts give
+    (c + ln E)^2; one expert gives mean s^2) and scipy's logsumexp on random logits."""
+    from scipy.special import logsumexp
+
+    for E, c in ((8, 0.0), (5, 1.5), (64, -3.0)):
+        s = np.full((7, E), c)
+        assert abs(orc.router_z_loss(s) - (c + math.log(E)) ** 2) < 1e-12
+    s1 = np.array([[0.5], [-2.0], [3.0]])
+    assert abs(orc.router_z_loss(s1) - np.mean(s1[:, 0] ** 2)) < 1e-15
+    rng = np.random.default_rng(24)
+    s = rng.normal(0, 4.0, (50, 16)) + 30.0  # large logits: needs the max subtraction
+    ref = float(np.mean(logsumexp(s, axis=1) ** 2))
+    assert abs(orc.router_z_loss(s) - ref) <= 1e-12 * ref
+
+
 def pin_bias_only(orc):
     """x = 0: the logits are the bias ([zh-moe] GatingNetwork adds b)."""
     b = np.array([1.5 * math.log(1.0 / (e + 1)) for e in range(6)])
@@ -565,6 +581,15 @@ def _capacity_no_renorm(s, k, cf):
     return _greedy(s, k, oracle.token_capacity(T, E, cf, k), order=range(T), renorm=False)
 
 
+def _z_loss_unsquared(s):
+    m = np.max(s, axis=1)
+    return float(np.mean(m + np.log(np.sum(np.exp(s - m[:, None]), axis=1))))
+
+
+def _z_loss_max_only(s):
+    return float(np.mean(np.max(s, axis=1) ** 2))
+
+
 def _silu_sign(a):
     return a / (1.0 + np.exp(a))
 
@@ -591,6 +616,8 @@ MUTANTS = {
     "capacity_without_k": dict(capacity_route=_capacity_without_k),
     "capacity_last_tokens_first": dict(capacity_route=_capacity_last_tokens_first),
     "capacity_kept_not_renormalised": dict(capacity_route=_capacity_no_renorm),
+    "z_loss_not_squared": dict(router_z_loss=_z_loss_unsquared),
+    "z_loss_max_instead_of_logsumexp": dict(router_z_loss=_z_loss_max_only),
 }
 
 
