@@ -119,6 +119,16 @@ def test_layer_workspace_and_errors(L):
     assert L.moe_layer_forward(ctypes.byref(fp), ctypes.byref(w), _p(), _p(), None, _p(), 1 << 30, z) == 2
     flagged = moe._Desc(8192, 1024, 4096, 8, 2, 0, 0.0, 1, 4)  # unknown routing flag bits
     assert L.moe_layer_forward(ctypes.byref(flagged), ctypes.byref(w), _p(), _p(), None, _p(), ws, z) == 1
+    # capacity-limited routing needs a positive factor, top-k routing and renormalised weights
+    cap0 = moe._Desc(8192, 1024, 4096, 8, 2, 0, 0.0, 1, moe.MOE_ROUTE_CAPACITY)
+    assert L.moe_layer_forward(ctypes.byref(cap0), ctypes.byref(w), _p(), _p(), None, _p(), ws, z) == 1
+    cap_nr = moe._Desc(8192, 1024, 4096, 8, 2, 0, 1.25, 1,
+                       moe.MOE_ROUTE_CAPACITY | moe.MOE_ROUTE_NO_RENORM)
+    assert L.moe_layer_forward(ctypes.byref(cap_nr), ctypes.byref(w), _p(), _p(), None, _p(), ws, z) == 1
+    cap_ec = moe._Desc(8192, 1024, 4096, 16, 0, 1, 2.0, 1, moe.MOE_ROUTE_CAPACITY)
+    ws_ec = L.moe_layer_workspace_size(ctypes.byref(cap_ec))
+    assert L.moe_layer_forward(ctypes.byref(cap_ec), ctypes.byref(w), _p(), _p(), None, _p(), ws_ec,
+                               z) == 1
 
 
 def test_no_cpu_fallback_without_device():
