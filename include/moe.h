@@ -104,11 +104,16 @@ moe_status moe_device_error(uint32_t* word, int clear);
  *             holds sum of g[t,e] over the r-th block of tokens (32 tokens
  *             for E <= 16, 64 above; moe_route_aux_rows(T) covers both),
  *             consumed by moe_aux_loss.
+ *   z_partials: optional fp32 [moe_route_aux_rows(T)]; entry r holds the sum
+ *             over the r-th block of tokens of (log sum_e exp s[t,e])^2, the
+ *             router z-loss of [sparse-moe] router_z_loss before its mean
+ *             (consumed by moe_aux_loss).
  * Limits: 1 <= k <= E <= 256.                                               */
 size_t moe_route_aux_rows(int T);
 moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, int d, int E,
                      int k, moe_dtype dt, int32_t* topk_idx, float* topk_w, float* logits,
-                     float* probs, float* aux_partials, int flags, moe_stream_t stream);
+                     float* probs, float* aux_partials, float* z_partials, int flags,
+                     moe_stream_t stream);
 
 /* -------------------------------------------------- expert-choice router
  * [sparse-moe] ExpertChoiceGating.forward:
@@ -235,11 +240,14 @@ moe_status moe_ec_combine(const float* y_perm, const int32_t* pos, const float* 
  *   (= loss / k; balanced routing gives 1)
  * p comes from probs [T,E] when probs != NULL, else from aux_partials
  * ([moe_route_aux_rows(T), E], written by moe_route); one must be given.
- * f, p, loss, f_frac, loss_frac: each may be NULL.
+ * Router z-loss ([sparse-moe] router_z_loss), optional: z_loss = mean over
+ *   tokens of (log sum_e exp s)^2 from z_partials (written by moe_route).
+ * f, p, loss, f_frac, loss_frac, z_loss: each may be NULL.
  * Fixed-order reductions: deterministic.                                    */
 moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int32_t* counts,
                         int T, int E, int k, float* f, float* p, float* loss, float* f_frac,
-                        float* loss_frac, moe_stream_t stream);
+                        float* loss_frac, const float* z_partials, float* z_loss,
+                        moe_stream_t stream);
 
 /* ---------------------------------------------------------- whole layer */
 typedef struct {
@@ -274,6 +282,7 @@ typedef struct {
   float* f_frac;           /* [E]    top-k only: counts / (T k) */
   float* loss_frac;        /* [1]    top-k only: loss / k */
   int32_t* dropped;        /* [1]    top-k with MOE_ROUTE_CAPACITY: dropped assignments */
+  float* z_loss;           /* [1]    top-k only: router z-loss */
 } moe_layer_outputs;
 
 /* Bytes of scratch moe_layer_forward needs for `desc` (0 on invalid desc). */

@@ -54,7 +54,7 @@ class _Weights(ctypes.Structure):
 
 
 _OUT_FIELDS = ("topk_idx", "topk_w", "logits", "counts", "offsets", "f", "p", "loss", "ec_idx",
-               "ec_score", "pos", "f_frac", "loss_frac", "dropped")
+               "ec_score", "pos", "f_frac", "loss_frac", "dropped", "z_loss")
 
 
 class _Outputs(ctypes.Structure):
@@ -68,7 +68,7 @@ _SIGS = {
     "moe_status_string": ([_I], ctypes.c_char_p),
     "moe_device_error": ([ctypes.POINTER(ctypes.c_uint32), _I], _I),
     "moe_route_aux_rows": ([_I], _Z),
-    "moe_route": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P], _I),
+    "moe_route": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P], _I),
     "moe_expert_choice_capacity": ([_I, _I, _F], _I),
     "moe_expert_choice_route": ([_P, _P, _P, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _Z),
@@ -82,7 +82,7 @@ _SIGS = {
     "moe_experts_swiglu": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "moe_combine": ([_P, _P, _P, _I, _I, _I, _P, _P], _I),
     "moe_ec_combine": ([_P, _P, _P, _I, _I, _I, _I, _P, _P], _I),
-    "moe_aux_loss": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P], _I),
+    "moe_aux_loss": ([_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P], _I),
     "moe_layer_workspace_size": ([ctypes.POINTER(_Desc)], _Z),
     "moe_layer_forward": ([ctypes.POINTER(_Desc), ctypes.POINTER(_Weights), _P, _P,
                            ctypes.POINTER(_Outputs), _P, _Z, _P], _I),
@@ -183,10 +183,12 @@ def moe_route(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[torch.Tensor], 
         out["probs"] = _empty((T, E), torch.float32, x)
     if want_aux:
         out["aux_partials"] = _empty((max(1, moe_route_aux_rows(T)), E), torch.float32, x)
+        out["z_partials"] = _empty((max(1, moe_route_aux_rows(T)),), torch.float32, x)
     _check("moe_route", lib().moe_route(
         _ptr(x), _ptr(w_g), _ptr(bias), T, d, E, k, _dtype(x), _ptr(out["topk_idx"]),
         _ptr(out["topk_w"]), _ptr(out.get("logits")), _ptr(out.get("probs")),
-        _ptr(out.get("aux_partials")), 0 if renormalize else MOE_ROUTE_NO_RENORM, _stream()))
+        _ptr(out.get("aux_partials")), _ptr(out.get("z_partials")),
+        0 if renormalize else MOE_ROUTE_NO_RENORM, _stream()))
     return out
 
 
@@ -336,10 +338,12 @@ def moe_ec_combine(y_perm: torch.Tensor, pos: torch.Tensor, ec_score: torch.Tens
 
 
 def moe_aux_loss(counts: torch.Tensor, T: int, k: int, aux_partials: Optional[torch.Tensor] = None,
-                 probs: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
+                 probs: Optional[torch.Tensor] = None,
+                 z_partials: Optional[torch.Tensor] = None) -> Dict[str, torch.Tensor]:
     """f [E], p [E], loss [1] from router partial sums (or from probs [T,E]), and the
-    fraction-of-assignments convention f_frac [E] = counts / (T k), loss_frac [1] = loss / k."""
-    _dev(counts, aux_partials, probs)
+    fraction-of-assignments convention f_frac [E] = counts / (T k), loss_frac [1] = loss / k;
+    with z_partials (from moe_route) also the router z-loss z_loss [1]."""
+    _dev(counts, aux_partials, probs, z_partials)
     E = counts.numel()
     if probs is not None and aux_partials is None:
         aux_partials = _empty((max(1, moe_route_aux_rows(T)), E), torch.float32, counts)
@@ -347,9 +351,12 @@ def moe_aux_loss(counts: torch.Tensor, T: int, k: int, aux_partials: Optional[to
            "loss": _empty((1,), torch.float32, counts),
            "f_frac": _empty((E,), torch.float32, counts),
            "loss_frac": _empty((1,), torch.float32, counts)}
+    if z_partials is not None:
+        out["z_loss"] = _empty((1,), torch.float32, counts)
     _check("moe_aux_loss", lib().moe_aux_loss(
         _ptr(probs), _ptr(aux_partials), _ptr(counts), T, E, k, _ptr(out["f"]), _ptr(out["p"]),
-        _ptr(out["loss"]), _ptr(out["f_frac"]), _ptr(out["loss_frac"]), _stream()))
+        _ptr(out["loss"]), _ptr(out["f_frac"]), _ptr(out["loss_frac"]), _ptr(z_partials),
+        _ptr(out.get("z_loss")), _stream()))
     return out
 
 

@@ -12,7 +12,8 @@
 // Aux: f_e = count_e / T, p_e = mean_t g[t,e], loss = E * sum_e f_e p_e, the
 // load_balancing_loss of the first page; optionally also the convention of
 // compute_load_balancing_loss in the second: f_frac_e = count_e / (T k),
-// loss_frac = loss / k.  p is reduced from per-block partial
+// loss_frac = loss / k; and the router z-loss of the second page, the mean of
+// the squared log-sum-exps, from the router's per-tile sums.  p is reduced from per-block partial
 // sums in a fixed order, so the result does not depend on scheduling.
 #pragma once
 
@@ -144,7 +145,8 @@ __global__ void __launch_bounds__(kAuxThreads)
     aux_finalize_kernel(const float* __restrict__ partials, int rows, const int32_t* __restrict__ counts,
                         int T, int E, int k, float* __restrict__ f, float* __restrict__ p,
                         float* __restrict__ loss, float* __restrict__ f_frac,
-                        float* __restrict__ loss_frac) {
+                        float* __restrict__ loss_frac, const float* __restrict__ z_partials,
+                        float* __restrict__ z_loss) {
   pdl_begin();
   __shared__ float s[MOE_MAX_EXPERTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -172,6 +174,13 @@ __global__ void __launch_bounds__(kAuxThreads)
   }
   if (threadIdx.x == 0 && loss) *loss = (float)E * s[0];
   if (threadIdx.x == 0 && loss_frac) *loss_frac = (float)E * s[0] / (float)k;
+  if (warp == 0 && z_partials && z_loss) {  // router z-loss: fixed-order mean
+    float acc = 0.f;
+    for (int r = lane; r < rows; r += 32) acc += z_partials[r];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+    if (lane == 0) *z_loss = acc / (float)T;
+  }
 }
 
 }  // namespace moe

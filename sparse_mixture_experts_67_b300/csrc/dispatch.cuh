@@ -147,7 +147,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
                             float* __restrict__ p, float* __restrict__ loss,
                             float* __restrict__ f_frac, float* __restrict__ loss_frac,
                             float4* __restrict__ y_zero, int d4, int tokens_per_tile, int cap,
-                            float* __restrict__ w_cap, int32_t* __restrict__ dropped) {
+                            float* __restrict__ w_cap, int32_t* __restrict__ dropped,
+                            const float* __restrict__ z_partials, float* __restrict__ z_loss) {
   pdl_begin();
   __shared__ int running[MOE_MAX_EXPERTS];
   __shared__ int s_tot[MOE_MAX_EXPERTS];
@@ -306,6 +307,13 @@ __global__ void __launch_bounds__(kDispatchThreads)
   }
   if (threadIdx.x == 0 && loss) *loss = (float)E * s_fp[0];
   if (threadIdx.x == 0 && loss_frac) *loss_frac = (float)E * s_fp[0] / (float)k;
+  if (warp == 0 && z_partials && z_loss) {  // router z-loss: fixed-order mean
+    float acc = 0.f;
+    for (int r = lane; r < tiles; r += 32) acc += z_partials[r];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+    if (lane == 0) *z_loss = acc / (float)T;
+  }
 }
 
 // x_perm[r,:] = x[src[r] / div, :]; one warp per row, 16-byte vectors.

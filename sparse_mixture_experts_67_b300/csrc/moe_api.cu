@@ -81,7 +81,7 @@ size_t moe_route_aux_rows(int T) { return T <= 0 ? 0 : (size_t)ceil_div(T, kRout
 
 moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, int d, int E, int k,
                      moe_dtype dt, int32_t* topk_idx, float* topk_w, float* logits, float* probs,
-                     float* aux_partials, int flags, moe_stream_t stream) {
+                     float* aux_partials, float* z_partials, int flags, moe_stream_t stream) {
   if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
   if (flags & ~MOE_ROUTE_NO_RENORM) return MOE_ERR_INVALID_ARG;
   moe_status st = check_dims(d, dt);
@@ -91,7 +91,7 @@ moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, i
   if (dt == MOE_BF16 && (!aligned16(x) || !aligned16(w_g))) return MOE_ERR_UNSUPPORTED;
   return cuda_status(launch_router(x, w_g, bias, T, d, E, k, dt == MOE_BF16, topk_idx, topk_w,
                                    logits, probs, aux_partials, (cudaStream_t)stream, nullptr,
-                                   nullptr, flags));
+                                   nullptr, flags, z_partials));
 }
 
 int moe_expert_choice_capacity(int T, int E, float capacity_factor) {
@@ -159,7 +159,8 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
                                   float* p = nullptr, float* loss = nullptr,
                                   float* y_zero = nullptr, float* f_frac = nullptr,
                                   float* loss_frac = nullptr, int cap = INT_MAX,
-                                  float* w_cap = nullptr, int32_t* dropped = nullptr) {
+                                  float* w_cap = nullptr, int32_t* dropped = nullptr,
+                                  const float* z_partials = nullptr, float* z_loss = nullptr) {
   const long long A = (long long)T * k;
   const int tiles = dispatch_tiles(A, tile);
   cudaError_t e = cudaSuccess;
@@ -173,7 +174,7 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
                  tiles, E, (int)A, tile_base, counts, offsets, cap, dropped);
     if (e == cudaSuccess && aux_partials)
       e = launch_k(aux_finalize_kernel, dim3(1), dim3(kAuxThreads), 0, s, nullptr, 0, aux_partials,
-                   tiles, counts, T, E, k, f, p, loss, f_frac, loss_frac);
+                   tiles, counts, T, E, k, f, p, loss, f_frac, loss_frac, z_partials, z_loss);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   const int32_t* base = separate_scan ? tile_base : nullptr;
@@ -182,7 +183,7 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
       (int)A, E, k, tile, tile_counts, base, tiles, perm, inv_perm, counts, offsets,
       static_cast<const uint4*>(x), (int)(d * elt_size(dt) / 16), static_cast<uint4*>(x_perm),
       aux_partials, T, f, p, loss, f_frac, loss_frac, reinterpret_cast<float4*>(y_zero), d / 4,
-      tile / k, cap, w_cap, dropped));
+      tile / k, cap, w_cap, dropped, z_partials, z_loss));
 }
 
 static moe_status check_permute(const void* x, const void* x_perm, int T, int d, int E, int k,
@@ -319,7 +320,8 @@ moe_status moe_ec_combine(const float* y_perm, const int32_t* pos, const float* 
 
 moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int32_t* counts, int T,
                         int E, int k, float* f, float* p, float* loss, float* f_frac,
-                        float* loss_frac, moe_stream_t stream) {
+                        float* loss_frac, const float* z_partials, float* z_loss,
+                        moe_stream_t stream) {
   if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!counts || (!probs && !aux_partials)) return MOE_ERR_INVALID_ARG;
@@ -334,7 +336,8 @@ moe_status moe_aux_loss(const float* probs, const float* aux_partials, const int
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return cuda_status(launch_k(aux_finalize_kernel, dim3(1), dim3(kAuxThreads), 0, s, nullptr, 0,
-                              aux_partials, rows, counts, T, E, k, f, p, loss, f_frac, loss_frac));
+                              aux_partials, rows, counts, T, E, k, f, p, loss, f_frac, loss_frac,
+                              z_partials, z_loss));
 }
 
 size_t moe_layer_workspace_size(const moe_layer_desc* desc) {
@@ -371,6 +374,7 @@ size_t moe_layer_workspace_size(const moe_layer_desc* desc) {
     cv.take_bytes(A * D.d * es);                           // x_perm
     cv.take_bytes(A * D.F * es);                           // h
     cv.take<float>(A * D.d);                               // y_perm
+    cv.take<float>(moe_route_aux_rows(D.T));               // z-loss partials
   }
   return cv.used + 256;
 }
@@ -450,6 +454,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   void* x_perm = cv.take_bytes(A * D.d * es);
   void* h = cv.take_bytes(A * D.F * es);
   float* y_perm = cv.take<float>(A * D.d);
+  float* zpart = cv.take<float>(moe_route_aux_rows(D.T));
   if (O.topk_idx) idx = O.topk_idx;
   if (O.topk_w) tw = O.topk_w;
   if (O.counts) counts = O.counts;
@@ -464,7 +469,8 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   int32_t* tile_base = reinterpret_cast<int32_t*>(static_cast<char*>(pw) +
                                                   align256((size_t)tiles * D.E * sizeof(int32_t)));
   if (launch_router(x, w->w_g, w->bias, D.T, D.d, D.E, k, D.dtype == MOE_BF16, idx, tw, O.logits,
-                    nullptr, aux, s, tile_counts, nullptr, D.flags) != cudaSuccess)
+                    nullptr, aux, s, tile_counts, nullptr, D.flags,
+                    O.z_loss ? zpart : nullptr) != cudaSuccess)
     return MOE_ERR_CUDA;
   // k <= 2 (bf16): the down GEMM accumulates the combine into y, zeroed by the scatter
   const bool fused_combine = D.dtype == MOE_BF16 && k <= 2;
@@ -484,7 +490,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
                        tile_counts, tile_base, tile, true, s, aux, O.f ? O.f : fpl,
                        O.p ? O.p : fpl + D.E, O.loss ? O.loss : fpl + 2 * D.E,
                        fused_combine ? y : nullptr, O.f_frac, O.loss_frac, cap,
-                       capacity ? tw : nullptr, O.dropped);
+                       capacity ? tw : nullptr, O.dropped, O.z_loss ? zpart : nullptr, O.z_loss);
   if (st != MOE_OK) return st;
   if (fused_combine) {
     // down projection with the combine in its epilogue (deterministic for k <= 2)

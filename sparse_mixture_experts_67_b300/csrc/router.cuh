@@ -65,6 +65,8 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, const uint32_t* a, cons
 // logitsT_out (nullable): the logits once more, transposed to [E, T] (row e is
 // what the expert-choice selection of expert e reads).
 // flags & MOE_ROUTE_NO_RENORM: the weights stay the selected probabilities.
+// z_rows (nullable, k > 0): per dispatch tile, the sum over its tokens of
+// (log sum_e exp s[t,e])^2 (the router z-loss before the mean), row of tile0.
 template <int TOK, int SUB = TOK, int P = 1>
 __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k,
                                 const float* __restrict__ bias, int32_t* __restrict__ idx_out,
@@ -72,7 +74,8 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
                                 float* __restrict__ probs_out, float* __restrict__ aux_rows,
                                 int32_t* __restrict__ tile_counts, int tile0, float* s_m,
                                 float* s_inv, int* s_cnt, float* s_part,
-                                float* __restrict__ logitsT_out = nullptr, int flags = 0) {
+                                float* __restrict__ logitsT_out = nullptr, int flags = 0,
+                                float* __restrict__ z_rows = nullptr) {
   static_assert(TOK % SUB == 0, "dispatch tiles split the CTA's tokens");
   static_assert(P >= 1 && P <= 32 && (P & (P - 1)) == 0, "threads per token: a power of two");
   constexpr int NSUB = TOK / SUB;
@@ -103,9 +106,18 @@ __device__ void router_epilogue(float* S, int ldS, int tok0, int T, int E, int k
     if (live && q == 0) {
       s_m[r] = m;
       s_inv[r] = 1.0f / sum;
+      if (z_rows) s_part[r] = m + logf(sum);  // log-sum-exp, read just below
     }
   }
   __syncthreads();
+  if (k > 0 && z_rows) {  // per dispatch tile: sum of lse^2 in token order
+    for (int st = tid; st < nsub; st += nthr) {
+      float acc = 0.f;
+      for (int ri = st * SUB; ri < min(ntok, st * SUB + SUB); ++ri) acc += s_part[ri] * s_part[ri];
+      z_rows[st] = acc;
+    }
+    __syncthreads();  // s_part is reused by the aux sums
+  }
   // coalesced optional outputs: element i of the CTA's [ntok, E] block
   if (logits_out || probs_out) {
     const size_t base = (size_t)tok0 * E;
@@ -247,7 +259,7 @@ __global__ void __launch_bounds__(kRouterThreadsBf16)
                        int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                        float* __restrict__ logits_out, float* __restrict__ probs_out,
                        float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts,
-                       float* __restrict__ logitsT, int flags) {
+                       float* __restrict__ logitsT, int flags, float* __restrict__ z_partials) {
   pdl_begin();
   using C = RouterBf16<NT, TOK>;
   constexpr int EP = C::EP, LD = C::LD, SBK = C::SBK, STAGES = C::STAGES;
@@ -354,7 +366,8 @@ __global__ void __launch_bounds__(kRouterThreadsBf16)
   router_epilogue<TOK, TOK, C::P>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
                        blockIdx.x,
-                       s_m, s_inv, s_cnt, s_part, logitsT, flags);
+                       s_m, s_inv, s_cnt, s_part, logitsT, flags,
+                       z_partials ? z_partials + blockIdx.x : nullptr);
 }
 
 // fp32 router: FFMA over 32-wide d chunks, same epilogue.
@@ -376,7 +389,7 @@ __global__ void __launch_bounds__(2 * TOK)
                       int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                       float* __restrict__ logits_out, float* __restrict__ probs_out,
                       float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts,
-                      float* __restrict__ logitsT, int flags) {
+                      float* __restrict__ logitsT, int flags, float* __restrict__ z_partials) {
   pdl_begin();
   constexpr int EP = 8 * NT;
   constexpr int ld = kRouterBKf + 1;
@@ -422,7 +435,8 @@ __global__ void __launch_bounds__(2 * TOK)
   router_epilogue<TOK, TOK, kPf>(S, ldS, tok0, T, E, k, bias, idx_out, w_out, logits_out, probs_out,
                        aux_partials ? aux_partials + (size_t)blockIdx.x * E : nullptr, tile_counts,
                        blockIdx.x,
-                       s_m, s_inv, s_cnt, s_part, logitsT, flags);
+                       s_m, s_inv, s_cnt, s_part, logitsT, flags,
+                       z_partials ? z_partials + blockIdx.x : nullptr);
 }
 
 inline int router_nt(int E) {
@@ -435,7 +449,7 @@ template <int NT, int TOK>
 cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, int T, int d, int E,
                              int k, bool bf16, int32_t* idx, float* w, float* logits, float* probs,
                              float* aux, int32_t* tile_counts, float* logitsT, int flags,
-                             cudaStream_t st) {
+                             float* z_partials, cudaStream_t st) {
   const int grid = ceil_div(T, TOK);
   if (bf16) {
     const size_t sm = router_smem_bytes_bf16<NT, TOK>();
@@ -445,7 +459,7 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     return launch_k(router_bf16_kernel<NT, TOK>, dim3(grid), dim3(kRouterThreadsBf16), sm, st,
                     nullptr, 0, static_cast<const __nv_bfloat16*>(x),
                     static_cast<const __nv_bfloat16*>(wg), bias, T, d, E, k, idx, w, logits, probs,
-                    aux, tile_counts, logitsT, flags);
+                    aux, tile_counts, logitsT, flags, z_partials);
   } else {
     const size_t sm = router_smem_bytes_f32<NT, TOK>();
     cudaError_t e = cudaFuncSetAttribute(router_f32_kernel<NT, TOK>,
@@ -453,7 +467,7 @@ cudaError_t launch_router_nt(const void* x, const void* wg, const float* bias, i
     if (e != cudaSuccess) return e;
     return launch_k(router_f32_kernel<NT, TOK>, dim3(grid), dim3(2 * TOK), sm, st, nullptr, 0,
                     static_cast<const float*>(x), static_cast<const float*>(wg), bias, T, d, E, k,
-                    idx, w, logits, probs, aux, tile_counts, logitsT, flags);
+                    idx, w, logits, probs, aux, tile_counts, logitsT, flags, z_partials);
   }
 }
 
@@ -461,14 +475,14 @@ inline cudaError_t launch_router_mma(const void* x, const void* wg, const float*
                                  int E, int k, bool bf16, int32_t* idx, float* w, float* logits,
                                  float* probs, float* aux, cudaStream_t st,
                                  int32_t* tile_counts = nullptr, float* logitsT = nullptr,
-                                 int flags = 0) {
+                                 int flags = 0, float* z_partials = nullptr) {
 #define MOE_ROUTER_CASE(NT_)                                                                     \
   case NT_:                                                                                      \
     return router_tokens(E) == 32                                                                \
                ? launch_router_nt<NT_, 32>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, \
-                                           aux, tile_counts, logitsT, flags, st)                                 \
+                                           aux, tile_counts, logitsT, flags, z_partials, st)                                 \
                : launch_router_nt<NT_, 64>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, \
-                                           aux, tile_counts, logitsT, flags, st);
+                                           aux, tile_counts, logitsT, flags, z_partials, st);
   switch (router_nt(E)) {
     MOE_ROUTER_CASE(1)
     MOE_ROUTER_CASE(2)
@@ -477,7 +491,7 @@ inline cudaError_t launch_router_mma(const void* x, const void* wg, const float*
     MOE_ROUTER_CASE(16)
     default:
       return launch_router_nt<32, 64>(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux,
-                                      tile_counts, logitsT, flags, st);
+                                      tile_counts, logitsT, flags, z_partials, st);
   }
 #undef MOE_ROUTER_CASE
 }

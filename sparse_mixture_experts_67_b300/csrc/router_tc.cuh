@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kThreads)
                      int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                      float* __restrict__ logits_out, float* __restrict__ probs_out,
                      float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts,
-                     float* __restrict__ logitsT, int flags) {
+                     float* __restrict__ logitsT, int flags, float* __restrict__ z_partials) {
   using C = Cfg<EN>;
   using namespace tc;
   static_assert(C::STAGES <= 16, "barrier arrays");
@@ -204,20 +204,21 @@ __global__ void __launch_bounds__(kThreads)
   router_epilogue<kTok, SUB, C::P>(Sx, C::LDS, tok0, T, E, k, nullptr, idx_out, w_out, logits_out,
                              probs_out, aux_partials ? aux_partials + (size_t)tile0 * E : nullptr,
                              tile_counts, tile0, S.s_m, S.s_inv, S.s_cnt, S.s_part, logitsT,
-                             flags);
+                             flags, z_partials ? z_partials + tile0 : nullptr);
 }
 
 template <int EN, int SUB>
 cudaError_t launch_en(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, int T, int d,
                       int E, int k, int32_t* idx, float* w, float* logits, float* probs, float* aux,
-                      int32_t* tile_counts, float* logitsT, int flags, cudaStream_t st) {
+                      int32_t* tile_counts, float* logitsT, int flags, float* z_partials,
+                      cudaStream_t st) {
   constexpr size_t sm = smem_bytes<EN>();
   static_assert(sm <= 227 * 1024, "router shared memory");
   auto kern = router_tc_kernel<EN, SUB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
   return launch_k(kern, dim3(ceil_div(T, kTok)), dim3(kThreads), sm, st, nullptr, 0, mx, mw, bias, T,
-                  d, E, k, idx, w, logits, probs, aux, tile_counts, logitsT, flags);
+                  d, E, k, idx, w, logits, probs, aux, tile_counts, logitsT, flags, z_partials);
 }
 
 // Which bf16 router runs: the tensor-core one from E > 16 on (measured, events
@@ -241,14 +242,15 @@ inline bool tc_router_enabled(int E) {
 // tokens.  Requires d % 64 == 0 for bf16 (checked by every caller).
 // logitsT (nullable): an [E, T] transposed copy of the logits (expert choice).
 // flags: MOE_ROUTE_NO_RENORM keeps the selected probabilities as the weights.
+// z_partials (nullable): per dispatch tile, the sum of squared log-sum-exps.
 inline cudaError_t launch_router(const void* x, const void* wg, const float* bias, int T, int d,
                                  int E, int k, bool bf16, int32_t* idx, float* w, float* logits,
                                  float* probs, float* aux, cudaStream_t st,
                                  int32_t* tile_counts = nullptr, float* logitsT = nullptr,
-                                 int flags = 0) {
+                                 int flags = 0, float* z_partials = nullptr) {
   if (!bf16 || !rtc::tc_router_enabled(E))
     return launch_router_mma(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st,
-                             tile_counts, logitsT, flags);
+                             tile_counts, logitsT, flags, z_partials);
   const int en = E <= 16 ? 16 : E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256;
   CUtensorMap mx, mw;
   if (!tc::make_map(&mx, x, (uint64_t)T, (uint64_t)d, rtc::kTok) ||
@@ -257,19 +259,19 @@ inline cudaError_t launch_router(const void* x, const void* wg, const float* bia
   switch (en) {
     case 16:
       return rtc::launch_en<16, 32>(mx, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
-                                    tile_counts, logitsT, flags, st);
+                                    tile_counts, logitsT, flags, z_partials, st);
     case 32:
       return rtc::launch_en<32, 64>(mx, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
-                                    tile_counts, logitsT, flags, st);
+                                    tile_counts, logitsT, flags, z_partials, st);
     case 64:
       return rtc::launch_en<64, 64>(mx, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
-                                    tile_counts, logitsT, flags, st);
+                                    tile_counts, logitsT, flags, z_partials, st);
     case 128:
       return rtc::launch_en<128, 64>(mx, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
-                                     tile_counts, logitsT, flags, st);
+                                     tile_counts, logitsT, flags, z_partials, st);
     default:
       return rtc::launch_en<256, 64>(mx, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
-                                     tile_counts, logitsT, flags, st);
+                                     tile_counts, logitsT, flags, z_partials, st);
   }
 }
 

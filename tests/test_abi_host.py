@@ -56,21 +56,21 @@ def _p(v=4096):
 def test_route_argument_errors(L):
     z = _nullp()
     # k > E, E > 256, k < 1, negative T: invalid before any device work
-    assert L.moe_route(_p(), _p(), z, 8, 64, 4, 5, 1, _p(), _p(), z, z, z, 0, z) == 1
-    assert L.moe_route(_p(), _p(), z, 8, 64, 300, 2, 1, _p(), _p(), z, z, z, 0, z) == 1
-    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 0, 1, _p(), _p(), z, z, z, 0, z) == 1
-    assert L.moe_route(_p(), _p(), z, -1, 64, 8, 2, 1, _p(), _p(), z, z, z, 0, z) == 1
+    assert L.moe_route(_p(), _p(), z, 8, 64, 4, 5, 1, _p(), _p(), z, z, z, z, 0, z) == 1
+    assert L.moe_route(_p(), _p(), z, 8, 64, 300, 2, 1, _p(), _p(), z, z, z, z, 0, z) == 1
+    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 0, 1, _p(), _p(), z, z, z, z, 0, z) == 1
+    assert L.moe_route(_p(), _p(), z, -1, 64, 8, 2, 1, _p(), _p(), z, z, z, z, 0, z) == 1
     # null required pointers
-    assert L.moe_route(z, _p(), z, 8, 64, 8, 2, 1, _p(), _p(), z, z, z, 0, z) == 1
-    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 2, 1, z, _p(), z, z, z, 0, z) == 1
+    assert L.moe_route(z, _p(), z, 8, 64, 8, 2, 1, _p(), _p(), z, z, z, z, 0, z) == 1
+    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 2, 1, z, _p(), z, z, z, z, 0, z) == 1
     # bf16 with d not a multiple of 64, unknown dtype, misaligned bf16 pointer
-    assert L.moe_route(_p(), _p(), z, 8, 96, 8, 2, 1, _p(), _p(), z, z, z, 0, z) == 2
-    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 2, 7, _p(), _p(), z, z, z, 0, z) == 2
-    assert L.moe_route(_p(4098), _p(), z, 8, 64, 8, 2, 1, _p(), _p(), z, z, z, 0, z) == 2
+    assert L.moe_route(_p(), _p(), z, 8, 96, 8, 2, 1, _p(), _p(), z, z, z, z, 0, z) == 2
+    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 2, 7, _p(), _p(), z, z, z, z, 0, z) == 2
+    assert L.moe_route(_p(4098), _p(), z, 8, 64, 8, 2, 1, _p(), _p(), z, z, z, z, 0, z) == 2
     # unknown routing flag bits
-    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 2, 1, _p(), _p(), z, z, z, 2, z) == 1
+    assert L.moe_route(_p(), _p(), z, 8, 64, 8, 2, 1, _p(), _p(), z, z, z, z, 2, z) == 1
     # T == 0 is a no-op
-    assert L.moe_route(z, z, z, 0, 64, 8, 2, 1, z, z, z, z, z, 0, z) == 0
+    assert L.moe_route(z, z, z, 0, 64, 8, 2, 1, z, z, z, z, z, z, 0, z) == 0
 
 
 def test_expert_choice_argument_errors(L):
@@ -97,7 +97,7 @@ def test_permute_and_experts_errors(L):
     assert L.moe_combine(_p(), _p(), _p(), 4, 6, 2, _p(), z) == 2
     assert L.moe_combine(z, _p(), _p(), 4, 8, 2, _p(), z) == 1
     assert L.moe_ec_combine(_p(), _p(), _p(), 4, 8, 2, 5, _p(), z) == 1
-    assert L.moe_aux_loss(z, z, _p(), 4, 8, 2, z, z, z, z, z, z) == 1
+    assert L.moe_aux_loss(z, z, _p(), 4, 8, 2, z, z, z, z, z, z, z, z) == 1
 
 
 def test_layer_workspace_and_errors(L):

@@ -93,6 +93,11 @@ def test_router_parity(moe, torch, case, router, monkeypatch):
     assert abs(float(_np(aux["loss"])[0]) - loss_ref) <= 1e-5 * max(1.0, loss_ref)
     f_frac_ref, loss_frac_ref = oracle.aux_stats_fraction(g_ref, idx_ref, E)
     np.testing.assert_allclose(_np(aux["f_frac"]), f_frac_ref, rtol=1e-7, atol=0)
+    auxz = moe.moe_aux_loss(counts, T, k, aux_partials=out["aux_partials"],
+                            z_partials=out["z_partials"])
+    torch.cuda.synchronize()
+    z_ref = oracle.router_z_loss(s_gpu)
+    assert abs(float(_np(auxz["z_loss"])[0]) - z_ref) <= 1e-5 * max(1.0, z_ref)
     assert abs(float(_np(aux["loss_frac"])[0]) - loss_frac_ref) <= 1e-5 * max(1.0, loss_frac_ref)
     aux2 = moe.moe_aux_loss(counts, T, k, probs=out["probs"])
     torch.cuda.synchronize()
@@ -208,7 +213,8 @@ def _topk_outputs(torch, cfg):
             "logits": ((T, E), torch.float32), "counts": ((E,), torch.int32),
             "offsets": ((E + 1,), torch.int32), "f": ((E,), torch.float32),
             "p": ((E,), torch.float32), "loss": ((1,), torch.float32),
-            "f_frac": ((E,), torch.float32), "loss_frac": ((1,), torch.float32)}
+            "f_frac": ((E,), torch.float32), "loss_frac": ((1,), torch.float32),
+            "z_loss": ((1,), torch.float32)}
 
 
 def _check_topk_layer(moe, torch, cfg, sample=None, renormalize=True):
@@ -230,6 +236,8 @@ def _check_topk_layer(moe, torch, cfg, sample=None, renormalize=True):
     f_frac_ref, loss_frac_ref = oracle.aux_stats_fraction(g_g, idx_g, cfg.E)
     np.testing.assert_allclose(_np(outs["f_frac"]), f_frac_ref, rtol=1e-6, atol=0)
     assert abs(float(_np(outs["loss_frac"])[0]) - loss_frac_ref) <= 1e-4 * max(1.0, loss_frac_ref)
+    z_ref = oracle.router_z_loss(s_gpu)
+    assert abs(float(_np(outs["z_loss"])[0]) - z_ref) <= 1e-5 * max(1.0, z_ref)
     # end-to-end routing against fp64 logits
     s64 = oracle.router_logits(x64, synth.to_f64(inp.w_g), inp.bias)
     idx64, w64, g64 = oracle.topk_route(s64, cfg.k, renormalize=renormalize)
