@@ -21,7 +21,10 @@
  *   - Weights use the nn.Linear layout: W_g [E,d]; W_gate, W_up [E,F,d]
  *     (K-major rows); W_down [E,d,F].
  *   - T == 0 (or R == 0) is a valid no-op.
- *   - Errors are reported by the return value; on any error nothing is enqueued.
+ *   - Errors are reported by the return value.  Arguments are checked before
+ *     the first launch, so on MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED and
+ *     MOE_ERR_WORKSPACE nothing is enqueued; after MOE_ERR_CUDA earlier stages
+ *     of the same call may have been enqueued and the outputs are undefined.
  *       MOE_ERR_INVALID_ARG  null required pointer, negative size, k < 1,
  *                            k > E, E > 256, capacity C > T, capacity_factor <= 0
  *       MOE_ERR_UNSUPPORTED  dtype/shape/alignment outside what the kernels take

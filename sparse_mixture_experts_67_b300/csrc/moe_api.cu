@@ -285,7 +285,15 @@ moe_status moe_grouped_down(const void* h, const int32_t* offsets, const void* w
 moe_status moe_experts_swiglu(const void* x_perm, const int32_t* offsets, const void* w_gate,
                               const void* w_up, const void* w_down, int R, int d, int F, int E,
                               moe_dtype dt, void* h, float* y_perm, moe_stream_t stream) {
-  moe_status st = moe_grouped_gateup_swiglu(x_perm, offsets, w_gate, w_up, R, d, F, E, dt, h, stream);
+  // every argument of both stages is checked before the first one is enqueued
+  moe_status st = check_experts(R, d, F, E, dt);
+  if (st != MOE_OK || R == 0) return st;
+  if (!x_perm || !offsets || !w_gate || !w_up || !w_down || !h || !y_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x_perm) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(h) || !aligned16(y_perm))
+    return MOE_ERR_UNSUPPORTED;
+  st = moe_grouped_gateup_swiglu(x_perm, offsets, w_gate, w_up, R, d, F, E, dt, h, stream);
   if (st != MOE_OK) return st;
   return moe_grouped_down(h, offsets, w_down, R, d, F, E, dt, y_perm, stream);
 }
@@ -397,6 +405,11 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   if (st != MOE_OK) return st;
   if (D.T == 0) return MOE_OK;
   if (!x || !y || !w->w_g || !w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+  // alignment of every caller pointer a stage reads in 16-byte vectors or TMA
+  // boxes, checked here so that an error never leaves earlier stages enqueued
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w->w_gate) || !aligned16(w->w_up) ||
+      !aligned16(w->w_down) || (D.dtype == MOE_BF16 && !aligned16(w->w_g)))
+    return MOE_ERR_UNSUPPORTED;
   const size_t need = moe_layer_workspace_size(desc);
   if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
   moe_layer_outputs none;
@@ -461,7 +474,6 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   if (O.offsets) offsets = O.offsets;
   st = check_permute(x, x_perm, D.T, D.d, D.E, k, D.dtype, counts, offsets);
   if (st != MOE_OK) return st;
-  if (D.dtype == MOE_BF16 && (!aligned16(x) || !aligned16(w->w_g))) return MOE_ERR_UNSUPPORTED;
   // router CTAs double as dispatch tiles: the router writes the per-tile counts
   const int tile = router_tokens(D.E) * k;
   const int tiles = dispatch_tiles((long long)A, tile);
@@ -474,7 +486,6 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
     return MOE_ERR_CUDA;
   // k <= 2 (bf16): the down GEMM accumulates the combine into y, zeroed by the scatter
   const bool fused_combine = D.dtype == MOE_BF16 && k <= 2;
-  if (fused_combine && (!aligned16(w->w_down) || !aligned16(y))) return MOE_ERR_UNSUPPORTED;
   // the scatter also copies the x rows into dispatch order: contiguous row blocks
   // keep the gate/up operand loads full-width TMA boxes (gathering rows inside
   // the GEMM re-fetches them once per n-block and measured several times slower)

@@ -136,3 +136,47 @@ def test_no_cpu_fallback_without_device():
     x = torch.zeros(4, 64)
     with pytest.raises(moe.MoEError):
         moe.moe_route(x, torch.zeros(8, 64), None, 2)
+
+
+def test_alignment_checked_before_any_launch(L):
+    """A misaligned caller pointer is MOE_ERR_UNSUPPORTED from the argument checks.
+    Without a device any launch would fail with MOE_ERR_CUDA (4), so a 2 here also
+    shows that no stage was enqueued before the check.  The pointers are not real
+    allocations, so this runs only where no CUDA device is visible."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("uses placeholder pointers: host-only check")
+    z = _nullp()
+    d = moe._Desc(64, 1024, 4096, 8, 2, 0, 0.0, 1)
+    ws = L.moe_layer_workspace_size(ctypes.byref(d))
+    good = dict(w_g=4096, bias=0, w_gate=4096, w_up=4096, w_down=4096)
+    # aligned pointers reach the first launch, which fails without a device
+    assert L.moe_layer_forward(ctypes.byref(d), ctypes.byref(moe._Weights(*good.values())), _p(),
+                               _p(), None, _p(), ws, z) == 4
+    for field in ("w_g", "w_gate", "w_up", "w_down"):
+        w = moe._Weights(*dict(good, **{field: 4104}).values())
+        assert L.moe_layer_forward(ctypes.byref(d), ctypes.byref(w), _p(), _p(), None, _p(), ws,
+                                   z) == 2, field
+    w = moe._Weights(*good.values())
+    assert L.moe_layer_forward(ctypes.byref(d), ctypes.byref(w), _p(4104), _p(), None, _p(), ws, z) == 2
+    assert L.moe_layer_forward(ctypes.byref(d), ctypes.byref(w), _p(), _p(4104), None, _p(), ws, z) == 2
+    # the same for expert choice and for the k > 2 path (separate combine)
+    ec = moe._Desc(64, 1024, 4096, 8, 0, 1, 2.0, 1)
+    ws_ec = L.moe_layer_workspace_size(ctypes.byref(ec))
+    assert L.moe_layer_forward(ctypes.byref(ec), ctypes.byref(w), _p(), _p(4104), None, _p(), ws_ec,
+                               z) == 2
+    k4 = moe._Desc(64, 1024, 4096, 8, 4, 0, 0.0, 1)
+    ws4 = L.moe_layer_workspace_size(ctypes.byref(k4))
+    w_bad_down = moe._Weights(*dict(good, w_down=4104).values())
+    assert L.moe_layer_forward(ctypes.byref(k4), ctypes.byref(w_bad_down), _p(), _p(), None, _p(),
+                               ws4, z) == 2
+    # both expert GEMMs' arguments are checked before the first one is enqueued
+    args = [_p(), _p(), _p(), _p(), _p(), 256, 1024, 4096, 8, 1, _p(), _p(), z]
+    assert L.moe_experts_swiglu(*args) == 4
+    for i in (4, 11):  # w_down, y_perm
+        bad = list(args)
+        bad[i] = _p(4104)
+        assert L.moe_experts_swiglu(*bad) == 2, i
+    missing = list(args)
+    missing[4] = z
+    assert L.moe_experts_swiglu(*missing) == 1
