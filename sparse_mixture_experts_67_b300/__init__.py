@@ -11,6 +11,7 @@ device the calls raise.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import re
 from typing import Dict, List, Optional
@@ -135,6 +136,29 @@ def _dev(*ts: Optional[torch.Tensor]) -> None:
             raise MoEError("argument check (tensor not contiguous)", 1)
 
 
+def _bad(what: str) -> MoEError:
+    return MoEError(f"argument check ({what})", 1)
+
+
+def _dims(t: torch.Tensor, ndim: int, name: str) -> None:
+    if t.dim() != ndim:
+        raise _bad(f"{name} must be {ndim}-D, got shape {tuple(t.shape)}")
+
+
+def _expect(t: Optional[torch.Tensor], name: str, dtype: Optional[torch.dtype] = None,
+            shape=None, min_numel: Optional[int] = None) -> None:
+    """Checks one tensor against the sizes and types the library is told about, so
+    that no kernel reads or writes past a buffer (None passes: optional argument)."""
+    if t is None:
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise _bad(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise _bad(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise _bad(f"{name} has {t.numel()} elements, needs at least {min_numel}")
+
+
 def _dtype(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return MOE_BF16
@@ -168,12 +192,21 @@ def moe_expert_choice_capacity(T: int, E: int, capacity_factor: float) -> int:
     return int(lib().moe_expert_choice_capacity(T, E, capacity_factor))
 
 
+def _check_router_args(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[torch.Tensor]) -> None:
+    _dims(x, 2, "x")
+    _dims(w_g, 2, "w_g")
+    E, d = w_g.shape[0], x.shape[1]
+    _expect(w_g, "w_g", dtype=x.dtype, shape=(E, d))
+    _expect(bias, "bias", dtype=torch.float32, shape=(E,))
+    _dev(x, w_g, bias)
+
+
 def moe_route(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[torch.Tensor], k: int,
               want_logits: bool = False, want_probs: bool = False,
               want_aux: bool = True, renormalize: bool = True) -> Dict[str, torch.Tensor]:
     """Top-k router: returns topk_idx [T,k] int32, topk_w [T,k] fp32 and the optional outputs.
     renormalize=False keeps the selected probabilities as the weights (MOE_ROUTE_NO_RENORM)."""
-    _dev(x, w_g, bias)
+    _check_router_args(x, w_g, bias)
     T, d = x.shape
     E = w_g.shape[0]
     out = {"topk_idx": _empty((T, k), torch.int32, x), "topk_w": _empty((T, k), torch.float32, x)}
@@ -195,7 +228,7 @@ def moe_route(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[torch.Tensor], 
 def moe_expert_choice_route(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[torch.Tensor],
                             capacity_factor: float) -> Dict[str, torch.Tensor]:
     """Expert-choice router: ec_idx [E,C], ec_score [E,C], pos [E,T], logits [T,E]."""
-    _dev(x, w_g, bias)
+    _check_router_args(x, w_g, bias)
     T, d = x.shape
     E = w_g.shape[0]
     C = moe_expert_choice_capacity(T, E, capacity_factor)
@@ -210,9 +243,17 @@ def moe_expert_choice_route(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[t
     return out
 
 
+def _check_permute_args(x: torch.Tensor, topk_idx: torch.Tensor, device: bool = True) -> None:
+    _dims(x, 2, "x")
+    _dims(topk_idx, 2, "topk_idx")
+    _expect(topk_idx, "topk_idx", dtype=torch.int32, shape=(x.shape[0], topk_idx.shape[1]))
+    if device:
+        _dev(x, topk_idx)
+
+
 def moe_permute(x: torch.Tensor, topk_idx: torch.Tensor, E: int) -> Dict[str, torch.Tensor]:
     """Stable dispatch: x_perm [T*k,d], counts [E], offsets [E+1], perm, inv_perm [T*k]."""
-    _dev(x, topk_idx)
+    _check_permute_args(x, topk_idx)
     T, d = x.shape
     k = topk_idx.shape[1]
     A = T * k
@@ -235,7 +276,7 @@ def moe_permute_noalloc(x: torch.Tensor, topk_idx: torch.Tensor, E: int,
     ``out`` may hold preallocated x_perm, counts, offsets, perm, inv_perm tensors
     (missing ones are created here with torch).
     """
-    _dev(x, topk_idx)
+    _check_permute_args(x, topk_idx, device=False)
     T, d = x.shape
     k = topk_idx.shape[1]
     A = T * k
@@ -244,9 +285,11 @@ def moe_permute_noalloc(x: torch.Tensor, topk_idx: torch.Tensor, E: int,
               "inv_perm": ((A,), torch.int32)}
     res = dict(out or {})
     for name, (shape, dtype) in shapes.items():
+        _expect(res.get(name), name, dtype=dtype, min_numel=math.prod(shape))
+    _dev(x, topk_idx, *res.values())
+    for name, (shape, dtype) in shapes.items():
         if name not in res:
             res[name] = _empty(shape, dtype, x)
-        _dev(res[name])
     _check("moe_permute_noalloc", lib().moe_permute_noalloc(
         _ptr(x), _ptr(topk_idx), T, d, E, k, _dtype(x), _ptr(res["x_perm"]), _ptr(res["counts"]),
         _ptr(res["offsets"]), _ptr(res["perm"]), _ptr(res["inv_perm"]), _stream()))
@@ -254,6 +297,8 @@ def moe_permute_noalloc(x: torch.Tensor, topk_idx: torch.Tensor, E: int,
 
 
 def moe_gather_rows(x: torch.Tensor, src: torch.Tensor, div: int) -> torch.Tensor:
+    _dims(x, 2, "x")
+    _expect(src, "src", dtype=torch.int32)
     _dev(x, src)
     T, d = x.shape
     R = src.numel()
@@ -263,11 +308,23 @@ def moe_gather_rows(x: torch.Tensor, src: torch.Tensor, div: int) -> torch.Tenso
     return out
 
 
+def _check_gateup_args(x: torch.Tensor, offsets: torch.Tensor, w_gate: torch.Tensor,
+                       w_up: torch.Tensor) -> None:
+    _dims(x, 2, "x")
+    _dims(w_gate, 3, "w_gate")
+    E, F = w_gate.shape[0], w_gate.shape[1]
+    _expect(w_gate, "w_gate", dtype=x.dtype, shape=(E, F, x.shape[1]))
+    _expect(w_up, "w_up", dtype=x.dtype, shape=(E, F, x.shape[1]))
+    _expect(offsets, "offsets", dtype=torch.int32, min_numel=E + 1)
+
+
 def moe_grouped_gateup_swiglu(x_perm: torch.Tensor, offsets: torch.Tensor, w_gate: torch.Tensor,
                               w_up: torch.Tensor, h: Optional[torch.Tensor] = None) -> torch.Tensor:
-    _dev(x_perm, offsets, w_gate, w_up, h)
+    _check_gateup_args(x_perm, offsets, w_gate, w_up)
     R, d = x_perm.shape
     E, F, _ = w_gate.shape
+    _expect(h, "h", dtype=x_perm.dtype, min_numel=R * F)
+    _dev(x_perm, offsets, w_gate, w_up, h)
     if h is None:
         h = _empty((R, F), x_perm.dtype, x_perm)
     _check("moe_grouped_gateup_swiglu", lib().moe_grouped_gateup_swiglu(
@@ -280,6 +337,8 @@ def moe_grouped_gateup_swiglu_gather(x: torch.Tensor, src: torch.Tensor, div: in
                                      offsets: torch.Tensor, w_gate: torch.Tensor,
                                      w_up: torch.Tensor) -> torch.Tensor:
     """Gate/up + SwiGLU reading row r of the grouped input from x[src[r] // div]."""
+    _check_gateup_args(x, offsets, w_gate, w_up)
+    _expect(src, "src", dtype=torch.int32)
     _dev(x, src, offsets, w_gate, w_up)
     T, d = x.shape
     R = src.numel()
@@ -293,9 +352,14 @@ def moe_grouped_gateup_swiglu_gather(x: torch.Tensor, src: torch.Tensor, div: in
 
 def moe_grouped_down(h: torch.Tensor, offsets: torch.Tensor, w_down: torch.Tensor,
                      y_perm: Optional[torch.Tensor] = None) -> torch.Tensor:
-    _dev(h, offsets, w_down, y_perm)
+    _dims(h, 2, "h")
+    _dims(w_down, 3, "w_down")
     R, F = h.shape
     E, d, _ = w_down.shape
+    _expect(w_down, "w_down", dtype=h.dtype, shape=(E, d, F))
+    _expect(offsets, "offsets", dtype=torch.int32, min_numel=E + 1)
+    _expect(y_perm, "y_perm", dtype=torch.float32, min_numel=R * d)
+    _dev(h, offsets, w_down, y_perm)
     if y_perm is None:
         y_perm = _empty((R, d), torch.float32, h)
     _check("moe_grouped_down", lib().moe_grouped_down(
@@ -305,9 +369,11 @@ def moe_grouped_down(h: torch.Tensor, offsets: torch.Tensor, w_down: torch.Tenso
 
 def moe_experts_swiglu(x_perm: torch.Tensor, offsets: torch.Tensor, w_gate: torch.Tensor,
                        w_up: torch.Tensor, w_down: torch.Tensor):
-    _dev(x_perm, offsets, w_gate, w_up, w_down)
+    _check_gateup_args(x_perm, offsets, w_gate, w_up)
     R, d = x_perm.shape
     E, F, _ = w_gate.shape
+    _expect(w_down, "w_down", dtype=x_perm.dtype, shape=(E, d, F))
+    _dev(x_perm, offsets, w_gate, w_up, w_down)
     h = _empty((R, F), x_perm.dtype, x_perm)
     y_perm = _empty((R, d), torch.float32, x_perm)
     _check("moe_experts_swiglu", lib().moe_experts_swiglu(
@@ -317,8 +383,13 @@ def moe_experts_swiglu(x_perm: torch.Tensor, offsets: torch.Tensor, w_gate: torc
 
 
 def moe_combine(y_perm: torch.Tensor, inv_perm: torch.Tensor, topk_w: torch.Tensor) -> torch.Tensor:
-    _dev(y_perm, inv_perm, topk_w)
+    _dims(y_perm, 2, "y_perm")
+    _dims(topk_w, 2, "topk_w")
     T, k = topk_w.shape
+    _expect(y_perm, "y_perm", dtype=torch.float32)
+    _expect(topk_w, "topk_w", dtype=torch.float32)
+    _expect(inv_perm, "inv_perm", dtype=torch.int32, min_numel=T * k)
+    _dev(y_perm, inv_perm, topk_w)
     d = y_perm.shape[1]
     y = _empty((T, d), torch.float32, y_perm)
     _check("moe_combine", lib().moe_combine(_ptr(y_perm), _ptr(inv_perm), _ptr(topk_w), T, d, k,
@@ -327,9 +398,15 @@ def moe_combine(y_perm: torch.Tensor, inv_perm: torch.Tensor, topk_w: torch.Tens
 
 
 def moe_ec_combine(y_perm: torch.Tensor, pos: torch.Tensor, ec_score: torch.Tensor) -> torch.Tensor:
-    _dev(y_perm, pos, ec_score)
+    _dims(y_perm, 2, "y_perm")
+    _dims(pos, 2, "pos")
+    _dims(ec_score, 2, "ec_score")
     E, T = pos.shape
     C = ec_score.shape[1]
+    _expect(pos, "pos", dtype=torch.int32)
+    _expect(ec_score, "ec_score", dtype=torch.float32, shape=(E, C))
+    _expect(y_perm, "y_perm", dtype=torch.float32, min_numel=E * C * y_perm.shape[1])
+    _dev(y_perm, pos, ec_score)
     d = y_perm.shape[1]
     y = _empty((T, d), torch.float32, pos)
     _check("moe_ec_combine", lib().moe_ec_combine(_ptr(y_perm), _ptr(pos), _ptr(ec_score), T, d, E,
@@ -343,8 +420,13 @@ def moe_aux_loss(counts: torch.Tensor, T: int, k: int, aux_partials: Optional[to
     """f [E], p [E], loss [1] from router partial sums (or from probs [T,E]), and the
     fraction-of-assignments convention f_frac [E] = counts / (T k), loss_frac [1] = loss / k;
     with z_partials (from moe_route) also the router z-loss z_loss [1]."""
-    _dev(counts, aux_partials, probs, z_partials)
     E = counts.numel()
+    rows = moe_route_aux_rows(T) if T > 0 else 0
+    _expect(counts, "counts", dtype=torch.int32)
+    _expect(aux_partials, "aux_partials", dtype=torch.float32, min_numel=rows * E)
+    _expect(probs, "probs", dtype=torch.float32, min_numel=T * E)
+    _expect(z_partials, "z_partials", dtype=torch.float32, min_numel=rows)
+    _dev(counts, aux_partials, probs, z_partials)
     if probs is not None and aux_partials is None:
         aux_partials = _empty((max(1, moe_route_aux_rows(T)), E), torch.float32, counts)
     out = {"f": _empty((E,), torch.float32, counts), "p": _empty((E,), torch.float32, counts),
@@ -370,6 +452,21 @@ def moe_layer_workspace_size(T: int, d: int, F: int, E: int, k: int, routing: in
     return int(lib().moe_layer_workspace_size(ctypes.byref(desc)))
 
 
+def _output_sizes(T: int, E: int, k: int, routing: int, capacity_factor: float):
+    """dtype and element count of each optional moe_layer_forward output (fields the
+    routing mode does not write need no room)."""
+    topk = routing == MOE_ROUTING_TOPK
+    kk = k if topk else 0
+    C = max(moe_expert_choice_capacity(T, E, capacity_factor), 0) if not topk else 0
+    i32, f32 = torch.int32, torch.float32
+    t = 1 if topk else 0
+    return {"topk_idx": (i32, T * kk), "topk_w": (f32, T * kk), "logits": (f32, T * E),
+            "counts": (i32, E * t), "offsets": (i32, (E + 1) * t), "f": (f32, E * t),
+            "p": (f32, E * t), "loss": (f32, t), "ec_idx": (i32, E * C), "ec_score": (f32, E * C),
+            "pos": (i32, E * T * (1 - t)), "f_frac": (f32, E * t), "loss_frac": (f32, t),
+            "dropped": (i32, t), "z_loss": (f32, t)}
+
+
 def moe_layer_forward(x: torch.Tensor, weights: Dict[str, torch.Tensor], k: int = 2,
                       routing: int = MOE_ROUTING_TOPK, capacity_factor: float = 0.0,
                       outputs: Optional[Dict[str, torch.Tensor]] = None,
@@ -382,13 +479,26 @@ def moe_layer_forward(x: torch.Tensor, weights: Dict[str, torch.Tensor], k: int 
     (MOE_ROUTE_CAPACITY); outputs["dropped"] ([1] int32) receives the number dropped."""
     w_g, bias = weights["w_g"], weights.get("bias")
     w_gate, w_up, w_down = weights["w_gate"], weights["w_up"], weights["w_down"]
-    _dev(x, w_g, bias, w_gate, w_up, w_down, y, workspace)
+    _dims(x, 2, "x")
+    _dims(w_gate, 3, "w_gate")
     T, d = x.shape
     E, F, _ = w_gate.shape
+    _expect(w_g, "w_g", dtype=x.dtype, shape=(E, d))
+    _expect(bias, "bias", dtype=torch.float32, shape=(E,))
+    _expect(w_gate, "w_gate", dtype=x.dtype, shape=(E, F, d))
+    _expect(w_up, "w_up", dtype=x.dtype, shape=(E, F, d))
+    _expect(w_down, "w_down", dtype=x.dtype, shape=(E, d, F))
+    _expect(y, "y", dtype=torch.float32, min_numel=T * d)
+    sizes = _output_sizes(T, E, k, routing, capacity_factor)
+    for name, t in (outputs or {}).items():
+        if name not in sizes:
+            raise _bad(f"unknown output {name!r}; expected one of {sorted(sizes)}")
+        _expect(t, name, dtype=sizes[name][0], min_numel=sizes[name][1])
+    _dev(x, w_g, bias, w_gate, w_up, w_down, y, workspace)
     flags = (0 if renormalize else MOE_ROUTE_NO_RENORM) | (MOE_ROUTE_CAPACITY if capacity else 0)
     desc = _desc(T, d, F, E, k, routing, capacity_factor, _dtype(x), flags)
     need = int(lib().moe_layer_workspace_size(ctypes.byref(desc)))
-    if workspace is None or workspace.numel() < need:
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = _empty((max(need, 1),), torch.uint8, x)
     if y is None:
         y = _empty((T, d), torch.float32, x)
@@ -400,7 +510,7 @@ def moe_layer_forward(x: torch.Tensor, weights: Dict[str, torch.Tensor], k: int 
                    w_gate.data_ptr(), w_up.data_ptr(), w_down.data_ptr())
     _check("moe_layer_forward", lib().moe_layer_forward(
         ctypes.byref(desc), ctypes.byref(wts), _ptr(x), _ptr(y), ctypes.byref(outs), _ptr(workspace),
-        workspace.numel(), _stream()))
+        workspace.numel() * workspace.element_size(), _stream()))
     return y
 
 
