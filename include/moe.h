@@ -21,6 +21,12 @@
  *   - Weights use the nn.Linear layout: W_g [E,d]; W_gate, W_up [E,F,d]
  *     (K-major rows); W_down [E,d,F].
  *   - T == 0 (or R == 0) is a valid no-op.
+ *   - Index tensors are device data the host never reads, so they are not
+ *     checked: topk_idx values must lie in [0, E), offsets must be
+ *     non-decreasing with offsets[E] <= R, gather sources in [0, T*div),
+ *     inv_perm values in [0, R) or -1, pos values in [0, E*C) or -1.  Values
+ *     outside these ranges are undefined behaviour (out-of-bounds accesses).
+ *     The layer call produces all of them itself and is not exposed to this.
  *   - Errors are reported by the return value.  Arguments are checked before
  *     the first launch, so on MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED and
  *     MOE_ERR_WORKSPACE nothing is enqueued; after MOE_ERR_CUDA earlier stages
