@@ -262,6 +262,40 @@ def pin_router_z_loss(orc):
     assert abs(orc.router_z_loss(s) - ref) <= 1e-12 * ref
 
 
+def pin_softmax_large_logits(orc):
+    """Softmax is unchanged by adding a constant to a row, also where exp alone would
+    overflow or underflow in fp64: [a, a-1, a-10] gives [1, e^-1, e^-10] / (1 + e^-1 + e^-10)
+    for every a (the max-subtracted form; router and expert-choice scores alike)."""
+    ref = np.array([1.0, math.exp(-1.0), math.exp(-10.0)])
+    ref /= ref.sum()
+    for a in (0.0, 1000.0, -1000.0):
+        s = np.array([[a, a - 1.0, a - 10.0]])
+        np.testing.assert_allclose(orc.softmax(s, axis=1)[0], ref, rtol=1e-14, atol=0)
+        _, w, g = orc.topk_route(s, 3)
+        np.testing.assert_allclose(g[0], ref, rtol=1e-14, atol=0)
+        _, _, sc, _ = orc.expert_choice_route(s.T.copy(), 1.0)  # 3 tokens, one expert, C = 3
+        np.testing.assert_allclose(sc[0], ref, rtol=1e-14, atol=0)
+
+
+def pin_capacity_rounding(orc):
+    """Both capacities truncate as Python int() does on the pages ([sparse-moe]
+    ExpertChoiceGating: int(T * capacity_factor / E); [zh-moe] expert_capacity_routing:
+    int(T / E * capacity_factor * top_k)).  Values worked by hand where the quotient is
+    not an integer: 10*1/4 = 2.5 -> 2, 7*0.5/2 = 1.75 -> 1, 10*0.3/4 = 0.75 -> 0,
+    10/3*1.25*2 = 8.33 -> 8, 7/2*1*1 = 3.5 -> 3, 9/4*1.5*2 = 6.75 -> 6."""
+    assert orc.expert_choice_capacity(10, 4, 1.0) == 2
+    assert orc.expert_choice_capacity(7, 2, 0.5) == 1
+    assert orc.expert_choice_capacity(10, 4, 0.3) == 0
+    assert orc.expert_choice_capacity(8192, 16, 2.0) == 1024
+    assert orc.token_capacity(10, 3, 1.25, 2) == 8
+    assert orc.token_capacity(7, 2, 1.0, 1) == 3
+    assert orc.token_capacity(9, 4, 1.5, 2) == 6
+    s = np.zeros((10, 4))  # all ties: the route takes C tokens per expert
+    C, ec_idx, _, _ = orc.expert_choice_route(s, 1.0)
+    assert C == 2 and ec_idx.shape == (4, 2)
+    assert orc.capacity_route(np.zeros((7, 2)), 1, 1.0)[5] == 3
+
+
 def pin_bias_only(orc):
     """x = 0: the logits are the bias ([zh-moe] GatingNetwork adds b)."""
     b = np.array([1.5 * math.log(1.0 / (e + 1)) for e in range(6)])
@@ -590,6 +624,87 @@ def _z_loss_max_only(s):
     return float(np.mean(np.max(s, axis=1) ** 2))
 
 
+def _softmax_no_max(s, axis=-1):
+    with np.errstate(over="ignore", invalid="ignore", under="ignore"):
+        z = np.exp(s)
+        return z / np.sum(z, axis=axis, keepdims=True)
+
+
+def _ec_capacity_ceil(T, E, cf):
+    return int(math.ceil(T * cf / E))
+
+
+def _token_capacity_ceil(T, E, cf, k):
+    return int(math.ceil(T / E * cf * k))
+
+
+def _ec_ties_to_higher_token(s, cf):
+    T, E = s.shape
+    C = oracle.expert_choice_capacity(T, E, cf)
+    scores = oracle.softmax(s.T, axis=1)
+    ec_idx = np.zeros((E, C), np.int64)
+    ec_score = np.zeros((E, C))
+    pos = np.full((E, T), -1, np.int64)
+    for e in range(E):
+        order = (T - 1 - np.argsort(-s[::-1, e], kind="stable"))[:C]
+        ec_idx[e], ec_score[e] = order, scores[e, order]
+        pos[e, order] = e * C + np.arange(C)
+    return C, ec_idx, ec_score, pos
+
+
+def _ec_combine_renormalised(x, ec_idx, ec_score, experts, round_h=None):
+    E, C = ec_idx.shape
+    tot = np.zeros(x.shape[0])
+    for e in range(E):
+        tot[ec_idx[e]] += ec_score[e]
+    y = np.zeros((x.shape[0], x.shape[1]))
+    for e in range(E):
+        if C:
+            out = oracle.swiglu_expert(x[ec_idx[e]], *experts[e], round_h=round_h)
+            y[ec_idx[e]] += (ec_score[e] / tot[ec_idx[e]])[:, None] * out
+    return y
+
+
+def _ec_combine_unweighted(x, ec_idx, ec_score, experts, round_h=None):
+    return oracle.expert_choice_forward(x, ec_idx, np.ones_like(ec_score), experts, round_h)
+
+
+def _dispatch_offsets_inclusive(idx, E):
+    counts, _, perm, inv = oracle.dispatch(idx, E)
+    return counts, np.concatenate([np.cumsum(counts), [counts.sum()]]), perm, inv
+
+
+def _bf16_truncates(a):
+    m, ex = np.frexp(np.asarray(a, np.float64))
+    return np.ldexp(np.trunc(m * 256.0) / 256.0, ex)
+
+
+def _dense_uniform(x, g, experts):
+    return oracle.dense_mixture(x, np.full_like(g, 1.0 / g.shape[1]), experts)
+
+
+def _p_from_combine_weights(g, idx, E):
+    T, k = idx.shape
+    counts, f, _, _ = oracle.aux_stats(g, idx, E)
+    p = np.zeros(E)
+    for t in range(T):
+        sel = g[t, idx[t]]
+        for j in range(k):
+            p[idx[t, j]] += sel[j] / sel.sum() / T
+    return counts, f, p, float(E * np.sum(f * p))
+
+
+def _forward_last_slot_only(x, idx, w, experts, round_h=None):
+    w2 = np.zeros_like(w)
+    w2[:, -1] = w[:, -1]
+    return oracle.moe_forward(x, idx, w2, experts, round_h)
+
+
+def _experts_reversed(x, w_g, bias=None):
+    s = (np.asarray(x, np.float64) @ np.asarray(w_g, np.float64).T)[:, ::-1].copy()
+    return s if bias is None else s + np.asarray(bias, np.float64)[None, :]
+
+
 def _silu_sign(a):
     return a / (1.0 + np.exp(a))
 
@@ -618,6 +733,18 @@ MUTANTS = {
     "capacity_kept_not_renormalised": dict(capacity_route=_capacity_no_renorm),
     "z_loss_not_squared": dict(router_z_loss=_z_loss_unsquared),
     "z_loss_max_instead_of_logsumexp": dict(router_z_loss=_z_loss_max_only),
+    "softmax_without_max_subtraction": dict(softmax=_softmax_no_max),
+    "ec_capacity_rounded_up": dict(expert_choice_capacity=_ec_capacity_ceil),
+    "token_capacity_rounded_up": dict(token_capacity=_token_capacity_ceil),
+    "ec_ties_to_higher_token": dict(expert_choice_route=_ec_ties_to_higher_token),
+    "ec_combine_renormalised": dict(expert_choice_forward=_ec_combine_renormalised),
+    "ec_combine_ignores_scores": dict(expert_choice_forward=_ec_combine_unweighted),
+    "dispatch_offsets_inclusive": dict(dispatch=_dispatch_offsets_inclusive),
+    "bf16_round_truncates": dict(bf16_round=_bf16_truncates),
+    "dense_mixture_uniform": dict(dense_mixture=_dense_uniform),
+    "p_from_combine_weights": dict(aux_stats=_p_from_combine_weights),
+    "forward_last_slot_only": dict(moe_forward=_forward_last_slot_only),
+    "router_experts_reversed": dict(router_logits=_experts_reversed),
 }
 
 
