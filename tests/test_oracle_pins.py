@@ -424,6 +424,35 @@ def pin_single_slot_selects_expert(orc):
                                    rtol=1e-13, atol=1e-13)
 
 
+def pin_forward_takes_weights_as_given(orc):
+    """The combine uses the weights it is handed, unrenormalised ([moe-intro] y = sum of
+    g_i E_i(x) over the top k): one-hot slot weights return that slot's expert, weights
+    summing to 0.3 or 2.5 give the per-token weighted sum of the slots' experts, and the
+    output is linear in the weights."""
+    rng = np.random.default_rng(12)
+    T, d, F, E, k = 9, 4, 6, 4, 3
+    x = rng.normal(size=(T, d))
+    experts = _rand_experts(rng, E, d, F)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    outs = [[orc.swiglu_expert(x[t:t + 1], *experts[idx[t, j]])[0] for j in range(k)]
+            for t in range(T)]
+    for j in range(k):
+        one_hot = np.zeros((T, k))
+        one_hot[:, j] = 1.0
+        y = orc.moe_forward(x, idx, one_hot, experts)
+        for t in range(T):
+            np.testing.assert_allclose(y[t], outs[t][j], rtol=1e-13, atol=1e-13)
+    for total in (0.3, 2.5):
+        w = rng.uniform(0.1, 1.0, (T, k))
+        w *= total / w.sum(axis=1, keepdims=True)
+        y = orc.moe_forward(x, idx, w, experts)
+        for t in range(T):
+            ref = sum(w[t, j] * outs[t][j] for j in range(k))
+            np.testing.assert_allclose(y[t], ref, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(orc.moe_forward(x, idx, 3.0 * w, experts), 3.0 * y,
+                                   rtol=1e-12, atol=1e-13)
+
+
 def pin_expert_choice_invariants(orc):
     rng = np.random.default_rng(12)
     for T, E, cf in ((30, 4, 1.0), (64, 16, 2.0), (9, 3, 0.25), (16, 4, 4.0)):
@@ -705,6 +734,83 @@ def _experts_reversed(x, w_g, bias=None):
     return s if bias is None else s + np.asarray(bias, np.float64)[None, :]
 
 
+def _z_loss_summed(s):
+    m = np.max(s, axis=1)
+    return float(np.sum((m + np.log(np.sum(np.exp(s - m[:, None]), axis=1))) ** 2))
+
+
+def _z_loss_without_max_back(s):
+    m = np.max(s, axis=1)
+    return float(np.mean(np.log(np.sum(np.exp(s - m[:, None]), axis=1)) ** 2))
+
+
+def _fraction_loss_without_E(g, idx, E):
+    f, loss = oracle.aux_stats_fraction(g, idx, E)
+    return f, loss / E
+
+
+def _topk_slots_ascending(s, k, renormalize=True):
+    idx, w, g = oracle.topk_route(s, k, renormalize)
+    return idx[:, ::-1].copy(), w[:, ::-1].copy(), g
+
+
+def _dispatch_perm_inv_swapped(idx, E):
+    counts, offsets, perm, inv = oracle.dispatch(idx, E)
+    return counts, offsets, inv, perm
+
+
+def _ec_pos_local(s, cf):
+    C, ec_idx, ec_score, pos = oracle.expert_choice_route(s, cf)
+    pos = pos.copy()
+    for e in range(s.shape[1]):
+        pos[e, pos[e] >= 0] -= e * C
+    return C, ec_idx, ec_score, pos
+
+
+def _ec_picks_ascending(s, cf):
+    C, ec_idx, ec_score, pos = oracle.expert_choice_route(s, cf)
+    ec_idx, ec_score = ec_idx[:, ::-1].copy(), ec_score[:, ::-1].copy()
+    pos = np.full_like(pos, -1)
+    for e in range(s.shape[1]):
+        pos[e, ec_idx[e]] = e * C + np.arange(C)
+    return C, ec_idx, ec_score, pos
+
+
+def _glu_without_silu(x, wg, wu, wd, round_h=None):
+    h = (x @ np.asarray(wg, np.float64).T) * (x @ np.asarray(wu, np.float64).T)
+    h = h if round_h is None else round_h(h)
+    return h @ np.asarray(wd, np.float64).T
+
+
+def _capacity_load_counts_drops(s, k, cf):
+    idx, w, kept, dropped, _, cap = oracle.capacity_route(s, k, cf)
+    return idx, w, kept, dropped, np.bincount(idx.ravel(), minlength=s.shape[1]), cap
+
+
+def _capacity_weights_of_all_slots(s, k, cf):
+    idx, _, kept, dropped, load, cap = oracle.capacity_route(s, k, cf)
+    return idx, np.where(kept, oracle.topk_route(s, k)[1], 0.0), kept, dropped, load, cap
+
+
+def _p_over_k(g, idx, E):
+    counts, f, p, _ = oracle.aux_stats(g, idx, E)
+    p = p / idx.shape[1]
+    return counts, f, p, float(E * np.sum(f * p))
+
+
+def _bias_subtracted(x, w_g, bias=None):
+    s = np.asarray(x, np.float64) @ np.asarray(w_g, np.float64).T
+    return s if bias is None else s - np.asarray(bias, np.float64)[None, :]
+
+
+def _silu_is_sigmoid(a):
+    return 1.0 / (1.0 + np.exp(-a))
+
+
+def _forward_renormalises(x, idx, w, experts, round_h=None):
+    return oracle.moe_forward(x, idx, w / w.sum(axis=1, keepdims=True), experts, round_h)
+
+
 def _silu_sign(a):
     return a / (1.0 + np.exp(a))
 
@@ -745,6 +851,20 @@ MUTANTS = {
     "p_from_combine_weights": dict(aux_stats=_p_from_combine_weights),
     "forward_last_slot_only": dict(moe_forward=_forward_last_slot_only),
     "router_experts_reversed": dict(router_logits=_experts_reversed),
+    "z_loss_summed_not_averaged": dict(router_z_loss=_z_loss_summed),
+    "z_loss_without_the_max_added_back": dict(router_z_loss=_z_loss_without_max_back),
+    "fraction_loss_without_E": dict(aux_stats_fraction=_fraction_loss_without_E),
+    "topk_slots_ascending": dict(topk_route=_topk_slots_ascending),
+    "dispatch_perm_and_inverse_swapped": dict(dispatch=_dispatch_perm_inv_swapped),
+    "ec_pos_without_segment_start": dict(expert_choice_route=_ec_pos_local),
+    "ec_picks_ascending": dict(expert_choice_route=_ec_picks_ascending),
+    "glu_without_silu": dict(swiglu_expert=_glu_without_silu),
+    "capacity_load_counts_drops": dict(capacity_route=_capacity_load_counts_drops),
+    "capacity_weights_of_all_slots": dict(capacity_route=_capacity_weights_of_all_slots),
+    "p_divided_by_k": dict(aux_stats=_p_over_k),
+    "bias_subtracted": dict(router_logits=_bias_subtracted),
+    "silu_is_sigmoid": dict(silu=_silu_is_sigmoid),
+    "forward_renormalises_weights": dict(moe_forward=_forward_renormalises),
 }
 
 
