@@ -300,9 +300,14 @@ def run_gpu(args, cfg):
 def launches_per_step(cfg) -> int:
     if cfg.routing == "expert_choice":
         return 7  # logits, EC select, offsets, gather, gate/up, down, EC combine
+    # the scatter reduces the per-tile count matrix itself unless tiles^2 * E exceeds
+    # 4 Mi reads; then a one-CTA scan and the aux finalisation run as two more launches
+    tile_tokens = 32 if cfg.E <= 16 else 64
+    tiles = -(-cfg.T // tile_tokens)
+    extra = 2 if tiles * tiles * cfg.E > 4 * 1024 * 1024 else 0
     if cfg.dtype == "bf16" and cfg.k <= 2:
-        return 4  # router (+ dispatch counts), scatter (+ scan, aux, y = 0), gate/up, down + combine
-    return 5  # router (+ dispatch counts), scatter (+ scan, aux), gate/up, down, combine
+        return 4 + extra  # router (+ dispatch counts), scatter (+ scan, aux, y = 0), gate/up, down + combine
+    return 5 + extra  # router (+ dispatch counts), scatter (+ scan, aux), gate/up, down, combine
 
 
 def stage_breakdown(moe, torch, cfg, x, w, flush, stream, steps):
