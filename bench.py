@@ -267,6 +267,7 @@ def run_gpu(args, cfg):
                    "l2": "flushed between timed steps (256 MiB write)",
                    "launch": "CUDA graph replay of moe_layer_forward (one graph launch per step)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "ms_per_step_median": float(np.median(step_ms)),
         "ms_per_step_eager_launch": eager_ms,
         "active_tflops": tflops,
         "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
