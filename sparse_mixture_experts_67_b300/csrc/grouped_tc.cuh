@@ -197,17 +197,6 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// As tma_load_2d, written to the same offset (and signalling the mbarrier at
-// the same offset) in every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tma_load_2d_mcast(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                                  int x, int y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::"
-      "cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
 // 2-CTA form: the completion is signalled on `cluster_bar`, which may be the
 // mbarrier of either CTA of the pair (here always the pair's rank-0 CTA).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t cluster_bar,
@@ -248,16 +237,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Arrive on the mbarrier at this offset in every CTA of cta_mask when this
-// thread's issued MMAs complete.
-__device__ __forceinline__ void tc_commit_mcast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -280,7 +259,9 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
       : "memory");
 }
 
-__device__ __forceinline__ void tc_commit_pair_mcast(uint64_t* bar, uint16_t cta_mask) {
+// Arrive on the mbarrier at this offset in each CTA of cta_mask once the
+// pair's issued MMAs complete (a completion signal; it moves no data).
+__device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
       "[%0], %1;" ::"r"(smem_u32(bar)),
@@ -363,11 +344,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // GATHER (gate/up only): row r of A is row gsrc[r] / gdiv of the tensor behind
 // tmA (x itself, mapped with a one-row box) instead of row r; each producer
 // lane brings 4 of the tile's 128 rows per k-block with one TMA gather4.
-// MCAST: launched in clusters of 2.  The two CTAs take the two 128-row halves
-// of a 256-row block for the same weight tile; each loads half of the B tile
-// and multicasts it into both CTAs' shared memory (half the weight-tile L2
-// requests).  A stage is refilled only after both CTAs' MMAs released it: each
-// MMA thread commits to the empty barriers of both CTAs (arrival count 2).
 // PAIR: launched in clusters of 2 as one 2-CTA MMA unit (tcgen05 cta_group::2)
 // over 256-row blocks.  Each CTA loads its own 128 A rows and its half of the
 // B tile (gate/up: rank 0 the gate rows, rank 1 the up rows), signalling the
@@ -376,7 +352,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // epilogue drains its own TMEM rows and arrives on rank 0's accumulator-empty
 // barrier (4 warps x 2 CTAs).  Per SM this moves 32 KiB instead of 48 KiB of
 // operands into shared memory per k-block for the same 128 x 256 outputs.
-// PAIRING: 0 single CTA, 1 MCAST, 2 PAIR.
+// PAIRING: 0 single CTA, 2 PAIR.
 template <bool GATEUP, int BN, bool COMBINE = false, bool GATHER = false, int PAIRING = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -386,7 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const float* __restrict__ topk_w = nullptr, int kslots = 1,
                       const __nv_bfloat16* __restrict__ gx = nullptr,
                       const int32_t* __restrict__ gsrc = nullptr, int gdiv = 1) {
-  constexpr bool MCAST = PAIRING == 1, PAIR = PAIRING == 2, CL = PAIRING != 0;
+  static_assert(PAIRING == 0 || PAIRING == 2, "single CTA or 2-CTA pair");
+  constexpr bool PAIR = PAIRING == 2, CL = PAIR;
   static_assert(!(PAIR && (GATHER || BN != 256)), "2-CTA MMA: 256-wide tiles without gather");
   using C = Cfg<BN, PAIR>;
   constexpr int STAGES = C::STAGES;
@@ -414,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], MCAST ? 2 : 1);
+      mbar_init(&S.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.tmem_full[b], 1);
@@ -464,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // of the loaded B tile), so the wave takes half as long.
   const int total_tiles = S.cum[E] * n_tiles;
   int full_units = total_tiles, split_tiles = 0;
-  if (!GATEUP && !MCAST && BN == 256) {
+  if (!GATEUP && BN == 256) {
     const int rem = total_tiles % ustride;
     if (rem > 0 && 2 * rem <= ustride) {
       full_units = total_tiles - rem;
@@ -546,13 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (lane == 0 && !PAIR) {
             if (!GATHER) tma_load_2d(sA, &tmA, &S.full[stage], kb * BK, c.row0);
-            if (MCAST) {
-              // this CTA's half of B (gate/up: rank 0 the gate rows, rank 1 the up
-              // rows; down: rows brow + rank * BN/2 through the half-height map)
-              tma_load_2d_mcast(sB + crank * (B_BYTES / 2), GATEUP && crank == 0 ? &tmB0 : &tmB1,
-                                &S.full[stage], kb * BK,
-                                GATEUP ? brow : brow + (int)crank * (BN / 2), kPair);
-            } else if (GATEUP) {
+            if (GATEUP) {
               tma_load_2d(sB, &tmB0, &S.full[stage], kb * BK, brow);
               tma_load_2d(sB + B_BYTES / 2, &tmB1, &S.full[stage], kb * BK, brow);
             } else {
@@ -626,9 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_f16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
                          (kb | kk) != 0 ? 1u : 0u);
           }
-          // frees the smem stage once these MMAs finish (in both CTAs when multicasting / paired)
-          if (PAIR) tc_commit_pair_mcast(&S.empty[stage], kPair);
-          else if (MCAST) tc_commit_mcast(&S.empty[stage], kPair);
+          // frees the smem stage once these MMAs finish (in both CTAs when paired)
+          if (PAIR) tc_commit_pair(&S.empty[stage], kPair);
           else tc_commit(&S.empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -636,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (PAIR) tc_commit_pair_mcast(&S.tmem_full[acc], kPair);
+        if (PAIR) tc_commit_pair(&S.tmem_full[acc], kPair);
         else tc_commit(&S.tmem_full[acc]);
         if (++acc == 2) {
           acc = 0;
@@ -644,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // drain: all issued MMAs complete before TMEM is released
-      if (PAIR) tc_commit_pair_mcast(&S.drain, 0x1);
+      if (PAIR) tc_commit_pair(&S.drain, 0x1);
       else tc_commit(&S.drain);
       const uint32_t a = smem_u32(&S.drain);
       const uint64_t t0 = global_timer_ns();
@@ -851,18 +821,17 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
                   gdiv);
 }
 
-// How 256-wide launches pair CTAs: 2 = 2-CTA MMA (PAIR, the default),
-// 1 = weight-tile multicast (MCAST), 0 = single CTAs.  MOE_GROUPED_CLUSTER in
-// the environment ("pair", "mcast", "none") selects one (tests, A/B timing).
+// How 256-wide launches pair CTAs: 2 = 2-CTA MMA (PAIR, the default), 0 =
+// single CTAs.  MOE_GROUPED_CLUSTER in the environment ("pair", "none")
+// selects one (tests, A/B timing).
 inline int cluster_mode() {
   const char* v = getenv("MOE_GROUPED_CLUSTER");
   if (!v || !*v) return 2;
-  if (v[0] == 'm') return 1;
   if (v[0] == 'n' || v[0] == '0') return 0;
   return 2;
 }
 
-// Cluster-of-2 launch of a 256-wide kernel (PAIRING 1 or 2).  The grid is the
+// Cluster-of-2 launch of a 256-wide kernel as one 2-CTA MMA unit (PAIRING 2).  The grid is the
 // number of clusters that fit at once (queried once per device and mode),
 // capped by the work, times two.
 template <bool GATEUP, bool COMBINE, int PAIRING>
@@ -905,12 +874,10 @@ cudaError_t launch_cluster(const CUtensorMap& a, const CUtensorMap& b0, const CU
 }
 
 template <bool GATEUP, bool COMBINE>
-cudaError_t launch_paired(int mode, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+cudaError_t launch_paired(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                           const int32_t* offsets, int R, int E, int N, int K, void* out,
                           cudaStream_t s, const int32_t* perm = nullptr,
                           const float* topk_w = nullptr, int kslots = 1) {
-  if (mode == 1)
-    return launch_cluster<GATEUP, COMBINE, 1>(a, b0, b1, offsets, R, E, N, K, out, s, perm, topk_w, kslots);
   return launch_cluster<GATEUP, COMBINE, 2>(a, b0, b1, offsets, R, E, N, K, out, s, perm, topk_w, kslots);
 }
 
@@ -954,7 +921,7 @@ inline cudaError_t launch_gateup_tc(const __nv_bfloat16* x_perm, const int32_t* 
       !tc::make_map(&m[2], w_up, (uint64_t)E * F, (uint64_t)d, bn / 2))
     return cudaErrorInvalidValue;
   if (bn == 256 && tc::cluster_mode() != 0)
-    return tc::launch_paired<true, false>(tc::cluster_mode(), m[0], m[1], m[2], offsets, R, E, F, d, h, s);
+    return tc::launch_paired<true, false>(m[0], m[1], m[2], offsets, R, E, F, d, h, s);
   return tc::launch<true>(m, bn, offsets, R, E, F, d, h, sms, s);
 }
 
@@ -999,7 +966,7 @@ inline cudaError_t launch_down_tc(const __nv_bfloat16* h, const int32_t* offsets
       !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, bn / 2))
     return cudaErrorInvalidValue;
   if (mode != 0)
-    return tc::launch_paired<false, false>(mode, m[0], m[1], m[2], offsets, R, E, d, F, y_perm, s);
+    return tc::launch_paired<false, false>(m[0], m[1], m[2], offsets, R, E, d, F, y_perm, s);
   return tc::launch<false>(m, bn, offsets, R, E, d, F, y_perm, sms, s);
 }
 
@@ -1018,7 +985,7 @@ inline cudaError_t launch_down_combine_tc(const __nv_bfloat16* h, const int32_t*
       !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, 128))
     return cudaErrorInvalidValue;
   if (mode != 0)
-    return tc::launch_paired<false, true>(mode, m[0], m[1], m[2], offsets, R, E, d, F, y, s, perm,
+    return tc::launch_paired<false, true>(m[0], m[1], m[2], offsets, R, E, d, F, y, s, perm,
                                           topk_w, k);
   return tc::launch_bn<false, 256, true>(m[0], m[1], m[2], offsets, R, E, d, F, y, sms, s, perm,
                                          topk_w, k);

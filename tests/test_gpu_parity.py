@@ -500,14 +500,14 @@ def test_gateup_gather_bit_identical(moe, torch, case, tile_n, monkeypatch):
     assert torch.equal(h_ref.view(torch.int16), h_gat.view(torch.int16))
 
 
-@pytest.mark.parametrize("mode", ["pair", "mcast"])
 @pytest.mark.parametrize("k", [2, 4])
-def test_cluster_paths_bit_identical(moe, torch, k, mode, monkeypatch):
-    """Clusters of 2 change only where operand bytes come from and which SM issues the
-    MMA (pair: one M = 256 instruction over both CTAs' rows; mcast: weight tiles
-    multicast), never the per-element arithmetic: outputs equal the single-CTA path
-    bit for bit.  Row counts leave partial 256-row blocks and an expert of < 128 rows."""
-    cfg = synth.small_config("mcast", 4000, 256, 512, 8, k, "bf16", seed=60, x_std=1.0, w_std=0.05)
+def test_cluster_paths_bit_identical(moe, torch, k, monkeypatch):
+    """The 2-CTA pair changes only where operand bytes come from and which SM issues the
+    MMA (one M = 256 instruction over both CTAs' rows), never the per-element arithmetic:
+    outputs equal the single-CTA path bit for bit.  Row counts leave partial 256-row
+    blocks and an expert of < 128 rows."""
+    mode = "pair"
+    cfg = synth.small_config("pair_layer", 4000, 256, 512, 8, k, "bf16", seed=60, x_std=1.0, w_std=0.05)
     inp = synth.make_inputs(cfg)
     w = dev_weights(inp)
     x = to_dev(inp.x)
@@ -523,10 +523,10 @@ def test_cluster_paths_bit_identical(moe, torch, k, mode, monkeypatch):
     assert torch.equal(y_cl, y_one)
 
 
-@pytest.mark.parametrize("mode", ["pair", "mcast"])
-def test_cluster_paths_grouped_ragged(moe, torch, mode, monkeypatch):
-    """Both cluster forms of the separate gate/up and down entry points on ragged
+def test_cluster_paths_grouped_ragged(moe, torch, monkeypatch):
+    """The 2-CTA pair form of the separate gate/up and down entry points on ragged
     segments (empty experts, one row, a 128-row half block) against the single-CTA path."""
+    mode = "pair"
     cnts = [300, 0, 1, 128, 129, 700, 0, 255]
     d, F = 256, 512
     cfg = synth.small_config("pair_ragged", int(sum(cnts)), d, F, len(cnts), 1, "bf16", seed=61,
