@@ -5,11 +5,15 @@
 
 One step = one full layer forward (router, dispatch, gate/up GEMM + SwiGLU,
 down GEMM, combine, aux statistics) over one batch of synthetic tokens of the
-workload, inputs resident in HBM.  L2 is flushed (a 256 MiB write) between
-timed steps; each step is timed with CUDA events on the launching stream.
-Prints one JSON line.  Under torchrun every rank runs its own replica of the
-workload (tokens are independent, no collective on the data path); the time
-is the max over ranks and the value counts the tokens of all ranks.
+workload, inputs resident in HBM.  The default workload is the largest one,
+the Mixtral-shaped layer (d=4096, F=14336, E=8, top-2) at T=16384 tokens.
+L2 is flushed (a 256 MiB write) between timed steps; each step is timed with
+CUDA events on the launching stream.  Prints one JSON line; on one GPU the
+line also carries the other workloads (top-2 d=1024, the fine-grained E=64
+layer, expert choice, and the large layer at T=16/256/4096) under
+"workloads".  Under torchrun every rank runs its own replica of the workload
+(tokens are independent, no collective on the data path); the time is the max
+over ranks and the value counts the tokens of all ranks.
 
 --impl reference times the fp64 CPU oracle on bounded samples of the same
 workload on the host cores (rank 0 only).
@@ -47,11 +51,12 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="top2_d1024")
+    ap.add_argument("--workload", default="large_d4096")
     ap.add_argument("--tokens", type=int, default=0, help="override T (large_d4096 sweep)")
     ap.add_argument("--impl", default="moe", choices=["moe", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the other workloads")
     return ap.parse_args(argv)
 
 
@@ -67,6 +72,13 @@ def describe(cfg: synth.LayerConfig) -> str:
         return (f"{cfg.name}: expert-choice T={cfg.T} d={cfg.d} F={cfg.F} E={cfg.E} "
                 f"cf={cfg.capacity_factor} C={cfg.C} {cfg.dtype}")
     return f"{cfg.name}: top-{cfg.k} T={cfg.T} d={cfg.d} F={cfg.F} E={cfg.E} {cfg.dtype}"
+
+
+def workload_keys(cfg: synth.LayerConfig, ws: int) -> dict:
+    """The workload part of the JSON line's config (the same in both arms)."""
+    return {"workload": describe(cfg), "T_per_gpu": cfg.T, "d_model": cfg.d, "d_ff": cfg.F,
+            "experts": cfg.E, "k": cfg.k, "routing": cfg.routing,
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}
 
 
 def load_peaks():
@@ -166,6 +178,82 @@ class ClockSampler:
 # ---------------------------------------------------------------- GPU arm
 
 
+def _upload(torch, dev, a):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def _device_weights(torch, dev, inp):
+    return {"w_g": _upload(torch, dev, inp.w_g),
+            "bias": None if inp.bias is None else _upload(torch, dev, inp.bias),
+            "w_gate": _upload(torch, dev, inp.w_gate), "w_up": _upload(torch, dev, inp.w_up),
+            "w_down": _upload(torch, dev, inp.w_down)}
+
+
+def _capture(torch, layer, x, y, warmup):
+    """Warm-up launches, then the layer captured once into a CUDA graph."""
+    for _ in range(max(3, warmup)):
+        layer(x, y=y)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer(x, y=y)
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+        layer(x, y=y)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    return graph
+
+
+def _timed_replays(torch, graph, flush, stream, steps):
+    """Device ms of each graph replay, L2 flushed before each."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def _weight_bytes(cfg, experts_used: int) -> float:
+    """Expert weight bytes a forward reads when `experts_used` experts hold rows."""
+    return 3.0 * experts_used * cfg.F * cfg.d * (2 if cfg.dtype == "bf16" else 4)
+
+
+def dominant_kernel(cfg, stages, peaks, peak_src, experts_used=None):
+    """Roofline entry of the stage that takes the most time: the gate/up GEMM against the
+    bf16 tensor peak when the expert segments are compute-bound, against HBM on its
+    weight bytes when they are not (fewer rows per expert than the ridge point)."""
+    gu_ms = stages["gateup_ms"]
+    flops = 4.0 * cfg.R * cfg.d * cfg.F
+    used = cfg.E if experts_used is None else experts_used
+    rows_per_expert = cfg.R / max(used, 1)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)  # flop per byte
+    b = 2 if cfg.dtype == "bf16" else 4
+    if rows_per_expert * 2 / b >= ridge / 2:  # ~rows flop per weight byte
+        achieved = flops / (gu_ms / 1e3) / 1e12
+        return {"kernel": "grouped gate/up GEMM + SwiGLU", "bound": "tensor",
+                "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "peak_kind": f"bf16 dense burst ({peak_src})", "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"],
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "algorithmic_flops_per_launch": flops}
+    byts = 2.0 * used * cfg.F * cfg.d * b + cfg.R * cfg.d * b + cfg.R * cfg.F * b
+    achieved = byts / (gu_ms / 1e3) / 1e9
+    return {"kernel": "grouped gate/up GEMM + SwiGLU (weight-bandwidth-bound)", "bound": "hbm",
+            "achieved": achieved, "peak": peaks["hbm_gbs"], "peak_kind": f"HBM copy ({peak_src})",
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+            "algorithmic_bytes_per_launch": byts}
+
+
 def run_gpu(args, cfg):
     import torch
 
@@ -181,54 +269,26 @@ def run_gpu(args, cfg):
     dev = torch.device("cuda", local_rank)
 
     inp = synth.make_inputs(cfg)
-
-    def up(a):
-        if a.dtype == np.uint16:
-            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    w = {"w_g": up(inp.w_g), "bias": None if inp.bias is None else up(inp.bias),
-         "w_gate": up(inp.w_gate), "w_up": up(inp.w_up), "w_down": up(inp.w_down)}
-    x = up(inp.x)
+    w = _device_weights(torch, dev, inp)
+    x = _upload(torch, dev, inp.x)
     ec = cfg.routing == "expert_choice"
     layer = moe.MoELayer(w, k=cfg.k, routing=1 if ec else 0, capacity_factor=cfg.capacity_factor)
     y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
-    for _ in range(max(3, args.warmup)):
-        layer(x, y=y)
-    torch.cuda.synchronize()
     # the step is replayed from a CUDA graph: one launch per step, no host work
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        layer(x, y=y)
-    torch.cuda.current_stream().wait_stream(side)
-    with torch.cuda.graph(graph, capture_error_mode="relaxed"):
-        layer(x, y=y)
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
+    graph = _capture(torch, layer, x, y, args.warmup)
 
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    for i in range(K):
-        flush.fill_(i & 0xFF)
-        ev[i][0].record(stream)
-        graph.replay()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    step_ms = _timed_replays(torch, graph, flush, stream, K)
     if dist:
         dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     local_s = sum(step_ms) / 1e3
     # the same step launched eagerly through the API, for comparison
     eager = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -240,6 +300,7 @@ def run_gpu(args, cfg):
         b.record(stream)
     torch.cuda.synchronize()
     eager_ms = sum(a.elapsed_time(b) for a, b in eager) / len(eager)
+    del graph
 
     # per-stage breakdown through the individual entry points (same kernels)
     stages = (stage_breakdown_ec if ec else stage_breakdown)(moe, torch, cfg, x, w, flush, stream,
@@ -262,40 +323,91 @@ def run_gpu(args, cfg):
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded normal x and weights of the workload's shape; no dataset)",
-        "config": {"workload": describe(cfg), "T_per_gpu": cfg.T, "d_model": cfg.d, "d_ff": cfg.F,
-                   "experts": cfg.E, "k": cfg.k, "routing": cfg.routing,
-                   "l2": "flushed between timed steps (256 MiB write)",
-                   "launch": "CUDA graph replay of moe_layer_forward (one graph launch per step)",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "config": dict(workload_keys(cfg, ws),
+                       l2="flushed between timed steps (256 MiB write)",
+                       launch="CUDA graph replay of moe_layer_forward (one graph launch per step)"),
         "ms_per_step_median": float(np.median(step_ms)),
         "ms_per_step_eager_launch": eager_ms,
         "active_tflops": tflops,
         "frac_of_bf16_peak": {"burst": tflops / peaks["bf16_tflops"],
                               "sustained": tflops / peaks["bf16_tflops_sustained"],
                               "source": peak_src},
-        "stages_ms": stages,
+        "stages_ms": {k_: v for k_, v in stages.items() if k_ != "experts_used"},
         "gpu_launches": launches_per_step(cfg) * K,
         "clocks": clk,
         "e2e": e2e,
     }
     if stages:
-        gu_ms = stages.get("gateup_ms")
-        gu_flops = 4.0 * cfg.R * cfg.d * cfg.F
-        achieved = gu_flops / (gu_ms / 1e3) / 1e12
+        # the GEMM is timed alone (events around its launch): the burst figure is its
+        # denominator; the sustained one is reported beside it
+        roof = dominant_kernel(cfg, stages, peaks, peak_src, stages.get("experts_used"))
         traffic = recorded_traffic("gateup", cfg.name)
-        # the kernel is timed alone (events around its launch) for ~0.2 ms at a time:
-        # the burst figure is its denominator; the sustained one is reported beside it
-        line["roofline"] = {
-            "kernel": "grouped gate/up GEMM + SwiGLU", "bound": "tensor", "achieved": achieved,
-            "peak": peaks["bf16_tflops"], "peak_kind": f"bf16 dense burst ({peak_src})",
-            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-            "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-            "traffic": None if traffic is None else traffic["bytes_per_launch"],
-            "algorithmic_flops_per_launch": gu_flops,
-        }
+        roof["traffic"] = None if traffic is None else traffic["bytes_per_launch"]
+        line["roofline"] = roof
+    if ws == 1 and not args.no_sweep:
+        del layer, y, x
+        torch.cuda.empty_cache()
+        line["workloads"] = sweep(moe, torch, dev, cfg, inp, w, flush, stream, peaks, peak_src,
+                                  min(K, 30), args.warmup)
     if not args.no_cpu_baseline and ws == 1:
-        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds)
+        del w
+        torch.cuda.empty_cache()
+        line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_seconds, inp)
     return line
+
+
+# the other workloads reported beside the headline: (name, T override)
+SWEEP = (("top2_d1024", 0), ("fine_e64", 0), ("ec_e16", 0), ("large_d4096", 16),
+         ("large_d4096", 256), ("large_d4096", 4096))
+
+
+def sweep(moe, torch, dev, main_cfg, main_inp, main_w, flush, stream, peaks, peak_src, steps,
+          warmup):
+    """ms per step (CUDA-graph replay, L2 flushed), tokens/s, active TFLOP/s and the
+    dominant kernel's roofline fraction of each workload in SWEEP; the large layer at
+    smaller T reuses the headline's weights and the leading rows of its x."""
+    out = []
+    for name, T in SWEEP:
+        base = synth.CONFIGS[name]
+        cfg = base.with_tokens(T) if T else base
+        if cfg == main_cfg:
+            continue
+        same_weights = name == main_cfg.name.split("@")[0] and T <= main_cfg.T
+        if same_weights:
+            inp, w = None, main_w
+            x = _upload(torch, dev, main_inp.x[:cfg.T])
+        else:
+            inp = synth.make_inputs(cfg)
+            w = _device_weights(torch, dev, inp)
+            x = _upload(torch, dev, inp.x)
+        ec = cfg.routing == "expert_choice"
+        layer = moe.MoELayer(w, k=cfg.k, routing=1 if ec else 0,
+                             capacity_factor=cfg.capacity_factor)
+        y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
+        graph = _capture(torch, layer, x, y, warmup)
+        ms_list = _timed_replays(torch, graph, flush, stream, steps)
+        del graph
+        ms = float(np.mean(ms_list))
+        stages = (stage_breakdown_ec if ec else stage_breakdown)(moe, torch, cfg, x, w, flush,
+                                                                 stream, min(steps, 10))
+        used = stages.get("experts_used")
+        rec = {"workload": describe(cfg), "ms_per_step": ms,
+               "ms_per_step_median": float(np.median(ms_list)), "steps": steps,
+               "tokens_per_s": cfg.T / (ms / 1e3),
+               "active_tflops": cfg.active_flops() / (ms / 1e3) / 1e12,
+               "stages_ms": {k_: v for k_, v in stages.items() if k_ != "experts_used"},
+               "dominant_kernel": dominant_kernel(cfg, stages, peaks, peak_src, used)}
+        rec["frac_of_bf16_burst"] = rec["active_tflops"] / peaks["bf16_tflops"]
+        if used is not None and rec["dominant_kernel"]["bound"] == "hbm":
+            wb = _weight_bytes(cfg, used)
+            rec["step_weight_bytes"] = wb
+            rec["step_hbm_frac"] = wb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]
+        out.append(rec)
+        del layer, y, x
+        if not same_weights:
+            del w, inp
+        torch.cuda.empty_cache()
+    return out
 
 
 def launches_per_step(cfg) -> int:
@@ -340,7 +452,9 @@ def stage_breakdown(moe, torch, cfg, x, w, flush, stream, steps):
         if i >= 3:
             for j, n in enumerate(names):
                 acc[n] += evs[j].elapsed_time(evs[j + 1])
-    return {n: v / steps for n, v in acc.items()}
+    res = {n: v / steps for n, v in acc.items()}
+    res["experts_used"] = int((p["counts"] > 0).sum().item())
+    return res
 
 
 def stage_breakdown_ec(moe, torch, cfg, x, w, flush, stream, steps):
@@ -464,10 +578,10 @@ class _Pre:
         return self.items[e]
 
 
-def cpu_baseline(cfg, seconds: float, sample_tokens: int = 256):
+def cpu_baseline(cfg, seconds: float, inp=None, sample_tokens: int = 256):
     import oracle
 
-    inp = synth.make_inputs(cfg)
+    inp = inp if inp is not None else synth.make_inputs(cfg)
     x64, wg64 = synth.to_f64(inp.x), synth.to_f64(inp.w_g)
     experts = _Pre(inp)
     rng = np.random.default_rng(7)
@@ -506,7 +620,9 @@ def run_reference(args, cfg):
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(cfg), "T_per_gpu": cfg.T}, "impl": "reference",
+            "config": dict(workload_keys(cfg, ws), l2="not applicable (host CPU)",
+                           launch="fp64 oracle on the host cores, one sample per step"),
+            "impl": "reference",
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

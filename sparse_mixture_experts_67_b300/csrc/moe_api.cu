@@ -34,6 +34,10 @@ moe_status check_dims(int d, moe_dtype dt) {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Top-k layers in bf16 with k <= 2 fuse the weighted combine into the down
+// GEMM's epilogue (deterministic: at most two additions onto zero per element).
+bool fused_combine(const moe_layer_desc& D) { return D.dtype == MOE_BF16 && D.k <= 2; }
+
 struct Carver {
   char* base;
   size_t used = 0;
@@ -381,8 +385,8 @@ size_t moe_layer_workspace_size(const moe_layer_desc* desc) {
     cv.take<int32_t>(A);                                   // inv_perm
     cv.take_bytes(A * D.d * es);                           // x_perm
     cv.take_bytes(A * D.F * es);                           // h
-    cv.take<float>(A * D.d);                               // y_perm
     cv.take<float>(moe_route_aux_rows(D.T));               // z-loss partials
+    if (!fused_combine(D)) cv.take<float>(A * D.d);        // y_perm (separate combine only)
   }
   return cv.used + 256;
 }
@@ -466,8 +470,11 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   int32_t* inv_perm = cv.take<int32_t>(A);
   void* x_perm = cv.take_bytes(A * D.d * es);
   void* h = cv.take_bytes(A * D.F * es);
-  float* y_perm = cv.take<float>(A * D.d);
   float* zpart = cv.take<float>(moe_route_aux_rows(D.T));
+  // k <= 2 (bf16): the down GEMM accumulates the combine into y, zeroed by the
+  // scatter, and no [R, d] y_perm exists
+  const bool fused = fused_combine(D);
+  float* y_perm = fused ? nullptr : cv.take<float>(A * D.d);
   if (O.topk_idx) idx = O.topk_idx;
   if (O.topk_w) tw = O.topk_w;
   if (O.counts) counts = O.counts;
@@ -484,8 +491,6 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
                     nullptr, aux, s, tile_counts, nullptr, D.flags,
                     O.z_loss ? zpart : nullptr) != cudaSuccess)
     return MOE_ERR_CUDA;
-  // k <= 2 (bf16): the down GEMM accumulates the combine into y, zeroed by the scatter
-  const bool fused_combine = D.dtype == MOE_BF16 && k <= 2;
   // the scatter also copies the x rows into dispatch order: contiguous row blocks
   // keep the gate/up operand loads full-width TMA boxes (gathering rows inside
   // the GEMM re-fetches them once per n-block and measured several times slower)
@@ -500,10 +505,10 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   st = dispatch_launch(x, idx, D.T, D.d, D.E, k, D.dtype, x_perm, counts, offsets, perm, inv_perm,
                        tile_counts, tile_base, tile, true, s, aux, O.f ? O.f : fpl,
                        O.p ? O.p : fpl + D.E, O.loss ? O.loss : fpl + 2 * D.E,
-                       fused_combine ? y : nullptr, O.f_frac, O.loss_frac, cap,
+                       fused ? y : nullptr, O.f_frac, O.loss_frac, cap,
                        capacity ? tw : nullptr, O.dropped, O.z_loss ? zpart : nullptr, O.z_loss);
   if (st != MOE_OK) return st;
-  if (fused_combine) {
+  if (fused) {
     // down projection with the combine in its epilogue (deterministic for k <= 2)
     st = moe_grouped_gateup_swiglu(x_perm, offsets, w->w_gate, w->w_up, (int)A, D.d, D.F, D.E,
                                    D.dtype, h, stream);

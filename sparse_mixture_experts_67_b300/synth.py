@@ -17,6 +17,8 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from typing import Dict, Optional, Sequence, Tuple
 
 import numpy as np
@@ -153,13 +155,25 @@ class LayerInputs:
     w_down: np.ndarray  # [E, d, F]
 
 
-def make_inputs(cfg: LayerConfig) -> LayerInputs:
+def make_inputs(cfg: LayerConfig, threads: int = 0) -> LayerInputs:
+    """All tensors of a workload.  The experts are drawn on a thread pool (numpy's
+    generators release the GIL); every tensor has its own stream, so the values do
+    not depend on the thread count or the order the draws finish in."""
     store = np.uint16 if cfg.dtype == "bf16" else np.float32
     w_gate = np.empty((cfg.E, cfg.F, cfg.d), dtype=store)
     w_up = np.empty((cfg.E, cfg.F, cfg.d), dtype=store)
     w_down = np.empty((cfg.E, cfg.d, cfg.F), dtype=store)
-    for e in range(cfg.E):
+
+    def fill(e: int) -> None:
         w_gate[e], w_up[e], w_down[e] = make_expert_weights(cfg, e)
+
+    n = threads or min(cfg.E, os.cpu_count() or 1, 16)
+    if n > 1 and cfg.E > 1:
+        with ThreadPoolExecutor(n) as ex:
+            list(ex.map(fill, range(cfg.E)))
+    else:
+        for e in range(cfg.E):
+            fill(e)
     return LayerInputs(cfg, make_x(cfg), make_router_weight(cfg), router_bias(cfg),
                        w_gate, w_up, w_down)
 

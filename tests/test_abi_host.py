@@ -104,8 +104,12 @@ def test_layer_workspace_and_errors(L):
     d = moe._Desc(8192, 1024, 4096, 8, 2, 0, 0.0, 1)
     ws = L.moe_layer_workspace_size(ctypes.byref(d))
     A = 8192 * 2
-    # at least x_perm + h (bf16) + y_perm (fp32)
-    assert ws >= A * 1024 * 2 + A * 4096 * 2 + A * 1024 * 4
+    # bf16 top-2 combines inside the down GEMM: at least x_perm + h (bf16), no y_perm
+    assert A * 1024 * 2 + A * 4096 * 2 <= ws < A * 1024 * 2 + A * 4096 * 2 + A * 1024 * 4
+    # top-4 keeps the [R, d] fp32 y_perm for the separate combine
+    d4 = moe._Desc(8192, 1024, 4096, 8, 4, 0, 0.0, 1)
+    A4 = 8192 * 4
+    assert L.moe_layer_workspace_size(ctypes.byref(d4)) >= A4 * 1024 * 2 + A4 * 4096 * 2 + A4 * 1024 * 4
     ec = moe._Desc(8192, 1024, 4096, 16, 0, 1, 2.0, 1)
     R = 16 * 1024
     assert L.moe_layer_workspace_size(ctypes.byref(ec)) >= R * 1024 * 2 + R * 4096 * 2 + R * 1024 * 4

@@ -47,11 +47,16 @@ def test_noalloc_permute_matches_workspace_permute_twice():
     import sparse_mixture_experts_67_b300 as moe
 
     # first call spans more tiles and experts than the second, so stale
-    # entries of the shared scratch lie inside and beyond the second's range
-    cases = [("noalloc_a", 6000, 128, 64, 4, "bf16"), ("noalloc_b", 1500, 64, 8, 2, "bf16")]
+    # entries of the shared scratch lie inside and beyond the second's range;
+    # the third has 293 tiles of 2048 assignments, so 293^2 * 64 > 4 Mi reads
+    # sends it through the separate one-CTA scan, which writes the tile bases
+    # into the second half of the array (293 * 64 entries fit in that half)
+    cases = [("noalloc_a", 6000, 128, 64, 4, "bf16"), ("noalloc_b", 1500, 64, 8, 2, "bf16"),
+             ("noalloc_scan", 150000, 64, 64, 4, "bf16")]
     for name, T, d, E, k, dt in cases:
         rng = np.random.default_rng(T + E)
-        idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+        # k distinct experts per token: the first k of a random order of the E
+        idx = np.argsort(rng.random((T, E)), axis=1)[:, :k].astype(np.int32)
         x = to_dev(synth.make_x(synth.small_config(name, T, d, 64, E, k, dt, seed=T)))
         idx_d = torch.from_numpy(idx).cuda()
         ref = moe.moe_permute(x, idx_d, E)
