@@ -136,15 +136,21 @@ moe_status moe_route(const void* x, const void* w_g, const float* bias, int T, i
  *     (the non-zero pattern of the page's dispatch mask; dispatch row of a pick),
  *   logits [T,E] fp32: required.
  * pos doubles as scratch: the router stores the logits there transposed
- * ([E,T] fp32 bits) and the selection of expert e reads row e once, coalesced,
- * before writing the position map over it.
- * Limits: T <= 16384 (one expert's keys are sorted in shared memory),
- *         C <= T, E <= 256.                                                  */
+ * ([E,T] fp32 bits) and the selection reads each row once, coalesced, before
+ * writing the position map over it.
+ * ws: device scratch of moe_expert_choice_workspace_size(T, E, capacity_factor)
+ *   bytes (caller-owned; contents on entry do not matter), holding each
+ *   1024-token slice's sorted candidates and softmax partial sums.
+ * Errors: MOE_ERR_INVALID_ARG for T < 0, E outside 1..256, a capacity factor
+ *   that is not positive or C > T, a required pointer NULL; MOE_ERR_WORKSPACE
+ *   when ws is NULL or smaller than the size above (C > 0).
+ * Limits: C <= T, E <= 256.                                                  */
 int moe_expert_choice_capacity(int T, int E, float capacity_factor);
+size_t moe_expert_choice_workspace_size(int T, int E, float capacity_factor);
 moe_status moe_expert_choice_route(const void* x, const void* w_g, const float* bias, int T,
                                    int d, int E, float capacity_factor, moe_dtype dt,
                                    int32_t* ec_idx, float* ec_score, int32_t* pos,
-                                   float* logits, moe_stream_t stream);
+                                   float* logits, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------- dispatch
  * Groups the T*k assignments by expert ([sparse-moe] MoELayerWithAuxLoss

@@ -20,7 +20,7 @@ import torch
 
 __all__ = [
     "MoEError", "lib", "declared_symbols", "moe_route", "moe_expert_choice_route",
-    "moe_expert_choice_capacity", "moe_permute", "moe_permute_noalloc", "moe_gather_rows", "moe_grouped_gateup_swiglu",
+    "moe_expert_choice_capacity", "moe_expert_choice_workspace_size", "moe_permute", "moe_permute_noalloc", "moe_gather_rows", "moe_grouped_gateup_swiglu",
     "moe_grouped_gateup_swiglu_gather",
     "moe_grouped_down", "moe_experts_swiglu", "moe_combine", "moe_ec_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_layer_workspace_size", "moe_route_aux_rows", "moe_device_error",
@@ -71,7 +71,8 @@ _SIGS = {
     "moe_route_aux_rows": ([_I], _Z),
     "moe_route": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P], _I),
     "moe_expert_choice_capacity": ([_I, _I, _F], _I),
-    "moe_expert_choice_route": ([_P, _P, _P, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P], _I),
+    "moe_expert_choice_workspace_size": ([_I, _I, _F], _Z),
+    "moe_expert_choice_route": ([_P, _P, _P, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_permute_workspace_size": ([_I, _I, _I], _Z),
     "moe_permute": ([_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P], _I),
     "moe_gather_rows": ([_P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
@@ -192,6 +193,10 @@ def moe_expert_choice_capacity(T: int, E: int, capacity_factor: float) -> int:
     return int(lib().moe_expert_choice_capacity(T, E, capacity_factor))
 
 
+def moe_expert_choice_workspace_size(T: int, E: int, capacity_factor: float) -> int:
+    return int(lib().moe_expert_choice_workspace_size(T, E, capacity_factor))
+
+
 def _check_router_args(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[torch.Tensor]) -> None:
     _dims(x, 2, "x")
     _dims(w_g, 2, "w_g")
@@ -237,9 +242,12 @@ def moe_expert_choice_route(x: torch.Tensor, w_g: torch.Tensor, bias: Optional[t
     out = {"ec_idx": _empty((E, C), torch.int32, x), "ec_score": _empty((E, C), torch.float32, x),
            "pos": _empty((E, T), torch.int32, x), "logits": _empty((T, E), torch.float32, x),
            "C": C}
+    ws_bytes = int(lib().moe_expert_choice_workspace_size(T, E, capacity_factor))
+    ws = _empty((max(ws_bytes, 1),), torch.uint8, x)
     _check("moe_expert_choice_route", lib().moe_expert_choice_route(
         _ptr(x), _ptr(w_g), _ptr(bias), T, d, E, capacity_factor, _dtype(x), _ptr(out["ec_idx"]),
-        _ptr(out["ec_score"]), _ptr(out["pos"]), _ptr(out["logits"]), _stream()))
+        _ptr(out["ec_score"]), _ptr(out["pos"]), _ptr(out["logits"]), _ptr(ws), ws_bytes,
+        _stream()))
     return out
 
 

@@ -2,19 +2,11 @@
 // Experts(MoE) 아키텍처 심층 분석" (youngju.dev).
 //
 // Each expert scores all tokens with a softmax over its logit column and keeps
-// the C best tokens, C = floor(T * capacity_factor / E).  One CTA per expert,
-// each thread owning a contiguous run of tokens:
-//   - the column max and the sum of exponentials are block reductions;
-//   - a radix select (four 8-bit passes over order-preserving 32-bit keys)
-//     finds the C-th best logit;
-//   - ordered block scans keep every token above it plus, among the tokens
-//     equal to it, the lowest token ids (ties go to the lower token);
-//   - only the C picks are sorted (bitonic, in shared memory) by descending
-//     logit then ascending token, the output order.
-// The logits come from the router kernel run in logits-only mode, which also
-// writes them transposed into pos ([E, T], as fp32 bits): CTA e reads its row
-// there once, coalesced, keeps the order-preserving keys in shared memory and
-// only then overwrites the row with the position map.
+// the C best tokens, C = floor(T * capacity_factor / E), in descending score
+// order with ties to the lower token.  The logits come from the router kernel
+// run in logits-only mode, which also writes them transposed into pos ([E, T],
+// as fp32 bits); the select below reads each expert's row there once,
+// coalesced, and then overwrites it with the position map.
 #pragma once
 
 #include <float.h>
@@ -23,8 +15,6 @@
 
 namespace moe {
 
-constexpr int kEcThreads = 1024;
-constexpr int kEcMaxTokens = 16384;
 
 __device__ __forceinline__ float block_reduce_max(float v, float* scratch) {
 #pragma unroll
@@ -63,172 +53,198 @@ __device__ __forceinline__ float order_key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-inline int next_pow2_host(int v) {
-  int p = 1;
-  while (p < v) p <<= 1;
-  return p;
+
+
+// ------------------------------------------------------------ two-stage select
+// Expert e's logit column is cut into S = ceil(T / kEcSlice) slices; stage 1
+// runs one CTA per (slice, expert), stage 2 likewise, so E * S CTAs share the
+// work instead of E.
+//   stage 1 (ec_slice_kernel): the slice's max and sum of exponentials (about
+//     its own max), its pos entries set to -1, and its (key, token) pairs
+//     sorted ascending (bitonic, shared memory), i.e. by descending logit then
+//     ascending token; the first L = min(C, kEcSlice) are the slice's
+//     candidates (past the slice end: sentinels above every real key).
+//   stage 2 (ec_rank_kernel): every candidate's rank among all candidates of
+//     its expert is its index in its own list plus, for every other list, the
+//     number of entries below it (binary search).  Keys are unique (the token
+//     id is part of the key), and a token of the expert's top C has every
+//     token ahead of it within the first C of each slice, so those ranks are
+//     exact; any other candidate gets a rank of at least C.  Ranks below C
+//     place the token: ec_idx / ec_score at the rank, pos[e, t] = e * C + rank.
+//     The column's max and sum come from the slices' pairs in slice order.
+constexpr int kEcSlice = 1024;            // tokens per stage-1 CTA (one per thread)
+constexpr int kEcRankThreads = 1024;
+constexpr size_t kEcRankSmemMax = 160 * 1024;  // candidate lists staged in shared memory up to this
+
+inline int ec_slices(int T) { return T <= 0 ? 0 : ceil_div(T, kEcSlice); }
+inline int ec_list_len(int C) { return C < kEcSlice ? C : kEcSlice; }
+
+// Scratch of the select, bytes: candidate lists [E, S, L] (u64) and the
+// slices' (max, sum) pairs [E, S] (float2).
+inline size_t ec_scratch_bytes(int T, int E, int C) {
+  const size_t S = (size_t)ec_slices(T), L = (size_t)ec_list_len(C > 0 ? C : 1);
+  return ((size_t)E * S * L * 8 + 255) / 256 * 256 + (size_t)E * S * 8;
 }
 
-// Exclusive prefix sum over the CTA in thread order; *total gets the sum.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* total) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int n = __shfl_up_sync(kFullMask, incl, off);
-    if (lane >= off) incl += n;
+// Number of entries of the ascending list a[0..n) below key.
+__device__ __forceinline__ int count_below(const unsigned long long* a, int n, unsigned long long key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] < key) lo = mid + 1;
+    else hi = mid;
   }
-  if (lane == 31) s_warp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = lane < nw ? s_warp[lane] : 0;
-    int winc = w;
+  return lo;
+}
+
+// Keys past the slice end: above every finite logit's key (whose high word is
+// at most 0xFF7FFFFF) and distinct, so that every key of a slice is unique.
+__device__ __forceinline__ unsigned long long ec_sentinel(int i) {
+  return (0xFFFFFFFFull << 32) | (unsigned)i;
+}
+
+// Ascending sort of the CTA's kEcSlice keys, one per thread (all distinct): a
+// bitonic sort of each warp's 32 keys in registers, then five rounds that merge
+// pairs of sorted runs, each key moving to its index in its own run plus the
+// number of keys below it in the partner run (binary search).  Returns the
+// buffer holding the result.
+__device__ __forceinline__ unsigned long long* slice_sort(unsigned long long key,
+                                                          unsigned long long* buf0,
+                                                          unsigned long long* buf1) {
+  const int tid = threadIdx.x, lane = tid & 31;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int n = __shfl_up_sync(kFullMask, winc, off);
-      if (lane >= off) winc += n;
+  for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(kFullMask, key, j);
+      const bool take_min = ((lane & j) == 0) == ((lane & kk) == 0);
+      key = take_min ? (other < key ? other : key) : (other > key ? other : key);
     }
-    s_warp[lane] = winc - w;
-    if (lane == 31) s_warp[32] = winc;
   }
+  unsigned long long* src = buf0;
+  unsigned long long* dst = buf1;
+  src[tid] = key;
   __syncthreads();
-  const int res = s_warp[warp] + incl - v;
-  *total = s_warp[32];
-  __syncthreads();
-  return res;
+#pragma unroll 1
+  for (int len = 32; len < kEcSlice; len <<= 1) {
+    key = src[tid];  // the key now at this thread's position
+    const int run = tid / len, idx = tid - run * len;
+    const int below = count_below(src + (run ^ 1) * len, len, key);
+    dst[(run & ~1) * len + idx + below] = key;
+    __syncthreads();
+    unsigned long long* tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+  return src;
 }
 
-inline size_t ec_route_smem(int T, int C) {
-  return (((size_t)T * 4 + 15) & ~size_t(15)) + (size_t)next_pow2_host(C) * 8;
+__global__ void __launch_bounds__(kEcSlice)
+    ec_slice_kernel(int T, int E, int C, int L, int32_t* __restrict__ pos,
+                    unsigned long long* __restrict__ cand, float2* __restrict__ stats) {
+  pdl_begin();
+  __shared__ unsigned long long s_buf[2][kEcSlice];
+  __shared__ float scratch[32];
+  const int e = blockIdx.y, sl = blockIdx.x, S = gridDim.x;
+  const int t0 = sl * kEcSlice;
+  const int n = min(kEcSlice, T - t0);
+  const int tid = threadIdx.x;
+  int32_t* prow = pos + (size_t)e * T + t0;  // on entry: this expert's logits (fp32 bits)
+  float v = -FLT_MAX;
+  unsigned long long key = ec_sentinel(tid);
+  if (tid < n) {
+    v = __int_as_float(prow[tid]);
+    key = ((unsigned long long)(~float_order_key(v)) << 32) | (unsigned)(t0 + tid);
+  }
+  const float m = block_reduce_max(v, scratch);  // every read of the slice is done past here
+  const float sum = block_reduce_sum(tid < n ? expf(v - m) : 0.f, scratch);
+  if (tid < n) prow[tid] = -1;
+  if (threadIdx.x == 0) stats[(size_t)e * S + sl] = make_float2(m, sum);
+  if (C <= 0) return;
+  const unsigned long long* sorted = slice_sort(key, s_buf[0], s_buf[1]);
+  unsigned long long* out = cand + ((size_t)e * S + sl) * L;
+  for (int i = tid; i < L; i += blockDim.x) out[i] = sorted[i];
 }
 
-__global__ void __launch_bounds__(kEcThreads)
-    ec_route_kernel(int T, int E, int C, int c_pow2, int32_t* __restrict__ ec_idx,
-                    float* __restrict__ ec_score, int32_t* __restrict__ pos) {
+__global__ void __launch_bounds__(kEcRankThreads)
+    ec_rank_kernel(int T, int E, int C, int L, const unsigned long long* __restrict__ cand,
+                   const float2* __restrict__ stats, int stage_smem, int32_t* __restrict__ ec_idx,
+                   float* __restrict__ ec_score, int32_t* __restrict__ pos) {
   pdl_begin();
   extern __shared__ __align__(16) unsigned char ec_smem[];
-  uint32_t* s_key = reinterpret_cast<uint32_t*>(ec_smem);  // ascending = descending logit
-  unsigned long long* s_sel = reinterpret_cast<unsigned long long*>(
-      ec_smem + (((size_t)T * 4 + 15) & ~size_t(15)));
-  __shared__ float scratch[32];
-  __shared__ int s_warp[33];
-  __shared__ int s_hist[256];
-  __shared__ uint32_t s_prefix;
-  __shared__ int s_remaining;
-  const int e = blockIdx.x;
-  const int per = (T + kEcThreads - 1) / kEcThreads;
-  const int t0 = min(T, threadIdx.x * per), t1 = min(T, t0 + per);
-
-  int32_t* prow = pos + (size_t)e * T;  // on entry: this expert's logits (fp32 bits)
-  float m = -FLT_MAX;
-  for (int t = threadIdx.x; t < T; t += blockDim.x) {  // coalesced
-    const float v = __int_as_float(prow[t]);
-    m = fmaxf(m, v);
-    s_key[t] = ~float_order_key(v);
-  }
-  m = block_reduce_max(m, scratch);  // every read of the row is done past this barrier
-  float sum = 0.f;
-  for (int t = threadIdx.x; t < T; t += blockDim.x) {
-    sum += expf(order_key_float(~s_key[t]) - m);
-    prow[t] = -1;
-  }
-  sum = block_reduce_sum(sum, scratch);  // also publishes the pos writes to the CTA
-  if (C <= 0) return;
-
-  // radix select: the C-th smallest key K* and how many keys equal to it to take
-  uint32_t prefix = 0, mask = 0;
-  int remaining = C;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = threadIdx.x; b < 256; b += blockDim.x) s_hist[b] = 0;
-    __syncthreads();
-    for (int t = t0; t < t1; ++t) {
-      const uint32_t k = s_key[t];
-      if ((k & mask) == prefix) atomicAdd(&s_hist[(k >> shift) & 255u], 1);
+  __shared__ float s_m, s_inv;
+  const int e = blockIdx.y, sl = blockIdx.x, S = gridDim.x;
+  const unsigned long long* lists = cand + (size_t)e * S * L;
+  if (stage_smem) {  // all S lists of this expert, staged once (16-byte pieces, 4 in flight)
+    unsigned long long* sl_ = reinterpret_cast<unsigned long long*>(ec_smem);
+    const int n2 = S * L;  // u64 entries; the lists of one expert start 16-byte aligned
+    const uint4* g4 = reinterpret_cast<const uint4*>(lists);
+    uint4* s4 = reinterpret_cast<uint4*>(sl_);
+    const int n4 = n2 >> 1;
+    const int nt = blockDim.x;
+    int i = threadIdx.x;
+    if (n2 & 1) i = n4;  // an odd count may leave the lists 8-byte aligned: scalar loads only
+    for (; i + 3 * nt < n4; i += 4 * nt) {
+      const uint4 a = g4[i], b = g4[i + nt], c = g4[i + 2 * nt], d = g4[i + 3 * nt];
+      s4[i] = a;
+      s4[i + nt] = b;
+      s4[i + 2 * nt] = c;
+      s4[i + 3 * nt] = d;
     }
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      int loc = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) loc += s_hist[lane * 8 + i];
-      int incl = loc;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int n = __shfl_up_sync(kFullMask, incl, off);
-        if (lane >= off) incl += n;
-      }
-      int cum = incl - loc;
-      if (cum < remaining && remaining <= incl) {
-        for (int i = 0; i < 8; ++i) {
-          const int h = s_hist[lane * 8 + i];
-          if (remaining <= cum + h) {
-            s_prefix = prefix | ((uint32_t)(lane * 8 + i) << shift);
-            s_remaining = remaining - cum;
-            break;
-          }
-          cum += h;
-        }
-      }
-    }
-    __syncthreads();
-    prefix = s_prefix;
-    remaining = s_remaining;
-    mask |= 255u << shift;
+    for (; i < n4; i += nt) s4[i] = g4[i];
+    if (n2 & 1)
+      for (int j = threadIdx.x; j < n2; j += nt) sl_[j] = lists[j];
+    lists = sl_;
   }
-  // keep keys < K* and the first `remaining` keys == K* in token order
-  int n_eq = 0;
-  for (int t = t0; t < t1; ++t) n_eq += s_key[t] == prefix;
-  int total;
-  int eq_rank = block_exclusive_scan(n_eq, s_warp, &total);
-  int n_sel = 0;
-  {
-    int r = eq_rank;
-    for (int t = t0; t < t1; ++t) {
-      const uint32_t k = s_key[t];
-      if (k < prefix || (k == prefix && r++ < remaining)) ++n_sel;
-    }
+  if (threadIdx.x == 0) {  // the column's softmax denominator, slices in order
+    const float2* st = stats + (size_t)e * S;
+    float m = st[0].x;
+    for (int i = 1; i < S; ++i) m = fmaxf(m, st[i].x);
+    float sum = 0.f;
+    for (int i = 0; i < S; ++i) sum += st[i].y * expf(st[i].x - m);
+    s_m = m;
+    s_inv = 1.0f / sum;
   }
-  int slot = block_exclusive_scan(n_sel, s_warp, &total);
-  {
-    int r = eq_rank;
-    for (int t = t0; t < t1; ++t) {
-      const uint32_t k = s_key[t];
-      if (k < prefix || (k == prefix && r++ < remaining))
-        s_sel[slot++] = ((unsigned long long)k << 32) | (unsigned)t;
-    }
-  }
-  for (int i = C + threadIdx.x; i < c_pow2; i += blockDim.x) s_sel[i] = ~0ull;
   __syncthreads();
-  for (int kk = 2; kk <= c_pow2; kk <<= 1) {
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < c_pow2; i += blockDim.x) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long a = s_sel[i], b = s_sel[ixj];
-          const bool up = (i & kk) == 0;
-          if ((a > b) == up) {
-            s_sel[i] = b;
-            s_sel[ixj] = a;
-          }
-        }
-      }
-      __syncthreads();
+  const float m = s_m, inv = s_inv;
+  const unsigned long long* mine = lists + (size_t)sl * L;
+  for (int c = threadIdx.x; c < L; c += blockDim.x) {
+    const unsigned long long key = mine[c];
+    if ((key >> 32) == 0xFFFFFFFFull) continue;  // past the slice end
+    int rank = c;
+    for (int j = 0; j < S && rank < C; ++j)
+      if (j != sl) rank += count_below(lists + (size_t)j * L, L, key);
+    if (rank < C) {
+      const int t = (int)(key & 0xffffffffu);
+      const float v = order_key_float((uint32_t)(key >> 32) ^ 0xffffffffu);
+      ec_idx[(size_t)e * C + rank] = t;
+      ec_score[(size_t)e * C + rank] = expf(v - m) * inv;
+      pos[(size_t)e * T + t] = e * C + rank;
     }
-  }
-  const float inv = 1.0f / sum;
-  for (int c = threadIdx.x; c < C; c += blockDim.x) {
-    const int t = (int)(s_sel[c] & 0xffffffffu);
-    const float v = order_key_float((uint32_t)(s_sel[c] >> 32) ^ 0xffffffffu);
-    ec_idx[(size_t)e * C + c] = t;
-    ec_score[(size_t)e * C + c] = expf(v - m) * inv;
-    pos[(size_t)e * T + t] = e * C + c;
   }
 }
 
-inline int next_pow2(int v) {
-  int p = 1;
-  while (p < v) p <<= 1;
-  return p;
+// Stage 1 and stage 2 on the logits already transposed into pos ([E, T], fp32
+// bits).  scratch: ec_scratch_bytes(T, E, C) bytes, 256-byte aligned.
+inline cudaError_t launch_ec_select(int T, int E, int C, int32_t* ec_idx, float* ec_score,
+                                    int32_t* pos, void* scratch, cudaStream_t s) {
+  const int S = ec_slices(T), L = ec_list_len(C > 0 ? C : 1);
+  unsigned long long* cand = static_cast<unsigned long long*>(scratch);
+  float2* stats = reinterpret_cast<float2*>(static_cast<char*>(scratch) +
+                                            ((size_t)E * S * L * 8 + 255) / 256 * 256);
+  cudaError_t err = launch_k(ec_slice_kernel, dim3(S, E), dim3(kEcSlice), 0, s, nullptr, 0, T, E, C,
+                             L, pos, cand, stats);
+  if (err != cudaSuccess || C <= 0) return err;
+  const size_t lists_bytes = (size_t)S * L * 8;
+  const int stage = lists_bytes <= kEcRankSmemMax ? 1 : 0;
+  const size_t sm = stage ? lists_bytes : 0;
+  err = cudaFuncSetAttribute(ec_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kEcRankSmemMax);
+  if (err != cudaSuccess) return err;
+  return launch_k(ec_rank_kernel, dim3(S, E), dim3(kEcRankThreads), sm, s, nullptr, 0, T, E, C, L,
+                  (const unsigned long long*)cand, (const float2*)stats, stage, ec_idx, ec_score,
+                  pos);
 }
+
 
 }  // namespace moe

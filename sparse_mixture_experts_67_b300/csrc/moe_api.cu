@@ -103,30 +103,33 @@ int moe_expert_choice_capacity(int T, int E, float capacity_factor) {
   return (int)floor((double)T * (double)capacity_factor / (double)E);
 }
 
+size_t moe_expert_choice_workspace_size(int T, int E, float capacity_factor) {
+  const int C = moe_expert_choice_capacity(T, E, capacity_factor);
+  if (C < 0 || T <= 0 || E > MOE_MAX_EXPERTS) return 0;
+  return ec_scratch_bytes(T, E, C) + 256;
+}
+
 moe_status moe_expert_choice_route(const void* x, const void* w_g, const float* bias, int T, int d,
                                    int E, float capacity_factor, moe_dtype dt, int32_t* ec_idx,
-                                   float* ec_score, int32_t* pos, float* logits,
-                                   moe_stream_t stream) {
+                                   float* ec_score, int32_t* pos, float* logits, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
   if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS || !(capacity_factor > 0.f)) return MOE_ERR_INVALID_ARG;
   moe_status st = check_dims(d, dt);
   if (st != MOE_OK) return st;
   const int C = moe_expert_choice_capacity(T, E, capacity_factor);
   if (C > T) return MOE_ERR_INVALID_ARG;
-  if (T > kEcMaxTokens) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!x || !w_g || !pos || !logits || (C > 0 && (!ec_idx || !ec_score))) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < moe_expert_choice_workspace_size(T, E, capacity_factor))
+    return MOE_ERR_WORKSPACE;
   if (dt == MOE_BF16 && (!aligned16(x) || !aligned16(w_g))) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = (cudaStream_t)stream;
   // logits [T, E] for the caller, and transposed into pos for the selection
   cudaError_t e = launch_router(x, w_g, bias, T, d, E, /*k=*/0, dt == MOE_BF16, nullptr, nullptr,
                                 logits, nullptr, nullptr, s, nullptr, reinterpret_cast<float*>(pos));
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  const int c2 = next_pow2(C > 0 ? C : 1);
-  const size_t sm = ec_route_smem(T, C > 0 ? C : 1);
-  e = cudaFuncSetAttribute(ec_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_k(ec_route_kernel, dim3(E), dim3(kEcThreads), sm, s, nullptr, 0, T, E, C,
-                              c2, ec_idx, ec_score, pos));
+  char* scratch = static_cast<char*>(ws) + ((256 - (reinterpret_cast<uintptr_t>(ws) & 255)) & 255);
+  return cuda_status(launch_ec_select(T, E, C, ec_idx, ec_score, pos, scratch, s));
 }
 
 size_t moe_permute_workspace_size(int T, int E, int k) {
@@ -371,6 +374,7 @@ size_t moe_layer_workspace_size(const moe_layer_desc* desc) {
     cv.take_bytes(R * D.d * es);        // x_perm
     cv.take_bytes(R * D.F * es);        // h
     cv.take<float>(R * D.d);            // y_perm
+    cv.take_bytes(moe_expert_choice_workspace_size(D.T, D.E, D.capacity_factor));  // select
   } else {
     if (D.k < 1 || D.k > D.E) return 0;
     const size_t A = (size_t)D.T * D.k;
@@ -435,12 +439,14 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
     void* x_perm = cv.take_bytes(R * D.d * es);
     void* h = cv.take_bytes(R * D.F * es);
     float* y_perm = cv.take<float>(R * D.d);
+    const size_t sel_bytes = moe_expert_choice_workspace_size(D.T, D.E, D.capacity_factor);
+    void* sel_ws = cv.take_bytes(sel_bytes);
     if (O.logits) logits = O.logits;
     if (O.ec_idx) ec_idx = O.ec_idx;
     if (O.ec_score) ec_score = O.ec_score;
     if (O.pos) pos = O.pos;
     st = moe_expert_choice_route(x, w->w_g, w->bias, D.T, D.d, D.E, D.capacity_factor, D.dtype,
-                                 ec_idx, ec_score, pos, logits, stream);
+                                 ec_idx, ec_score, pos, logits, sel_ws, sel_bytes, stream);
     if (st != MOE_OK) return st;
     if (R > 0) {
       // expert e owns dispatch rows [e*C, (e+1)*C)

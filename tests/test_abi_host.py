@@ -75,12 +75,18 @@ def test_route_argument_errors(L):
 
 def test_expert_choice_argument_errors(L):
     z = _nullp()
-    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 4, 0.0, 1, _p(), _p(), _p(), _p(), z) == 1
+    ws = L.moe_expert_choice_workspace_size(8, 4, 1.0)
+    assert ws > 0
+    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 4, 0.0, 1, _p(), _p(), _p(), _p(), _p(), ws, z) == 1
     # capacity above T
-    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 2, 4.0, 1, _p(), _p(), _p(), _p(), z) == 1
-    # beyond the shared-memory sort
-    assert L.moe_expert_choice_route(_p(), _p(), z, 20000, 64, 16, 1.0, 1, _p(), _p(), _p(), _p(), z) == 2
-    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 4, 1.0, 1, _p(), _p(), z, _p(), z) == 1
+    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 2, 4.0, 1, _p(), _p(), _p(), _p(), _p(), ws, z) == 1
+    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 4, 1.0, 1, _p(), _p(), z, _p(), _p(), ws, z) == 1
+    # the select's scratch: missing or one byte short
+    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 4, 1.0, 1, _p(), _p(), _p(), _p(), z, ws, z) == 3
+    assert L.moe_expert_choice_route(_p(), _p(), z, 8, 64, 4, 1.0, 1, _p(), _p(), _p(), _p(), _p(), ws - 1, z) == 3
+    # no token limit: the scratch grows with T (slices of 1024 tokens)
+    big = L.moe_expert_choice_workspace_size(40000, 16, 2.0)
+    assert big >= 16 * 40 * 1024 * 8
 
 
 def test_permute_and_experts_errors(L):

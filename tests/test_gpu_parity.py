@@ -404,6 +404,17 @@ def test_layer_expert_choice_capacities(moe, torch, T, E, cf):
     _check_ec_layer(moe, torch, cfg)
 
 
+@pytest.mark.parametrize("T,E,cf", [(32768, 16, 2.0), (5000, 8, 1.0)], ids=["T32768_C4096", "T5000_C625"])
+def test_layer_expert_choice_many_slices(moe, torch, T, E, cf):
+    """Token counts beyond one 1024-token slice per expert: 32 slices whose candidate
+    lists are searched in global memory (too large to stage), and a capacity below the
+    slice length with a ragged last slice."""
+    cfg = synth.LayerConfig(f"ec_T{T}_E{E}", T=T, d=64, F=64, E=E, k=0, dtype="bf16", x_std=1.0,
+                            w_std=0.05, wg_std=0.1, seed=36, routing="expert_choice",
+                            capacity_factor=cf)
+    _check_ec_layer(moe, torch, cfg)
+
+
 def test_expert_choice_route_exact_ties(moe, torch):
     """Tokens with identical rows tie exactly on every expert's logit: the selection keeps
     the lower token ids and orders equal scores by token, as the oracle does."""
