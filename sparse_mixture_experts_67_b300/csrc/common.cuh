@@ -14,7 +14,7 @@ constexpr unsigned kFullMask = 0xffffffffu;
 
 // Device error word: non-zero once a kernel gave up on a bounded barrier wait.
 // Codes: bit 0 = producer wait timed out, bit 1 = MMA wait, bit 2 = epilogue
-// wait, bit 3 = drain wait at exit.
+// wait, bit 3 = drain wait at exit, bit 4 = expert-choice slice wait.
 __device__ uint32_t g_error_word;
 
 __device__ __forceinline__ void record_error(uint32_t code) { atomicOr(&g_error_word, code); }

@@ -79,11 +79,20 @@ constexpr size_t kEcRankSmemMax = 160 * 1024;  // candidate lists staged in shar
 inline int ec_slices(int T) { return T <= 0 ? 0 : ceil_div(T, kEcSlice); }
 inline int ec_list_len(int C) { return C < kEcSlice ? C : kEcSlice; }
 
-// Scratch of the select, bytes: candidate lists [E, S, L] (u64) and the
-// slices' (max, sum) pairs [E, S] (float2).
+// Scratch of the select, bytes: candidate lists [E, S, L] (u64), the slices'
+// (max, sum) pairs [E, S] (float2) and the per-expert arrival counts [E] of the
+// one-launch form, each region 256-byte aligned.
 inline size_t ec_scratch_bytes(int T, int E, int C) {
   const size_t S = (size_t)ec_slices(T), L = (size_t)ec_list_len(C > 0 ? C : 1);
-  return ((size_t)E * S * L * 8 + 255) / 256 * 256 + (size_t)E * S * 8;
+  return ((size_t)E * S * L * 8 + 255) / 256 * 256 + ((size_t)E * S * 8 + 255) / 256 * 256 +
+         (size_t)E * sizeof(int);
+}
+
+// MOE_EC_TWO_LAUNCHES=1 in the environment keeps the two stages as two
+// launches (tests, A/B timing).
+inline bool ec_two_launches() {
+  const char* v = getenv("MOE_EC_TWO_LAUNCHES");
+  return v && v[0] == '1';
 }
 
 // Number of entries of the ascending list a[0..n) below key.
@@ -139,13 +148,14 @@ __device__ __forceinline__ unsigned long long* slice_sort(unsigned long long key
   return src;
 }
 
-__global__ void __launch_bounds__(kEcSlice)
-    ec_slice_kernel(int T, int E, int C, int L, int32_t* __restrict__ pos,
-                    unsigned long long* __restrict__ cand, float2* __restrict__ stats) {
-  pdl_begin();
-  __shared__ unsigned long long s_buf[2][kEcSlice];
-  __shared__ float scratch[32];
-  const int e = blockIdx.y, sl = blockIdx.x, S = gridDim.x;
+// Stage 1 for (slice sl, expert e): the slice's (max, sum) pair, its pos
+// entries set to -1 after they were read, and (C > 0) its first L sorted keys.
+__device__ __forceinline__ void ec_slice_phase(int T, int C, int L, int S, int e, int sl,
+                                               int32_t* __restrict__ pos,
+                                               unsigned long long* __restrict__ cand,
+                                               float2* __restrict__ stats,
+                                               unsigned long long (*s_buf)[kEcSlice],
+                                               float* scratch) {
   const int t0 = sl * kEcSlice;
   const int n = min(kEcSlice, T - t0);
   const int tid = threadIdx.x;
@@ -166,50 +176,56 @@ __global__ void __launch_bounds__(kEcSlice)
   for (int i = tid; i < L; i += blockDim.x) out[i] = sorted[i];
 }
 
-__global__ void __launch_bounds__(kEcRankThreads)
-    ec_rank_kernel(int T, int E, int C, int L, const unsigned long long* __restrict__ cand,
-                   const float2* __restrict__ stats, int stage_smem, int32_t* __restrict__ ec_idx,
-                   float* __restrict__ ec_score, int32_t* __restrict__ pos) {
-  pdl_begin();
-  extern __shared__ __align__(16) unsigned char ec_smem[];
-  __shared__ float s_m, s_inv;
-  const int e = blockIdx.y, sl = blockIdx.x, S = gridDim.x;
+// Stage 2 for (slice sl, expert e): ranks of the slice's candidates among all
+// of the expert's; ranks below C place the token.  Reads other CTAs' lists and
+// pairs through L2 (ld.global.cg), so the fused kernel may run it right after
+// its wait.  stage_smem: the lists are first copied to smem_lists.
+__device__ __forceinline__ void ec_rank_phase(int T, int C, int L, int S, int e, int sl,
+                                              const unsigned long long* __restrict__ cand,
+                                              const float2* __restrict__ stats, int stage_smem,
+                                              unsigned long long* smem_lists,
+                                              int32_t* __restrict__ ec_idx,
+                                              float* __restrict__ ec_score,
+                                              int32_t* __restrict__ pos, float* s_mi) {
   const unsigned long long* lists = cand + (size_t)e * S * L;
   if (stage_smem) {  // all S lists of this expert, staged once (16-byte pieces, 4 in flight)
-    unsigned long long* sl_ = reinterpret_cast<unsigned long long*>(ec_smem);
     const int n2 = S * L;  // u64 entries; the lists of one expert start 16-byte aligned
     const uint4* g4 = reinterpret_cast<const uint4*>(lists);
-    uint4* s4 = reinterpret_cast<uint4*>(sl_);
+    uint4* s4 = reinterpret_cast<uint4*>(smem_lists);
     const int n4 = n2 >> 1;
     const int nt = blockDim.x;
     int i = threadIdx.x;
     if (n2 & 1) i = n4;  // an odd count may leave the lists 8-byte aligned: scalar loads only
     for (; i + 3 * nt < n4; i += 4 * nt) {
-      const uint4 a = g4[i], b = g4[i + nt], c = g4[i + 2 * nt], d = g4[i + 3 * nt];
+      const uint4 a = __ldcg(g4 + i), b = __ldcg(g4 + i + nt), c = __ldcg(g4 + i + 2 * nt),
+                  d = __ldcg(g4 + i + 3 * nt);
       s4[i] = a;
       s4[i + nt] = b;
       s4[i + 2 * nt] = c;
       s4[i + 3 * nt] = d;
     }
-    for (; i < n4; i += nt) s4[i] = g4[i];
+    for (; i < n4; i += nt) s4[i] = __ldcg(g4 + i);
     if (n2 & 1)
-      for (int j = threadIdx.x; j < n2; j += nt) sl_[j] = lists[j];
-    lists = sl_;
+      for (int j = threadIdx.x; j < n2; j += nt) smem_lists[j] = __ldcg(lists + j);
+    lists = smem_lists;
   }
   if (threadIdx.x == 0) {  // the column's softmax denominator, slices in order
     const float2* st = stats + (size_t)e * S;
-    float m = st[0].x;
-    for (int i = 1; i < S; ++i) m = fmaxf(m, st[i].x);
+    float m = __ldcg(st).x;
+    for (int i = 1; i < S; ++i) m = fmaxf(m, __ldcg(st + i).x);
     float sum = 0.f;
-    for (int i = 0; i < S; ++i) sum += st[i].y * expf(st[i].x - m);
-    s_m = m;
-    s_inv = 1.0f / sum;
+    for (int i = 0; i < S; ++i) {
+      const float2 p = __ldcg(st + i);
+      sum += p.y * expf(p.x - m);
+    }
+    s_mi[0] = m;
+    s_mi[1] = 1.0f / sum;
   }
   __syncthreads();
-  const float m = s_m, inv = s_inv;
+  const float m = s_mi[0], inv = s_mi[1];
   const unsigned long long* mine = lists + (size_t)sl * L;
   for (int c = threadIdx.x; c < L; c += blockDim.x) {
-    const unsigned long long key = mine[c];
+    const unsigned long long key = stage_smem ? mine[c] : __ldcg(mine + c);
     if ((key >> 32) == 0xFFFFFFFFull) continue;  // past the slice end
     int rank = c;
     for (int j = 0; j < S && rank < C; ++j)
@@ -224,20 +240,108 @@ __global__ void __launch_bounds__(kEcRankThreads)
   }
 }
 
+__global__ void __launch_bounds__(kEcSlice)
+    ec_slice_kernel(int T, int E, int C, int L, int32_t* __restrict__ pos,
+                    unsigned long long* __restrict__ cand, float2* __restrict__ stats) {
+  pdl_begin();
+  __shared__ unsigned long long s_buf[2][kEcSlice];
+  __shared__ float scratch[32];
+  ec_slice_phase(T, C, L, gridDim.x, blockIdx.y, blockIdx.x, pos, cand, stats, s_buf, scratch);
+}
+
+__global__ void __launch_bounds__(kEcRankThreads)
+    ec_rank_kernel(int T, int E, int C, int L, const unsigned long long* __restrict__ cand,
+                   const float2* __restrict__ stats, int stage_smem, int32_t* __restrict__ ec_idx,
+                   float* __restrict__ ec_score, int32_t* __restrict__ pos) {
+  pdl_begin();
+  extern __shared__ __align__(16) unsigned char ec_smem[];
+  __shared__ float s_mi[2];
+  ec_rank_phase(T, C, L, gridDim.x, blockIdx.y, blockIdx.x, cand, stats, stage_smem,
+                reinterpret_cast<unsigned long long*>(ec_smem), ec_idx, ec_score, pos, s_mi);
+}
+
+// Both stages in one cooperative launch (every CTA resident): after its stage 1
+// a CTA counts itself in arrive[e] and waits, bounded, until all S slices of its
+// expert have posted, then runs stage 2.  arrive must be zero on entry.  A wait
+// that gives up records kErrEcWait and skips stage 2.
+constexpr uint32_t kErrEcWait = 16u;
+constexpr uint64_t kEcWaitTimeoutNs = 1000000000ull;
+
+__global__ void __launch_bounds__(kEcSlice)
+    ec_select_kernel(int T, int E, int C, int L, int32_t* __restrict__ pos,
+                     unsigned long long* __restrict__ cand, float2* __restrict__ stats,
+                     int stage_smem, int32_t* __restrict__ ec_idx, float* __restrict__ ec_score,
+                     int* __restrict__ arrive) {
+  pdl_begin();
+  extern __shared__ __align__(16) unsigned char ec_smem[];
+  __shared__ unsigned long long s_buf[2][kEcSlice];
+  __shared__ float scratch[32];
+  __shared__ float s_mi[2];
+  __shared__ int s_ok;
+  const int e = blockIdx.y, sl = blockIdx.x, S = gridDim.x;
+  ec_slice_phase(T, C, L, S, e, sl, pos, cand, stats, s_buf, scratch);
+  if (C <= 0) return;
+  __threadfence();  // this CTA's list, pair and pos entries before its arrival
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicAdd(arrive + e, 1);
+    volatile int* a = arrive + e;
+    int ok = 1;
+    const uint64_t t0 = global_timer_ns();
+    while (*a < S) {
+      if (global_timer_ns() - t0 > kEcWaitTimeoutNs) {
+        record_error(kErrEcWait);
+        ok = 0;
+        break;
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  ec_rank_phase(T, C, L, S, e, sl, cand, stats, stage_smem,
+                reinterpret_cast<unsigned long long*>(ec_smem), ec_idx, ec_score, pos, s_mi);
+}
+
 // Stage 1 and stage 2 on the logits already transposed into pos ([E, T], fp32
-// bits).  scratch: ec_scratch_bytes(T, E, C) bytes, 256-byte aligned.
+// bits).  scratch: ec_scratch_bytes(T, E, C) bytes, 256-byte aligned.  One
+// cooperative launch when the E * S CTAs fit on the GPU at once, else the two
+// stages as two launches.
 inline cudaError_t launch_ec_select(int T, int E, int C, int32_t* ec_idx, float* ec_score,
                                     int32_t* pos, void* scratch, cudaStream_t s) {
   const int S = ec_slices(T), L = ec_list_len(C > 0 ? C : 1);
   unsigned long long* cand = static_cast<unsigned long long*>(scratch);
-  float2* stats = reinterpret_cast<float2*>(static_cast<char*>(scratch) +
-                                            ((size_t)E * S * L * 8 + 255) / 256 * 256);
-  cudaError_t err = launch_k(ec_slice_kernel, dim3(S, E), dim3(kEcSlice), 0, s, nullptr, 0, T, E, C,
-                             L, pos, cand, stats);
-  if (err != cudaSuccess || C <= 0) return err;
+  char* tail = static_cast<char*>(scratch) + ((size_t)E * S * L * 8 + 255) / 256 * 256;
+  float2* stats = reinterpret_cast<float2*>(tail);
+  int* arrive = reinterpret_cast<int*>(tail + (((size_t)E * S * 8 + 255) / 256) * 256);
   const size_t lists_bytes = (size_t)S * L * 8;
   const int stage = lists_bytes <= kEcRankSmemMax ? 1 : 0;
   const size_t sm = stage ? lists_bytes : 0;
+  if (C > 0 && !ec_two_launches()) {
+    cudaError_t err = cudaFuncSetAttribute(ec_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kEcRankSmemMax);
+    if (err != cudaSuccess) return err;
+    int per_sm = 0, dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ec_select_kernel, kEcSlice, sm) ==
+            cudaSuccess &&
+        (long long)per_sm * sms >= (long long)S * E) {
+      err = cudaMemsetAsync(arrive, 0, (size_t)E * sizeof(int), s);
+      if (err != cudaSuccess) return err;
+      cudaLaunchAttribute coop;
+      coop.id = cudaLaunchAttributeCooperative;
+      coop.val.cooperative = 1;
+      err = launch_k(ec_select_kernel, dim3(S, E), dim3(kEcSlice), sm, s, &coop, 1, T, E, C, L, pos,
+                     cand, stats, stage, ec_idx, ec_score, arrive);
+      if (err == cudaSuccess) return err;
+      (void)cudaGetLastError();  // not launched: take the two-launch form
+    }
+  }
+  cudaError_t err = launch_k(ec_slice_kernel, dim3(S, E), dim3(kEcSlice), 0, s, nullptr, 0, T, E, C,
+                             L, pos, cand, stats);
+  if (err != cudaSuccess || C <= 0) return err;
   err = cudaFuncSetAttribute(ec_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kEcRankSmemMax);
   if (err != cudaSuccess) return err;
@@ -245,6 +349,5 @@ inline cudaError_t launch_ec_select(int T, int E, int C, int32_t* ec_idx, float*
                   (const unsigned long long*)cand, (const float2*)stats, stage, ec_idx, ec_score,
                   pos);
 }
-
 
 }  // namespace moe

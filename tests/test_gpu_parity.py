@@ -379,7 +379,11 @@ def _check_ec_layer(moe, torch, cfg):
     return assert_close_output(_np(y), y_ref, cfg.dtype, what=f"y[{cfg.name}]", ref_bf16_h=y_ref_h)
 
 
-def test_layer_small_expert_choice(moe, torch):
+@pytest.mark.parametrize("launches", ["one", "two"])
+def test_layer_small_expert_choice(moe, torch, launches, monkeypatch):
+    """The select as one cooperative launch (slices wait for their expert's other slices)
+    and as two launches."""
+    monkeypatch.setenv("MOE_EC_TWO_LAUNCHES", "1" if launches == "two" else "0")
     cfg = synth.LayerConfig("small_ec", T=500, d=128, F=256, E=6, k=0, dtype="bf16", x_std=1.0,
                             w_std=0.05, wg_std=0.1, seed=31, routing="expert_choice",
                             capacity_factor=1.5)
@@ -404,11 +408,13 @@ def test_layer_expert_choice_capacities(moe, torch, T, E, cf):
     _check_ec_layer(moe, torch, cfg)
 
 
+@pytest.mark.parametrize("launches", ["one", "two"])
 @pytest.mark.parametrize("T,E,cf", [(32768, 16, 2.0), (5000, 8, 1.0)], ids=["T32768_C4096", "T5000_C625"])
-def test_layer_expert_choice_many_slices(moe, torch, T, E, cf):
+def test_layer_expert_choice_many_slices(moe, torch, T, E, cf, launches, monkeypatch):
     """Token counts beyond one 1024-token slice per expert: 32 slices whose candidate
     lists are searched in global memory (too large to stage), and a capacity below the
-    slice length with a ragged last slice."""
+    slice length with a ragged last slice; one cooperative launch or two."""
+    monkeypatch.setenv("MOE_EC_TWO_LAUNCHES", "1" if launches == "two" else "0")
     cfg = synth.LayerConfig(f"ec_T{T}_E{E}", T=T, d=64, F=64, E=E, k=0, dtype="bf16", x_std=1.0,
                             w_std=0.05, wg_std=0.1, seed=36, routing="expert_choice",
                             capacity_factor=cf)
