@@ -231,8 +231,13 @@ def _weight_bytes(cfg, experts_used: int) -> float:
 def dominant_kernel(cfg, stages, peaks, peak_src, experts_used=None):
     """Roofline entry of the stage that takes the most time: the gate/up GEMM against the
     bf16 tensor peak when the expert segments are compute-bound, against HBM on its
-    weight bytes when they are not (fewer rows per expert than the ridge point)."""
+    weight bytes when they are not (fewer rows per expert than the ridge point).  The
+    fp32 workload (FFMA kernels, microseconds per launch) is launch-latency-bound and
+    has no roofline entry."""
     gu_ms = stages["gateup_ms"]
+    if cfg.dtype != "bf16":
+        return {"kernel": "grouped gate/up (fp32 FFMA)", "bound": "latency", "frac": None,
+                "note": "a few microseconds per launch; parity workload, not a throughput target"}
     flops = 4.0 * cfg.R * cfg.d * cfg.F
     used = cfg.E if experts_used is None else experts_used
     rows_per_expert = cfg.R / max(used, 1)
@@ -357,7 +362,7 @@ def run_gpu(args, cfg):
 
 
 # the other workloads reported beside the headline: (name, T override)
-SWEEP = (("top2_d1024", 0), ("fine_e64", 0), ("ec_e16", 0), ("large_d4096", 16),
+SWEEP = (("tiny_fp32", 0), ("top2_d1024", 0), ("fine_e64", 0), ("ec_e16", 0), ("large_d4096", 16),
          ("large_d4096", 256), ("large_d4096", 4096))
 
 
@@ -397,7 +402,8 @@ def sweep(moe, torch, dev, main_cfg, main_inp, main_w, flush, stream, peaks, pea
                "active_tflops": cfg.active_flops() / (ms / 1e3) / 1e12,
                "stages_ms": {k_: v for k_, v in stages.items() if k_ != "experts_used"},
                "dominant_kernel": dominant_kernel(cfg, stages, peaks, peak_src, used)}
-        rec["frac_of_bf16_burst"] = rec["active_tflops"] / peaks["bf16_tflops"]
+        rec["frac_of_bf16_burst"] = (rec["active_tflops"] / peaks["bf16_tflops"]
+                                     if cfg.dtype == "bf16" else None)
         if used is not None and rec["dominant_kernel"]["bound"] == "hbm":
             wb = _weight_bytes(cfg, used)
             rec["step_weight_bytes"] = wb
@@ -607,7 +613,7 @@ def run_reference(args, cfg):
     x64, wg64 = synth.to_f64(inp.x), synth.to_f64(inp.w_g)
     experts = _Pre(inp)
     rng = np.random.default_rng(11)
-    per_step = 128
+    per_step = min(128, cfg.T)
     for _ in range(args.warmup):
         _oracle_step(oracle, cfg, x64, wg64, experts, np.sort(rng.choice(cfg.T, per_step, replace=False)))
     t0 = time.perf_counter()
