@@ -52,6 +52,10 @@ ROUTER_CASES = [
     ("multi_bf16_e16", 1000, 512, 16, 2, "bf16", None),
     ("multi_bf16_e64", 1000, 512, 64, 4, "bf16", "zipf"),
     ("multi_bf16_e128", 333, 256, 128, 6, "bf16", None),
+    # more dispatch tiles per CTA than one MMA tile holds, not a multiple of it: each
+    # CTA's last, shorter tile goes through the second x map (32 or 64 rows)
+    ("rem_bf16_e8", 20000, 128, 8, 2, "bf16", None),
+    ("rem_bf16_e64", 40000, 128, 64, 4, "bf16", "zipf"),
 ]
 
 
@@ -269,6 +273,17 @@ def test_layer_small_bf16_multi_tile(moe, torch, E, k, router, monkeypatch):
         monkeypatch.setenv("MOE_ROUTER_TC", "1" if router == "tcgen05" else "0")
     cfg = synth.small_config(f"small_bf16_e{E}", 1000, 256, 384, E, k, "bf16", seed=21 + E,
                              x_std=1.0, w_std=0.02, wg_std=0.1)
+    _check_topk_layer(moe, torch, cfg)
+
+
+@pytest.mark.parametrize("E,k,T", [(8, 2, 20000), (64, 4, 40000)])
+def test_layer_tensor_core_router_short_last_tiles(moe, torch, E, k, T, monkeypatch):
+    """The tensor-core router with five dispatch tiles per CTA (MMA tiles of four or two,
+    then a shorter one through the second x map), through the dispatch counts, the aux
+    statistics and the whole layer."""
+    monkeypatch.setenv("MOE_ROUTER_TC", "1")
+    cfg = synth.small_config(f"short_tiles_e{E}", T, 128, 128, E, k, "bf16", seed=70 + E,
+                             x_std=1.0, w_std=0.05, wg_std=0.1, bias="zipf" if E > 16 else "none")
     _check_topk_layer(moe, torch, cfg)
 
 
