@@ -415,6 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t trow = tmem + (uint32_t)(acc * EN + col0) + ((uint32_t)(q * 32) << 16);
       float m = -INFINITY, inv = 0.f, lse = 0.f;
       float gk[8];  // half 0: the first 8 selected probabilities
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) gk[jj] = 0.f;
       if (k > 0 && tile_counts && h == 0) {  // expert counts, filled by the top-k below
         __syncwarp();  // the previous tile's counts have been read
         for (int e = lane; e < E; e += 32) S.cnt[q][e] = 0;
