@@ -297,6 +297,21 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])             \
       : "r"(taddr))
 
+// 16 TMEM lanes x 8 repetitions of 256 bits: thread i gets, for repetition j
+// (columns 8j .. 8j+7), r[4j], r[4j+1] = lane i/4, columns 8j + 2(i%4) + {0,1}
+// and r[4j+2], r[4j+3] = lane i/4 + 8, the same columns (the layout of an
+// m16n8 accumulator fragment, repeated along the columns).
+#define MOE_TMEM_LD16x256_X8(taddr, r)                                                             \
+  asm volatile(                                                                                   \
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14," \
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"              \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),       \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),   \
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),            \
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),            \
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])             \
+      : "r"(taddr))
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -361,7 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const int32_t* __restrict__ perm = nullptr,
                       const float* __restrict__ topk_w = nullptr, int kslots = 1,
                       const __nv_bfloat16* __restrict__ gx = nullptr,
-                      const int32_t* __restrict__ gsrc = nullptr, int gdiv = 1) {
+                      const int32_t* __restrict__ gsrc = nullptr, int gdiv = 1,
+                      int frag_store = 0) {
   static_assert(PAIRING == 0 || PAIRING == 2, "single CTA or 2-CTA pair");
   constexpr bool PAIR = PAIRING == 2, CL = PAIR;
   static_assert(!(PAIR && (GATHER || BN != 256)), "2-CTA MMA: 256-wide tiles without gather");
@@ -697,6 +713,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float wgt = (COMBINE && valid) ? topk_w[a] : 0.f;
         const int tok = a / kslots;
         float* Y = static_cast<float*>(out);
+        // plain stores go straight from the fragments, the combine's atomics through
+        // the staging (float4 additions covering four rows each measured faster)
+        const bool use_frag = frag_store == 2 ? !COMBINE : frag_store == 1;
+        if (use_frag) {
+          // straight from the 16x256b fragments: four lanes store one row's 32
+          // contiguous bytes per instruction (whole sectors), no shared memory
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {  // the warp's two 16-row halves
+            const int rl0 = hh * 16 + (lane >> 2), rl1 = rl0 + 8;  // rows within the warp's 32
+            const int g0 = rbase + rl0, g1 = rbase + rl1;
+            const int t0 = __shfl_sync(kFullMask, tok, rl0), t1 = __shfl_sync(kFullMask, tok, rl1);
+            const float w0 = __shfl_sync(kFullMask, wgt, rl0), w1 = __shfl_sync(kFullMask, wgt, rl1);
+            const bool v0 = g0 < c.row_end, v1 = g1 < c.row_end;
+            const uint32_t tq = taddr + ((uint32_t)(hh * 16) << 16);
+#pragma unroll 1
+            for (int cc = 0; cc < width; cc += 64) {
+              uint32_t v[32];
+              MOE_TMEM_LD16x256_X8(tq + cc, v);
+              tmem_ld_wait();
+              if (n0 + cc < N) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const int col = n0 + cc + 8 * j + 2 * (lane & 3);
+                  const float2 a0 = make_float2(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]));
+                  const float2 a1 = make_float2(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                  if (COMBINE) {
+                    if (v0) atomicAdd(reinterpret_cast<float2*>(Y + (size_t)t0 * N + col),
+                                      make_float2(w0 * a0.x, w0 * a0.y));
+                    if (v1) atomicAdd(reinterpret_cast<float2*>(Y + (size_t)t1 * N + col),
+                                      make_float2(w1 * a1.x, w1 * a1.y));
+                  } else {
+                    if (v0) *reinterpret_cast<float2*>(Y + (size_t)g0 * N + col) = a0;
+                    if (v1) *reinterpret_cast<float2*>(Y + (size_t)g1 * N + col) = a1;
+                  }
+                }
+              }
+            }
+          }
+        } else
 #pragma unroll 1
         for (int cc = 0; cc < width; cc += 32) {
           uint32_t v[32];
@@ -795,6 +850,19 @@ inline bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// How the down GEMM's epilogue writes: 1 = straight from 16x256b TMEM fragments,
+// 0 = through a shared-memory transpose into whole row segments, 2 = the first
+// for plain stores of Y and the second for the fused combine's atomics
+// (measured, whole layers alternating A/B: fine_e64 1001 against 1011 us;
+// top2_d1024 297 against 293 us, large_d4096 at T=4096 2023 against 2014 us).
+// MOE_DOWN_EPILOGUE in the environment ("frag", "staged") forces one.
+inline int down_frag_store() {
+  const char* v = getenv("MOE_DOWN_EPILOGUE");
+  if (v && v[0] == 'f') return 1;
+  if (v && v[0] == 's') return 0;
+  return 2;
+}
+
 inline int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -818,7 +886,7 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   const int grid = (int)std::min<long long>(sms, max_tiles);
   return launch_k(grouped_tc_kernel<GATEUP, BN, COMBINE, GATHER>, dim3(grid), dim3(kThreads), sm, s,
                   nullptr, 0, a, b0, b1, offsets, R, E, N, K, out, perm, topk_w, kslots, gx, gsrc,
-                  gdiv);
+                  gdiv, down_frag_store());
 }
 
 // How 256-wide launches pair CTAs: 2 = 2-CTA MMA (PAIR, the default), 0 =
@@ -870,7 +938,7 @@ cudaError_t launch_cluster(const CUtensorMap& a, const CUtensorMap& b0, const CU
   const int clusters = (int)std::min<long long>(max_clusters[dev], units);
   return launch_k(kern, dim3(2 * clusters), dim3(kThreads), sm, s, &attr, 1, a, b0, b1, offsets, R,
                   E, N, K, out, perm, topk_w, kslots, (const __nv_bfloat16*)nullptr,
-                  (const int32_t*)nullptr, 1);
+                  (const int32_t*)nullptr, 1, down_frag_store());
 }
 
 template <bool GATEUP, bool COMBINE>

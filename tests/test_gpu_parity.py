@@ -609,6 +609,27 @@ def test_cluster_paths_grouped_ragged(moe, torch, monkeypatch):
 
 
 @pytest.mark.parametrize("k", [2, 4])
+def test_down_epilogue_forms_bit_identical(moe, torch, k, monkeypatch):
+    """The down GEMM's epilogue storing straight from TMEM fragments equals the
+    shared-memory-staged form bit for bit: the same fp32 values stored, or (k <= 2, the
+    fused combine) the same two additions onto zero per element; ragged segments and a
+    split last wave (3000 tokens, 256-column tiles) included."""
+    cfg = synth.small_config("down_epi", 3000, 256, 512, 8, k, "bf16", seed=64, x_std=1.0, w_std=0.05)
+    inp = synth.make_inputs(cfg)
+    w = dev_weights(inp)
+    x = to_dev(inp.x)
+    outs = {}
+    for form in ("frag", "staged"):
+        monkeypatch.setenv("MOE_DOWN_EPILOGUE", form)
+        y = torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32, device="cuda")
+        moe.moe_layer_forward(x, w, k=k, y=y)
+        outs[form] = y
+    torch.cuda.synchronize()
+    assert not torch.isnan(outs["frag"]).any()
+    assert torch.equal(outs["frag"], outs["staged"])
+
+
+@pytest.mark.parametrize("k", [2, 4])
 def test_programmatic_dependent_launch_bit_identical(moe, torch, k, monkeypatch):
     """With programmatic dependent launch each kernel starts under the tail of the previous
     one but waits for its completion before touching memory: outputs equal the plainly
