@@ -8,18 +8,24 @@
 // Persistent, one CTA per SM, each owning a contiguous range of dispatch tiles
 // (SUB = 32 or 64 tokens) and taking them in MMA tiles of up to 128 tokens:
 //   warp 0     one thread streams, per 64-column k-block, the tile's x rows as
-//              32-row TMA boxes and the W_g k-block ([EN x 64], rows past E
+//              32-row TMA boxes and the W_g k-block ([NM x 64], rows past E
 //              zero-filled) into a ring of about 180 KiB; the whole range is
 //              requested as fast as the ring frees, so HBM sees every CTA's
 //              reads from the start;
 //   warp 1     allocates TMEM; one thread issues tcgen05.mma kind::f16
-//              (M = 128, N = EN, K = 16) into one of two accumulators;
-//   warps 2-5  epilogue, thread = token (TMEM lane): reads its logits row
-//              straight from TMEM in 16- or 32-column chunks, reduces max and
-//              sum of exponentials, selects the top-k by repeated arg-max on
-//              (logit desc, index asc), and reduces the statistics of its
-//              32 tokens with warp butterflies; for SUB = 64 two warps' sums are
-//              added in a fixed order through shared memory.
+//              (M = 128, N = NM, K = 16) into one of two accumulators;
+//   warps 2-9  epilogue, thread = token (TMEM lane): reads its logits row
+//              straight from TMEM, reduces max and sum of exponentials,
+//              selects the top-k by repeated arg-max on (logit desc, index
+//              asc), and reduces the statistics of its 32 tokens with warp
+//              butterflies.
+// The epilogue has two forms.  Up to 16 experts (EN = 8 or 16 columns read,
+// the MMA N at least 16) one warp holds a token's whole row: warps 2-5 take
+// the tiles of accumulator 0 and warps 6-9 those of accumulator 1, one warp per
+// TMEM lane quarter, and no warp exchanges anything with another.  From 32
+// experts on, two warps share each lane quarter, each holding half of every
+// row, and exchange partial maxima, sums and top-k candidates through shared
+// memory; for SUB = 64 two quarters' statistics are added in a fixed order.
 // With two accumulators the epilogue of one MMA tile overlaps the loads and
 // MMAs of the next.  Rows of a partial MMA tile beyond its tokens hold stale
 // shared memory; the MMA rows are independent, so only those TMEM lanes carry
@@ -64,10 +70,14 @@ constexpr int kRingBytes = 180 * 1024;
 constexpr int kRingPad = kMmaTok * kBK * 2;  // 16 KiB
 constexpr int kMaxStages = 32;
 
+// EN: logit columns the epilogue reads (8, 16, ... 256); NM: the MMA's N
+// (the smallest legal N for M = 128 is 16); SOLO: the one-warp-per-row epilogue.
 template <int EN>
 struct Cfg {
-  static constexpr int B_BYTES = EN * kBK * 2;
-  static constexpr uint32_t TMEM_COLS = 2 * EN < 32 ? 32 : 2 * EN;  // two accumulators
+  static constexpr int NM = EN < 16 ? 16 : EN;
+  static constexpr bool SOLO = EN <= 16;
+  static constexpr int B_BYTES = NM * kBK * 2;
+  static constexpr uint32_t TMEM_COLS = 2 * NM < 32 ? 32 : 2 * NM;  // two accumulators
 };
 
 __host__ __device__ constexpr int stage_bytes_for(int a_rows, int b_bytes) {
@@ -86,7 +96,8 @@ struct RSmem {  // after the ring and its pad
   uint32_t tmem_base;
   int abort_flag;
   float bias[MOE_MAX_EXPERTS];
-  int cnt[4][MOE_MAX_EXPERTS];    // per epilogue warp: expert counts of its 32 tokens
+  int cnt[4][MOE_MAX_EXPERTS];    // per lane quarter: expert counts of its 32 tokens
+  int cnt16[8][16];               // one-warp rows (E <= 16): per epilogue warp
   float gsum[4][MOE_MAX_EXPERTS]; // per lane quarter: column sums of g (SUB = 64 pairs)
   float zsum[4];
   float xf[2][2][kMmaTok];        // pair exchange of floats: [parity][half][row]
@@ -128,12 +139,17 @@ __device__ __forceinline__ void tmem_chunk(uint32_t taddr, uint32_t (&v)[CH]) {
   tc::tmem_ld_wait();
 }
 
-// Sum over the 32 lanes of each of the 32 values v[0..31] (a fixed butterfly):
-// on return lane l holds, in v[0], the sum over all lanes of v[l].
-__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32]) {
+// Sum over the 32 lanes of each of the N values v[0..N-1] (N = 8, 16 or 32):
+// a transpose within aligned groups of N lanes, then a butterfly across the
+// groups.  On return lane l holds, in v[0], the sum over all lanes of
+// v[l % N]; the order of the additions is fixed and every lane holding the
+// same column gets the same value.
+template <int N>
+__device__ __forceinline__ float warp_transpose_sum(float (&v)[N]) {
+  static_assert(N == 8 || N == 16 || N == 32, "row width");
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
+  for (int s = N / 2; s >= 1; s >>= 1) {
     const bool hi = (lane & s) != 0;
 #pragma unroll
     for (int i = 0; i < s; ++i) {
@@ -142,6 +158,8 @@ __device__ __forceinline__ float warp_transpose_sum32(float (&v)[32]) {
       v[i] = (hi ? v[i + s] : v[i]) + recv;
     }
   }
+#pragma unroll
+  for (int o = N; o < 32; o <<= 1) v[0] += __shfl_xor_sync(kFullMask, v[0], o);
   return v[0];
 }
 
@@ -230,8 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      int tpc, int tpm, int a_rows, int rem_rows) {
   using C = Cfg<EN>;
   using namespace tc;
-  constexpr int HC = EN / 2;  // columns per epilogue half
+  constexpr int HC = EN / 2;  // columns per epilogue half (two-warp rows)
   static_assert(SUB == 32 || SUB == 64, "dispatch tile");
+  static_assert(!C::SOLO || SUB == 32, "one-warp rows keep 32-token dispatch tiles");
   static_assert(stages_for(stage_bytes_for(kMmaTok, C::B_BYTES)) >= 2, "ring depth");
   const int STAGE_BYTES = stage_bytes_for(a_rows, C::B_BYTES);
   const int A_BYTES = a_rows * kBK * 2;
@@ -254,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&S.tmem_full[b], 1);
-      mbar_init(&S.tmem_empty[b], 8);  // one arrival per epilogue warp
+      mbar_init(&S.tmem_empty[b], C::SOLO ? 4 : 8);  // one arrival per epilogue warp of the tile
     }
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -325,14 +344,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = make_idesc_bf16(kMmaTok, EN);
+      constexpr uint32_t idesc = make_idesc_bf16(kMmaTok, C::NM);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int u = dt0; u < dt1 && ok; u += tpm) {
         if (!mbar_wait<false, true>(&S.tmem_empty[acc], acc_phase ^ 1u, abort_flag, kErrMma)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * EN);
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * C::NM);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait<false, true>(&S.full[stage], phase, abort_flag, kErrMma)) {
             ok = false;
@@ -372,303 +391,412 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // Eight warps, two per TMEM lane quarter: thread (q, h, lane) handles token
-    // row 32q + lane and the expert columns [h * HC, (h + 1) * HC) of it.  The
-    // pair exchanges its partial max and sum and, per top-k pass, its best
-    // candidate through shared memory (a named barrier per quarter); half 0
-    // writes the selection, counts and z sums.  Both warps of a pair run the
-    // same sequence of barriers whatever happens to a wait, so none can hang.
     const int ew = warp - 2;          // 0..7
     const int q = warp & 3;           // TMEM lane quarter: tile rows 32q .. 32q + 31
-    const int h = ew >> 2;            // column half
-    const int col0 = h * HC;
+    const int h = ew >> 2;            // warps 2-5: 0, warps 6-9: 1
     for (int e = threadIdx.x - 64; e < MOE_MAX_EXPERTS; e += kEpiThreads)
       S.bias[e] = (bias != nullptr && e < E) ? bias[e] : 0.f;
     epi_bar();
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    int xc = 0;  // pair exchanges so far
-    // the pair's max (either order gives the same value) and sum (half 0's first)
-    auto pair_max = [&](float v, int r) {
-      float o;
-      int oi;
-      pair_xchg(S, v, 0, o, oi, h, q, r, xc);
-      return fmaxf(v, o);
-    };
-    auto pair_sum = [&](float v, int r) {
-      float o;
-      int oi;
-      pair_xchg(S, v, 0, o, oi, h, q, r, xc);
-      return h == 0 ? v + o : o + v;
-    };
-    for (int u = dt0; u < dt1; u += tpm) {
-      const int tok0 = u * SUB;
-      const int ntok = min(min(dt1, u + tpm) * SUB, T) - tok0;
-      // a wait that gives up sets the abort flag (the error word records it); the
-      // warp still runs the tile's barriers, with garbage values
-      mbar_wait<false, true>(&S.tmem_full[acc], acc_phase, abort_flag, kErrEpilogue);
-      tc_fence_after();
-      const bool qlive = q * 32 < ntok;  // uniform over the pair
-      const int r = q * 32 + lane;       // tile row = TMEM lane
-      const bool live = qlive && r < ntok;
-      const int t = tok0 + r;
-      const uint32_t trow = tmem + (uint32_t)(acc * EN + col0) + ((uint32_t)(q * 32) << 16);
-      float m = -INFINITY, inv = 0.f, lse = 0.f;
-      float gk[8];  // half 0: the first 8 selected probabilities
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) gk[jj] = 0.f;
-      if (k > 0 && tile_counts && h == 0) {  // expert counts, filled by the top-k below
-        __syncwarp();  // the previous tile's counts have been read
-        for (int e = lane; e < E; e += 32) S.cnt[q][e] = 0;
-        __syncwarp();
-      }
-      if constexpr (HC <= 32) {
-        // this half's columns in registers; TMEM is released before any arithmetic
-        float sr[HC];
+    if constexpr (C::SOLO) {
+      // One warp per lane quarter and tile: thread (q, lane) holds all EN
+      // columns of token row 32q + lane; group h takes the MMA tiles of
+      // accumulator h (the even or the odd tiles of this CTA).
+      int ord = 0;  // MMA tiles of this CTA so far
+      for (int u = dt0; u < dt1; u += tpm, ++ord) {
+        const int acc = ord & 1;
+        if (acc != h) continue;
+        const uint32_t acc_phase = (uint32_t)(ord >> 1) & 1u;
+        const int tok0 = u * SUB;
+        const int ntok = min(min(dt1, u + tpm) * SUB, T) - tok0;
+        // a wait that gives up sets the abort flag (the error word records it)
+        mbar_wait<false, true>(&S.tmem_full[acc], acc_phase, abort_flag, kErrEpilogue);
+        tc_fence_after();
+        const bool qlive = q * 32 < ntok;  // warp-uniform: dispatch tile u + q is this CTA's
+        const int r = q * 32 + lane;       // tile row = TMEM lane
+        const bool live = qlive && r < ntok;
+        const int t = tok0 + r;
+        float sr[EN];
         if (qlive) {
-          uint32_t v[HC];
-          tmem_chunk<HC>(trow, v);
+          uint32_t v[EN];
+          tmem_chunk<EN>(tmem + (uint32_t)(acc * C::NM) + ((uint32_t)(q * 32) << 16), v);
 #pragma unroll
-          for (int i = 0; i < HC; ++i)
-            sr[i] = col0 + i < E ? __uint_as_float(v[i]) + S.bias[col0 + i] : -INFINITY;
+          for (int i = 0; i < EN; ++i) sr[i] = i < E ? __uint_as_float(v[i]) + S.bias[i] : -INFINITY;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.tmem_empty[acc]);
-        if (qlive) {
-          float ex[HC];
-          if (k > 0) {
-            m = pair_max(tree_max(sr), r);
+        if (!qlive) continue;
+        float m = -INFINITY, inv = 0.f, lse = 0.f;
+        float ex[EN];
+        if (k > 0) {
+          m = tree_max(sr);
 #pragma unroll
-            for (int i = 0; i < HC; ++i) ex[i] = col0 + i < E ? expf(sr[i] - m) : 0.f;
-            const float sum = pair_sum(tree_sum(ex), r);
-            inv = 1.0f / sum;
-            lse = m + logf(sum);
-          }
-          if (live) {
+          for (int i = 0; i < EN; ++i) ex[i] = i < E ? expf(sr[i] - m) : 0.f;
+          const float sum = tree_sum(ex);
+          inv = 1.0f / sum;
+          lse = m + logf(sum);
+        }
+        if (live) {
 #pragma unroll
-            for (int i = 0; i < HC; ++i) {
-              const int e = col0 + i;
-              if (e < E) {
-                if (logits_out) logits_out[(size_t)t * E + e] = sr[i];
-                if (logitsT) logitsT[(size_t)e * T + t] = sr[i];
-                if (k > 0 && probs_out) probs_out[(size_t)t * E + e] = ex[i] * inv;
-              }
-            }
-          }
-          if (k > 0 && aux_partials) {
-            float g[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) g[i] = (live && i < HC) ? ex[i % HC] * inv : 0.f;
-            const float colsum = warp_transpose_sum32(g);  // lane l: column col0 + l
-            if (lane < HC && col0 + lane < E) {
-              if (SUB == 32) aux_partials[(size_t)(u + q) * E + col0 + lane] = colsum;
-              else S.gsum[q][col0 + lane] = colsum;
-            }
-          }
-          if (k > 0) {
-            // top-k: each pass takes the better of the two halves' best remaining
-            // columns (ties to the lower index, which half 0 holds); the winner
-            // masks its pick to -inf
-            float selsum = 0.f;
-#pragma unroll 1
-            for (int j = 0; j < k; ++j) {
-              int bi;
-              float bv = tree_argmax(sr, bi);
-              bi += col0;
-              float ov;
-              int oi;
-              pair_xchg(S, bv, bi, ov, oi, h, q, r, xc);
-              const bool mine = h == 0 ? !(ov > bv) : (bv > ov);
-              float best = mine ? bv : ov;
-              int sel = mine ? bi : oi;
-#pragma unroll
-              for (int i = 0; i < HC; ++i) sr[i] = (mine && col0 + i == sel) ? -INFINITY : sr[i];
-              if (!(best > -INFINITY)) {  // only for non-finite logits: stay in range
-                sel = j < E ? j : 0;
-                best = -INFINITY;
-              }
-              const float gs = expf(best - m) * inv;  // same arithmetic as the probabilities
-              selsum += gs;
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) gk[jj] = jj == j ? gs : gk[jj];
-              if (live && h == 0) {
-                idx_out[(size_t)t * k + j] = sel;
-                w_out[(size_t)t * k + j] = gs;
-              }
-              if (tile_counts && h == 0) {  // one shared atomic per distinct expert of the warp
-                const unsigned peers = __match_any_sync(kFullMask, live ? sel : -1);
-                if (live && lane == __ffs(peers) - 1) atomicAdd(&S.cnt[q][sel], __popc(peers));
-              }
-            }
-            if (live && h == 0 && !(flags & MOE_ROUTE_NO_RENORM)) {
-              const float rs = 1.0f / selsum;
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj)
-                if (jj < k) w_out[(size_t)t * k + jj] = gk[jj] * rs;
-              for (int j = 8; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
+          for (int i = 0; i < EN; ++i) {
+            if (i < E) {
+              if (logits_out) logits_out[(size_t)t * E + i] = sr[i];
+              if (logitsT) logitsT[(size_t)i * T + t] = sr[i];
+              if (k > 0 && probs_out) probs_out[(size_t)t * E + i] = ex[i] * inv;
             }
           }
         }
-      } else {
-        // wide rows (E > 64): this half's columns in 32-column chunks, read from
-        // TMEM once per pass
-        if (qlive) {
-          if (k > 0) {
-            float mh = -INFINITY;
-#pragma unroll 1
-            for (int c = 0; c < HC; c += 32) {
-              uint32_t v[32];
-              tmem_chunk<32>(trow + c, v);
+        if (k == 0) continue;
+        const int tile = u + q;  // the dispatch tile of this quarter
+        if (aux_partials) {
+          float g[EN];
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (col0 + c + i < E) mh = fmaxf(mh, __uint_as_float(v[i]) + S.bias[col0 + c + i]);
-            }
-            m = pair_max(mh, r);
-            float sh = 0.f;
-#pragma unroll 1
-            for (int c = 0; c < HC; c += 32) {
-              uint32_t v[32];
-              tmem_chunk<32>(trow + c, v);
+          for (int i = 0; i < EN; ++i) g[i] = live ? ex[i] * inv : 0.f;
+          const float colsum = warp_transpose_sum<EN>(g);  // lane l: column l % EN
+          if (lane < E) aux_partials[(size_t)tile * E + lane] = colsum;
+        }
+        if (tile_counts) {
+          if (lane < 16) S.cnt16[ew][lane] = 0;
+          __syncwarp();
+        }
+        // top-k: repeated arg-max, each pick masked to -inf (ties to the lower index)
+        float gk[8];
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (col0 + c + i < E) sh += expf(__uint_as_float(v[i]) + S.bias[col0 + c + i] - m);
-            }
-            const float sum = pair_sum(sh, r);
-            inv = 1.0f / sum;
-            lse = m + logf(sum);
+        for (int jj = 0; jj < 8; ++jj) gk[jj] = 0.f;
+        float selsum = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+          int sel;
+          float best = tree_argmax(sr, sel);
+#pragma unroll
+          for (int i = 0; i < EN; ++i) sr[i] = i == sel ? -INFINITY : sr[i];
+          if (!(best > -INFINITY)) {  // only for non-finite logits: stay in range
+            sel = j < E ? j : 0;
+            best = -INFINITY;
           }
-#pragma unroll 1
-          for (int c = 0; c < HC; c += 32) {
-            uint32_t v[32];
-            tmem_chunk<32>(trow + c, v);
-            float g[32];
+          const float gs = expf(best - m) * inv;  // same arithmetic as the probabilities
+          selsum += gs;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int e = col0 + c + i;
-              const float s = __uint_as_float(v[i]) + S.bias[e < E ? e : 0];
-              g[i] = 0.f;
-              if (live && e < E) {
-                if (logits_out) logits_out[(size_t)t * E + e] = s;
-                if (logitsT) logitsT[(size_t)e * T + t] = s;
-                if (k > 0) {
-                  const float p = expf(s - m) * inv;
-                  if (probs_out) probs_out[(size_t)t * E + e] = p;
-                  g[i] = p;
+          for (int jj = 0; jj < 8; ++jj) gk[jj] = jj == j ? gs : gk[jj];
+          if (live) {
+            idx_out[(size_t)t * k + j] = sel;
+            w_out[(size_t)t * k + j] = gs;
+          }
+          if (tile_counts) {  // one shared atomic per distinct expert of the warp
+            const unsigned peers = __match_any_sync(kFullMask, live ? sel : -1);
+            if (live && lane == __ffs(peers) - 1) atomicAdd(&S.cnt16[ew][sel], __popc(peers));
+          }
+        }
+        if (live && !(flags & MOE_ROUTE_NO_RENORM)) {
+          const float rs = 1.0f / selsum;
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            if (jj < k) w_out[(size_t)t * k + jj] = gk[jj] * rs;
+          for (int j = 8; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
+        }
+        // per-dispatch-tile expert counts and z sums
+        float z = (live && z_partials) ? lse * lse : 0.f;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) z += __shfl_xor_sync(kFullMask, z, o);
+        if (tile_counts) {
+          __syncwarp();
+          if (lane < E) tile_counts[(size_t)tile * E + lane] = S.cnt16[ew][lane];
+        }
+        if (z_partials && lane == 0) z_partials[tile] = z;
+      }
+    } else {
+      // Two warps per TMEM lane quarter: thread (q, h, lane) handles token row
+      // 32q + lane and the expert columns [h * HC, (h + 1) * HC) of it.  The
+      // pair exchanges its partial max and sum and, per top-k pass, its best
+      // candidate through shared memory (a named barrier per quarter); half 0
+      // writes the selection, counts and z sums.  Both warps of a pair run the
+      // same sequence of barriers whatever happens to a wait, so none can hang.
+      const int col0 = h * HC;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      int xc = 0;  // pair exchanges so far
+      // the pair's max (either order gives the same value) and sum (half 0's first)
+      auto pair_max = [&](float v, int r) {
+        float o;
+        int oi;
+        pair_xchg(S, v, 0, o, oi, h, q, r, xc);
+        return fmaxf(v, o);
+      };
+      auto pair_sum = [&](float v, int r) {
+        float o;
+        int oi;
+        pair_xchg(S, v, 0, o, oi, h, q, r, xc);
+        return h == 0 ? v + o : o + v;
+      };
+      for (int u = dt0; u < dt1; u += tpm) {
+        const int tok0 = u * SUB;
+        const int ntok = min(min(dt1, u + tpm) * SUB, T) - tok0;
+        // a wait that gives up sets the abort flag (the error word records it); the
+        // warp still runs the tile's barriers, with garbage values
+        mbar_wait<false, true>(&S.tmem_full[acc], acc_phase, abort_flag, kErrEpilogue);
+        tc_fence_after();
+        const bool qlive = q * 32 < ntok;  // uniform over the pair
+        const int r = q * 32 + lane;       // tile row = TMEM lane
+        const bool live = qlive && r < ntok;
+        const int t = tok0 + r;
+        const uint32_t trow = tmem + (uint32_t)(acc * EN + col0) + ((uint32_t)(q * 32) << 16);
+        float m = -INFINITY, inv = 0.f, lse = 0.f;
+        float gk[8];  // half 0: the first 8 selected probabilities
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) gk[jj] = 0.f;
+        if (k > 0 && tile_counts && h == 0) {  // expert counts, filled by the top-k below
+          __syncwarp();  // the previous tile's counts have been read
+          for (int e = lane; e < E; e += 32) S.cnt[q][e] = 0;
+          __syncwarp();
+        }
+        if constexpr (HC <= 32) {
+          // this half's columns in registers; TMEM is released before any arithmetic
+          float sr[HC];
+          if (qlive) {
+            uint32_t v[HC];
+            tmem_chunk<HC>(trow, v);
+#pragma unroll
+            for (int i = 0; i < HC; ++i)
+              sr[i] = col0 + i < E ? __uint_as_float(v[i]) + S.bias[col0 + i] : -INFINITY;
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.tmem_empty[acc]);
+          if (qlive) {
+            float ex[HC];
+            if (k > 0) {
+              m = pair_max(tree_max(sr), r);
+#pragma unroll
+              for (int i = 0; i < HC; ++i) ex[i] = col0 + i < E ? expf(sr[i] - m) : 0.f;
+              const float sum = pair_sum(tree_sum(ex), r);
+              inv = 1.0f / sum;
+              lse = m + logf(sum);
+            }
+            if (live) {
+#pragma unroll
+              for (int i = 0; i < HC; ++i) {
+                const int e = col0 + i;
+                if (e < E) {
+                  if (logits_out) logits_out[(size_t)t * E + e] = sr[i];
+                  if (logitsT) logitsT[(size_t)e * T + t] = sr[i];
+                  if (k > 0 && probs_out) probs_out[(size_t)t * E + e] = ex[i] * inv;
                 }
               }
             }
             if (k > 0 && aux_partials) {
-              const float colsum = warp_transpose_sum32(g);  // lane l: column col0 + c + l
-              if (col0 + c + lane < E) {
-                if (SUB == 32) aux_partials[(size_t)(u + q) * E + col0 + c + lane] = colsum;
-                else S.gsum[q][col0 + c + lane] = colsum;
+              float g[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) g[i] = (live && i < HC) ? ex[i % HC] * inv : 0.f;
+              const float colsum = warp_transpose_sum<32>(g);  // lane l: column col0 + l
+              if (lane < HC && col0 + lane < E) {
+                if (SUB == 32) aux_partials[(size_t)(u + q) * E + col0 + lane] = colsum;
+                else S.gsum[q][col0 + lane] = colsum;
+              }
+            }
+            if (k > 0) {
+              // top-k: each pass takes the better of the two halves' best remaining
+              // columns (ties to the lower index, which half 0 holds); the winner
+              // masks its pick to -inf
+              float selsum = 0.f;
+#pragma unroll 1
+              for (int j = 0; j < k; ++j) {
+                int bi;
+                float bv = tree_argmax(sr, bi);
+                bi += col0;
+                float ov;
+                int oi;
+                pair_xchg(S, bv, bi, ov, oi, h, q, r, xc);
+                const bool mine = h == 0 ? !(ov > bv) : (bv > ov);
+                float best = mine ? bv : ov;
+                int sel = mine ? bi : oi;
+#pragma unroll
+                for (int i = 0; i < HC; ++i) sr[i] = (mine && col0 + i == sel) ? -INFINITY : sr[i];
+                if (!(best > -INFINITY)) {  // only for non-finite logits: stay in range
+                  sel = j < E ? j : 0;
+                  best = -INFINITY;
+                }
+                const float gs = expf(best - m) * inv;  // same arithmetic as the probabilities
+                selsum += gs;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) gk[jj] = jj == j ? gs : gk[jj];
+                if (live && h == 0) {
+                  idx_out[(size_t)t * k + j] = sel;
+                  w_out[(size_t)t * k + j] = gs;
+                }
+                if (tile_counts && h == 0) {  // one shared atomic per distinct expert of the warp
+                  const unsigned peers = __match_any_sync(kFullMask, live ? sel : -1);
+                  if (live && lane == __ffs(peers) - 1) atomicAdd(&S.cnt[q][sel], __popc(peers));
+                }
+              }
+              if (live && h == 0 && !(flags & MOE_ROUTE_NO_RENORM)) {
+                const float rs = 1.0f / selsum;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                  if (jj < k) w_out[(size_t)t * k + jj] = gk[jj] * rs;
+                for (int j = 8; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
               }
             }
           }
-          if (k > 0) {
-            // the j-th pick is the largest (logit, -index) strictly after the
-            // previous one, the better of the two halves' candidates
-            float pv = INFINITY, selsum = 0.f;
-            int pi = -1;
-#pragma unroll 1
-            for (int j = 0; j < k; ++j) {
-              float bv = -INFINITY;
-              int bi = -1;
+        } else {
+          // wide rows (E > 64): this half's columns in 32-column chunks, read from
+          // TMEM once per pass
+          if (qlive) {
+            if (k > 0) {
+              float mh = -INFINITY;
 #pragma unroll 1
               for (int c = 0; c < HC; c += 32) {
                 uint32_t v[32];
                 tmem_chunk<32>(trow + c, v);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const int e = col0 + c + i;
-                  if (e < E) {
-                    const float s = __uint_as_float(v[i]) + S.bias[e];
-                    const bool after = s < pv || (s == pv && e > pi);
-                    if (after && (bi < 0 ? s > -INFINITY : s > bv)) {
-                      bv = s;
-                      bi = e;
-                    }
+                for (int i = 0; i < 32; ++i)
+                  if (col0 + c + i < E) mh = fmaxf(mh, __uint_as_float(v[i]) + S.bias[col0 + c + i]);
+              }
+              m = pair_max(mh, r);
+              float sh = 0.f;
+#pragma unroll 1
+              for (int c = 0; c < HC; c += 32) {
+                uint32_t v[32];
+                tmem_chunk<32>(trow + c, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col0 + c + i < E) sh += expf(__uint_as_float(v[i]) + S.bias[col0 + c + i] - m);
+              }
+              const float sum = pair_sum(sh, r);
+              inv = 1.0f / sum;
+              lse = m + logf(sum);
+            }
+#pragma unroll 1
+            for (int c = 0; c < HC; c += 32) {
+              uint32_t v[32];
+              tmem_chunk<32>(trow + c, v);
+              float g[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int e = col0 + c + i;
+                const float s = __uint_as_float(v[i]) + S.bias[e < E ? e : 0];
+                g[i] = 0.f;
+                if (live && e < E) {
+                  if (logits_out) logits_out[(size_t)t * E + e] = s;
+                  if (logitsT) logitsT[(size_t)e * T + t] = s;
+                  if (k > 0) {
+                    const float p = expf(s - m) * inv;
+                    if (probs_out) probs_out[(size_t)t * E + e] = p;
+                    g[i] = p;
                   }
                 }
               }
-              float ov;
-              int oi;
-              pair_xchg(S, bv, bi, ov, oi, h, q, r, xc);
-              // half 0 holds the lower indices: it wins ties; no candidate loses
-              const bool mine = bi >= 0 && (oi < 0 || (h == 0 ? !(ov > bv) : (bv > ov)));
-              float best = mine ? bv : ov;
-              int sel = mine ? bi : oi;
-              if (sel < 0) {  // only for non-finite logits: stay in range
-                sel = j < E ? j : 0;
-                best = -INFINITY;
-              } else {
-                pv = best;
-                pi = sel;
-              }
-              const float gs = expf(best - m) * inv;  // same arithmetic as the probabilities
-              selsum += gs;
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) gk[jj] = jj == j ? gs : gk[jj];
-              if (live && h == 0) {
-                idx_out[(size_t)t * k + j] = sel;
-                w_out[(size_t)t * k + j] = gs;
-              }
-              if (tile_counts && h == 0) {  // one shared atomic per distinct expert of the warp
-                const unsigned peers = __match_any_sync(kFullMask, live ? sel : -1);
-                if (live && lane == __ffs(peers) - 1) atomicAdd(&S.cnt[q][sel], __popc(peers));
+              if (k > 0 && aux_partials) {
+                const float colsum = warp_transpose_sum<32>(g);  // lane l: column col0 + c + l
+                if (col0 + c + lane < E) {
+                  if (SUB == 32) aux_partials[(size_t)(u + q) * E + col0 + c + lane] = colsum;
+                  else S.gsum[q][col0 + c + lane] = colsum;
+                }
               }
             }
-            if (live && h == 0 && !(flags & MOE_ROUTE_NO_RENORM)) {
-              const float rs = 1.0f / selsum;
+            if (k > 0) {
+              // the j-th pick is the largest (logit, -index) strictly after the
+              // previous one, the better of the two halves' candidates
+              float pv = INFINITY, selsum = 0.f;
+              int pi = -1;
+#pragma unroll 1
+              for (int j = 0; j < k; ++j) {
+                float bv = -INFINITY;
+                int bi = -1;
+#pragma unroll 1
+                for (int c = 0; c < HC; c += 32) {
+                  uint32_t v[32];
+                  tmem_chunk<32>(trow + c, v);
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj)
-                if (jj < k) w_out[(size_t)t * k + jj] = gk[jj] * rs;
-              for (int j = 8; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
+                  for (int i = 0; i < 32; ++i) {
+                    const int e = col0 + c + i;
+                    if (e < E) {
+                      const float s = __uint_as_float(v[i]) + S.bias[e];
+                      const bool after = s < pv || (s == pv && e > pi);
+                      if (after && (bi < 0 ? s > -INFINITY : s > bv)) {
+                        bv = s;
+                        bi = e;
+                      }
+                    }
+                  }
+                }
+                float ov;
+                int oi;
+                pair_xchg(S, bv, bi, ov, oi, h, q, r, xc);
+                // half 0 holds the lower indices: it wins ties; no candidate loses
+                const bool mine = bi >= 0 && (oi < 0 || (h == 0 ? !(ov > bv) : (bv > ov)));
+                float best = mine ? bv : ov;
+                int sel = mine ? bi : oi;
+                if (sel < 0) {  // only for non-finite logits: stay in range
+                  sel = j < E ? j : 0;
+                  best = -INFINITY;
+                } else {
+                  pv = best;
+                  pi = sel;
+                }
+                const float gs = expf(best - m) * inv;  // same arithmetic as the probabilities
+                selsum += gs;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) gk[jj] = jj == j ? gs : gk[jj];
+                if (live && h == 0) {
+                  idx_out[(size_t)t * k + j] = sel;
+                  w_out[(size_t)t * k + j] = gs;
+                }
+                if (tile_counts && h == 0) {  // one shared atomic per distinct expert of the warp
+                  const unsigned peers = __match_any_sync(kFullMask, live ? sel : -1);
+                  if (live && lane == __ffs(peers) - 1) atomicAdd(&S.cnt[q][sel], __popc(peers));
+                }
+              }
+              if (live && h == 0 && !(flags & MOE_ROUTE_NO_RENORM)) {
+                const float rs = 1.0f / selsum;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                  if (jj < k) w_out[(size_t)t * k + jj] = gk[jj] * rs;
+                for (int j = 8; j < k; ++j) w_out[(size_t)t * k + j] *= rs;
+              }
             }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.tmem_empty[acc]);
-      }
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-      if (k == 0) continue;
-      // per-dispatch-tile expert counts (counted during the top-k) and z sums (half 0)
-      float z = (live && z_partials) ? lse * lse : 0.f;
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) z += __shfl_xor_sync(kFullMask, z, o);
-      if (SUB == 32) {
-        if (qlive && h == 0) {
+          tc_fence_before();
           __syncwarp();
-          const int tile = u + q;
-          if (tile_counts)
-            for (int e = lane; e < E; e += 32) tile_counts[(size_t)tile * E + e] = S.cnt[q][e];
-          if (z_partials && lane == 0) z_partials[tile] = z;
+          if (lane == 0) mbar_arrive(&S.tmem_empty[acc]);
         }
-      } else {
-        if (h == 0) {
-          if (lane == 0) S.zsum[q] = z;
-          if (!qlive)  // an empty quarter contributes nothing to its pair
-            for (int e = lane; e < E; e += 32) S.cnt[q][e] = 0;
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
         }
-        if (!qlive)
-          for (int e = col0 + lane; e < col0 + HC && e < E; e += 32) S.gsum[q][e] = 0.f;
-        epi_bar();
-        if ((q & 1) == 0 && qlive && h == 0) {  // quarters q, q+1 form dispatch tile u + q / 2
-          const int tile = u + (q >> 1);
-          for (int e = lane; e < E; e += 32) {
-            if (tile_counts) tile_counts[(size_t)tile * E + e] = S.cnt[q][e] + S.cnt[q + 1][e];
-            if (aux_partials) aux_partials[(size_t)tile * E + e] = S.gsum[q][e] + S.gsum[q + 1][e];
+        if (k == 0) continue;
+        // per-dispatch-tile expert counts (counted during the top-k) and z sums (half 0)
+        float z = (live && z_partials) ? lse * lse : 0.f;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) z += __shfl_xor_sync(kFullMask, z, o);
+        if (SUB == 32) {
+          if (qlive && h == 0) {
+            __syncwarp();
+            const int tile = u + q;
+            if (tile_counts)
+              for (int e = lane; e < E; e += 32) tile_counts[(size_t)tile * E + e] = S.cnt[q][e];
+            if (z_partials && lane == 0) z_partials[tile] = z;
           }
-          if (z_partials && lane == 0) z_partials[tile] = S.zsum[q] + S.zsum[q + 1];
+        } else {
+          if (h == 0) {
+            if (lane == 0) S.zsum[q] = z;
+            if (!qlive)  // an empty quarter contributes nothing to its pair
+              for (int e = lane; e < E; e += 32) S.cnt[q][e] = 0;
+          }
+          if (!qlive)
+            for (int e = col0 + lane; e < col0 + HC && e < E; e += 32) S.gsum[q][e] = 0.f;
+          epi_bar();
+          if ((q & 1) == 0 && qlive && h == 0) {  // quarters q, q+1 form dispatch tile u + q / 2
+            const int tile = u + (q >> 1);
+            for (int e = lane; e < E; e += 32) {
+              if (tile_counts) tile_counts[(size_t)tile * E + e] = S.cnt[q][e] + S.cnt[q + 1][e];
+              if (aux_partials) aux_partials[(size_t)tile * E + e] = S.gsum[q][e] + S.gsum[q + 1][e];
+            }
+            if (z_partials && lane == 0) z_partials[tile] = S.zsum[q] + S.zsum[q + 1];
+          }
+          epi_bar();  // the staging arrays are reused by the next tile
         }
-        epi_bar();  // the staging arrays are reused by the next tile
       }
-    }
+    }  // two-warp rows
   }
   tc_fence_before();
   __syncthreads();
@@ -727,15 +855,19 @@ inline cudaError_t launch_router(const void* x, const void* wg, const float* bia
   if (!bf16 || !rtc::tc_router_enabled(T, d, E))
     return launch_router_mma(x, wg, bias, T, d, E, k, bf16, idx, w, logits, probs, aux, st,
                              tile_counts, logitsT, flags, z_partials);
-  const int en = E <= 16 ? 16 : E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256;
+  const int en = E <= 8 ? 8 : E <= 16 ? 16 : E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256;
+  const int nm = en < 16 ? 16 : en;  // the MMA's N: W_g rows per box, past E zero-filled
   // the dispatch tile: router_tokens(E) tokens (32 up to E = 16, 64 above)
   const rtc::RouterPlan P(T, E, tc::sm_count());
   CUtensorMap mx, mx2, mw;
   if (!tc::make_map(&mx, x, (uint64_t)T, (uint64_t)d, (uint32_t)P.a_rows) ||
       !tc::make_map(&mx2, x, (uint64_t)T, (uint64_t)d, (uint32_t)(P.rem_rows > 0 ? P.rem_rows : P.a_rows)) ||
-      !tc::make_map(&mw, wg, (uint64_t)E, (uint64_t)d, (uint32_t)en))
+      !tc::make_map(&mw, wg, (uint64_t)E, (uint64_t)d, (uint32_t)nm))
     return cudaErrorInvalidValue;
   switch (en) {
+    case 8:
+      return rtc::launch_en<8, 32>(P, mx, mx2, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
+                                   tile_counts, logitsT, flags, z_partials, st);
     case 16:
       return rtc::launch_en<16, 32>(P, mx, mx2, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
                                     tile_counts, logitsT, flags, z_partials, st);

@@ -56,6 +56,11 @@ ROUTER_CASES = [
     # CTA's last, shorter tile goes through the second x map (32 or 64 rows)
     ("rem_bf16_e8", 20000, 128, 8, 2, "bf16", None),
     ("rem_bf16_e64", 40000, 128, 64, 4, "bf16", "zipf"),
+    # three MMA tiles per CTA (4 + 4 + 3 dispatch tiles, the last through the second x
+    # map): up to 16 experts both epilogue warp groups run, each over two accumulator
+    # phases
+    ("many_bf16_e5", 50000, 64, 5, 2, "bf16", None),
+    ("many_bf16_e16", 45000, 128, 16, 4, "bf16", None),
 ]
 
 
