@@ -16,17 +16,24 @@
 namespace moe {
 
 
+// Block-wide max and sum (blockDim a multiple of 32, at most 1024): a butterfly
+// in each warp, then warp 0 combines the warps' results the same way and
+// broadcasts through scratch[32].  The order of the additions is fixed, and every
+// thread returns the same value.  scratch holds 33 floats.
 __device__ __forceinline__ float block_reduce_max(float v, float* scratch) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, off));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) scratch[warp] = v;
   __syncthreads();
-  const int nw = blockDim.x >> 5;
-  float r = scratch[0];
-  for (int w = 1; w < nw; ++w) r = fmaxf(r, scratch[w]);
+  if (warp == 0) {
+    float r = lane < (int)(blockDim.x >> 5) ? scratch[lane] : -FLT_MAX;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) r = fmaxf(r, __shfl_xor_sync(kFullMask, r, off));
+    if (lane == 0) scratch[32] = r;
+  }
   __syncthreads();
-  return r;
+  return scratch[32];
 }
 
 __device__ __forceinline__ float block_reduce_sum(float v, float* scratch) {
@@ -35,11 +42,14 @@ __device__ __forceinline__ float block_reduce_sum(float v, float* scratch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) scratch[warp] = v;
   __syncthreads();
-  const int nw = blockDim.x >> 5;
-  float r = 0.f;
-  for (int w = 0; w < nw; ++w) r += scratch[w];  // fixed order
+  if (warp == 0) {
+    float r = lane < (int)(blockDim.x >> 5) ? scratch[lane] : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) r += __shfl_xor_sync(kFullMask, r, off);
+    if (lane == 0) scratch[32] = r;
+  }
   __syncthreads();
-  return r;
+  return scratch[32];
 }
 
 // Order-preserving map of a float to uint32 (ascending float -> ascending key).
@@ -61,17 +71,21 @@ __device__ __forceinline__ float order_key_float(uint32_t k) {
 // work instead of E.
 //   stage 1 (ec_slice_kernel): the slice's max and sum of exponentials (about
 //     its own max), its pos entries set to -1, and its (key, token) pairs
-//     sorted ascending (bitonic, shared memory), i.e. by descending logit then
-//     ascending token; the first L = min(C, kEcSlice) are the slice's
-//     candidates (past the slice end: sentinels above every real key).
+//     sorted ascending (bitonic within warps, then merge rounds in shared
+//     memory), i.e. by descending logit then ascending token; the first
+//     L = min(C, kEcSlice) are the slice's candidates (past the slice end:
+//     sentinels above every real key).
 //   stage 2 (ec_rank_kernel): every candidate's rank among all candidates of
 //     its expert is its index in its own list plus, for every other list, the
-//     number of entries below it (binary search).  Keys are unique (the token
-//     id is part of the key), and a token of the expert's top C has every
-//     token ahead of it within the first C of each slice, so those ranks are
-//     exact; any other candidate gets a rank of at least C.  Ranks below C
-//     place the token: ec_idx / ec_score at the rank, pos[e, t] = e * C + rank.
-//     The column's max and sum come from the slices' pairs in slice order.
+//     number of entries below it (binary search, one thread per candidate and
+//     list).  Keys are unique (the token id is part of the key), and a token
+//     of the expert's top C has every token ahead of it within the first C of
+//     each slice, so those ranks are exact; any other candidate gets a rank of
+//     at least C.  Ranks grow along a sorted list, so the candidates are taken
+//     in chunks from the front and the phase stops at the first chunk that
+//     reaches rank C.  Ranks below C place the token: ec_idx / ec_score at the
+//     rank, pos[e, t] = e * C + rank.  The column's max and sum come from the
+//     slices' pairs in slice order.
 constexpr int kEcSlice = 1024;            // tokens per stage-1 CTA (one per thread)
 constexpr int kEcRankThreads = 1024;
 constexpr size_t kEcRankSmemMax = 160 * 1024;  // candidate lists staged in shared memory up to this
@@ -186,7 +200,7 @@ __device__ __forceinline__ void ec_rank_phase(int T, int C, int L, int S, int e,
                                               unsigned long long* smem_lists,
                                               int32_t* __restrict__ ec_idx,
                                               float* __restrict__ ec_score,
-                                              int32_t* __restrict__ pos, float* s_mi) {
+                                              int32_t* __restrict__ pos, float* s_mi, int* s_cnt) {
   const unsigned long long* lists = cand + (size_t)e * S * L;
   if (stage_smem) {  // all S lists of this expert, staged once (16-byte pieces, 4 in flight)
     const int n2 = S * L;  // u64 entries; the lists of one expert start 16-byte aligned
@@ -224,19 +238,43 @@ __device__ __forceinline__ void ec_rank_phase(int T, int C, int L, int S, int e,
   __syncthreads();
   const float m = s_mi[0], inv = s_mi[1];
   const unsigned long long* mine = lists + (size_t)sl * L;
-  for (int c = threadIdx.x; c < L; c += blockDim.x) {
-    const unsigned long long key = stage_smem ? mine[c] : __ldcg(mine + c);
-    if ((key >> 32) == 0xFFFFFFFFull) continue;  // past the slice end
-    int rank = c;
-    for (int j = 0; j < S && rank < C; ++j)
-      if (j != sl) rank += count_below(lists + (size_t)j * L, L, key);
-    if (rank < C) {
-      const int t = (int)(key & 0xffffffffu);
-      const float v = order_key_float((uint32_t)(key >> 32) ^ 0xffffffffu);
-      ec_idx[(size_t)e * C + rank] = t;
-      ec_score[(size_t)e * C + rank] = expf(v - m) * inv;
-      pos[(size_t)e * T + t] = e * C + rank;
+  const int P = S - 1;  // the other lists
+  // Chunks of B keys, one thread per (key, list slot): slot jj searches the
+  // other lists jj, jj + J, ... (one list each unless there are more lists
+  // than threads).  Ranks grow along the sorted list, so the chunks stop after
+  // the first whose last key ranks at or beyond C (or runs past the list).
+  const int B = P > 0 ? max(1, (int)blockDim.x / P) : (int)blockDim.x;
+  const int J = (int)blockDim.x / B;  // list slots
+  const int kc = (int)threadIdx.x % B, jj = (int)threadIdx.x / B;
+#pragma unroll 1
+  for (int c0 = 0; c0 < L; c0 += B) {
+    const int c = c0 + kc;
+    const bool key_thread = jj == 0 && c < L;
+    unsigned long long key = 0ull;
+    bool real = false;
+    if (c < L && jj < J) {
+      key = stage_smem ? mine[c] : __ldcg(mine + c);
+      real = (key >> 32) != 0xFFFFFFFFull;  // else past the slice end
+      int cnt = 0;
+      if (real)
+        for (int q = jj; q < P; q += J) cnt += count_below(lists + (size_t)(q < sl ? q : q + 1) * L, L, key);
+      s_cnt[jj * B + kc] = cnt;
     }
+    __syncthreads();
+    bool more = false;
+    if (key_thread) {
+      int rank = c;
+      for (int q = 0; q < J; ++q) rank += s_cnt[q * B + kc];
+      if (real && rank < C) {
+        const int t = (int)(key & 0xffffffffu);
+        const float v = order_key_float((uint32_t)(key >> 32) ^ 0xffffffffu);
+        ec_idx[(size_t)e * C + rank] = t;
+        ec_score[(size_t)e * C + rank] = expf(v - m) * inv;
+        pos[(size_t)e * T + t] = e * C + rank;
+      }
+      more = (kc == B - 1) && real && rank < C;  // the chunk's last key still places a token
+    }
+    if (!__syncthreads_or(more)) break;  // also keeps s_cnt until every key thread read it
   }
 }
 
@@ -245,7 +283,7 @@ __global__ void __launch_bounds__(kEcSlice)
                     unsigned long long* __restrict__ cand, float2* __restrict__ stats) {
   pdl_begin();
   __shared__ unsigned long long s_buf[2][kEcSlice];
-  __shared__ float scratch[32];
+  __shared__ float scratch[33];
   ec_slice_phase(T, C, L, gridDim.x, blockIdx.y, blockIdx.x, pos, cand, stats, s_buf, scratch);
 }
 
@@ -256,8 +294,9 @@ __global__ void __launch_bounds__(kEcRankThreads)
   pdl_begin();
   extern __shared__ __align__(16) unsigned char ec_smem[];
   __shared__ float s_mi[2];
+  __shared__ int s_cnt[kEcRankThreads];
   ec_rank_phase(T, C, L, gridDim.x, blockIdx.y, blockIdx.x, cand, stats, stage_smem,
-                reinterpret_cast<unsigned long long*>(ec_smem), ec_idx, ec_score, pos, s_mi);
+                reinterpret_cast<unsigned long long*>(ec_smem), ec_idx, ec_score, pos, s_mi, s_cnt);
 }
 
 // Both stages in one cooperative launch (every CTA resident): after its stage 1
@@ -275,9 +314,10 @@ __global__ void __launch_bounds__(kEcSlice)
   pdl_begin();
   extern __shared__ __align__(16) unsigned char ec_smem[];
   __shared__ unsigned long long s_buf[2][kEcSlice];
-  __shared__ float scratch[32];
+  __shared__ float scratch[33];
   __shared__ float s_mi[2];
   __shared__ int s_ok;
+  __shared__ int s_cnt[kEcSlice];
   const int e = blockIdx.y, sl = blockIdx.x, S = gridDim.x;
   ec_slice_phase(T, C, L, S, e, sl, pos, cand, stats, s_buf, scratch);
   if (C <= 0) return;
@@ -301,7 +341,7 @@ __global__ void __launch_bounds__(kEcSlice)
   __syncthreads();
   if (!s_ok) return;
   ec_rank_phase(T, C, L, S, e, sl, cand, stats, stage_smem,
-                reinterpret_cast<unsigned long long*>(ec_smem), ec_idx, ec_score, pos, s_mi);
+                reinterpret_cast<unsigned long long*>(ec_smem), ec_idx, ec_score, pos, s_mi, s_cnt);
 }
 
 // Stage 1 and stage 2 on the logits already transposed into pos ([E, T], fp32

@@ -6,12 +6,14 @@
 // (expert counts, column sums of g, sums of squared log-sum-exps).
 //
 // Persistent, one CTA per SM, each owning a contiguous range of dispatch tiles
-// (SUB = 32 or 64 tokens) and taking them in MMA tiles of up to 128 tokens:
-//   warp 0     one thread streams, per 64-column k-block, the tile's x rows as
-//              32-row TMA boxes and the W_g k-block ([NM x 64], rows past E
-//              zero-filled) into a ring of about 180 KiB; the whole range is
-//              requested as fast as the ring frees, so HBM sees every CTA's
-//              reads from the start;
+// (SUB = 32 or 64 tokens; the ranges of all SMs differ by one tile at most)
+// and taking them in MMA tiles of up to 128 tokens:
+//   warp 0     one thread streams, per 64-column k-block, the tile's x rows
+//              (one TMA box; a CTA's shorter last tile one box per dispatch
+//              tile) and the W_g k-block ([NM x 64],
+//              rows past E zero-filled) into a ring of about 180 KiB; the whole
+//              range is requested as fast as the ring frees, so HBM sees every
+//              CTA's reads from the start;
 //   warp 1     allocates TMEM; one thread issues tcgen05.mma kind::f16
 //              (M = 128, N = NM, K = 16) into one of two accumulators;
 //   warps 2-9  epilogue, thread = token (TMEM lane): reads its logits row
@@ -60,12 +62,12 @@ constexpr int kBK = 64;        // K per stage: one 128-byte swizzled row per tok
         "=r"(r[14]), "=r"(r[15])                                                                  \
       : "r"(taddr))
 
-// The ring is cut at run time into stages of [a_rows x 64] x plus [EN x 64] W_g
+// The ring is cut at run time into stages of [a_rows x 64] x plus [NM x 64] W_g
 // (1 KiB-aligned), a_rows the most tokens any CTA's MMA tile holds, so that a
 // launch of small tiles keeps as many x bytes in flight as one of full tiles.
-// The MMA still reads 128 rows of A from a stage's start; rows past a_rows lie
-// in the next stage or, for the last one, in the pad after the ring, and only
-// reach TMEM lanes no thread reads.
+// The MMA still reads 128 rows of A from a stage's start; rows past the tile's
+// tokens lie in the next stage or, for the last one, in the pad after the
+// ring, and only reach TMEM lanes no thread reads.
 constexpr int kRingBytes = 180 * 1024;
 constexpr int kRingPad = kMmaTok * kBK * 2;  // 16 KiB
 constexpr int kMaxStages = 32;
@@ -191,7 +193,7 @@ __device__ __forceinline__ float tree_sum(const float (&v)[N]) {
 // Largest entry and its index; the left operand of every comparison holds the
 // lower indices, and it keeps ties, so equal values go to the lower index.
 template <int N>
-__device__ __forceinline__ float tree_argmax(const float (&v)[N], int& idx) {
+__host__ __device__ __forceinline__ float tree_argmax(const float (&v)[N], int& idx) {
   float t[N];
   int ix[N];
 #pragma unroll
@@ -211,47 +213,118 @@ __device__ __forceinline__ float tree_argmax(const float (&v)[N], int& idx) {
   return t[0];
 }
 
+// The top-k of a row of N logits held in registers (N = 8 G, G <= 4): the
+// best remaining entry of each group of 8 columns is kept, so a pick re-scans
+// only the 8 columns of its own group instead of the row.  Comparisons keep
+// the left (lower-column) operand on ties, within a group and across groups,
+// so equal logits go to the lower column, as with a scan of the whole row.
+template <int N>
+struct RowTopK {
+  static_assert(N % 8 == 0 && N <= 32, "groups of 8 columns, at most 32");
+  static constexpr int G = N / 8;
+  float gv[G];     // best remaining logit of each group
+  int gi[G];       // its column
+  uint32_t taken;  // columns picked so far
+
+  __host__ __device__ __forceinline__ void init(const float (&v)[N]) {
+    taken = 0u;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float t[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) t[i] = v[8 * g + i];
+      int li;
+      gv[g] = tree_argmax(t, li);
+      gi[g] = 8 * g + li;
+    }
+  }
+  // the best remaining (logit, column)
+  __host__ __device__ __forceinline__ float best(int& col) const {
+    float t[G];
+    int c[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      t[g] = gv[g];
+      c[g] = gi[g];
+    }
+#pragma unroll
+    for (int w = G / 2; w >= 1; w >>= 1)
+#pragma unroll
+      for (int g = 0; g < w; ++g) {
+        const bool right = t[2 * g + 1] > t[2 * g];
+        t[g] = right ? t[2 * g + 1] : t[2 * g];
+        c[g] = right ? c[2 * g + 1] : c[2 * g];
+      }
+    col = c[0];
+    return t[0];
+  }
+  // when pick holds: mark column col taken and re-scan its group
+  __host__ __device__ __forceinline__ void take(const float (&v)[N], int col, bool pick) {
+    taken |= pick ? 1u << col : 0u;
+    const int grp = col >> 3;
+    const uint32_t tk = taken >> (8 * grp);
+    float t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float x = v[i];
+#pragma unroll
+      for (int g = 1; g < G; ++g) x = grp == g ? v[8 * g + i] : x;
+      t[i] = (tk >> i) & 1u ? -INFINITY : x;
+    }
+    int li;
+    const float nv = tree_argmax(t, li);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const bool upd = pick && g == grp;
+      gv[g] = upd ? nv : gv[g];
+      gi[g] = upd ? 8 * grp + li : gi[g];
+    }
+  }
+};
+
 __device__ __forceinline__ void epi_bar() {  // the eight epilogue warps
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
 
-// Work split (host side, RouterPlan): every CTA owns tpc consecutive dispatch
-// tiles of SUB tokens (the last CTA what remains) and takes them in MMA tiles
-// of tpm dispatch tiles, a_rows = tpm * SUB tokens, each loaded per k-block
-// by one TMA box of a_rows rows.  A CTA whose tpc is not a multiple of tpm
-// ends with a tile of rem = tpc % tpm dispatch tiles, loaded through a second
-// map whose box holds rem * SUB rows, so that no CTA reads another's rows; the
-// last CTA's short tile reads past T, which TMA fills with zeros.
+// Work split (host side, RouterPlan): the ndt dispatch tiles of SUB tokens
+// are dealt over grid = min(SMs, ndt) CTAs in consecutive ranges, base tiles
+// each and one more for the first `extra` CTAs, so every SM streams and no
+// two ranges differ by more than one tile.  A CTA takes its range in MMA
+// tiles of up to tpm dispatch tiles (tpm * SUB <= 128 tokens); per k-block a
+// shorter tile's dispatch tiles come in one TMA box of SUB rows each, so no CTA reads
+// another's rows, and the last tile's box reads past T as zeros.  A full MMA
+// tile's rows come in one box of tpm * SUB rows instead (measured faster than
+// tpm boxes at E <= 16).
 struct RouterPlan {
-  int sub, ndt, tpc, grid, tpm, a_rows, rem_rows;
+  int sub, ndt, grid, base, extra, tpm;
   RouterPlan(int T, int E, int sms) {
     sub = E <= 16 ? 32 : 64;
     ndt = T <= 0 ? 0 : (T + sub - 1) / sub;
-    tpc = ndt <= 0 ? 1 : (ndt + sms - 1) / sms;
-    grid = ndt <= 0 ? 0 : (ndt + tpc - 1) / tpc;
-    tpm = std::min(tpc, kMmaTok / sub);
-    a_rows = tpm * sub;
-    rem_rows = (tpc % tpm) * sub;
+    grid = ndt <= 0 ? 0 : std::min(sms, ndt);
+    base = grid > 0 ? ndt / grid : 0;
+    extra = grid > 0 ? ndt % grid : 0;
+    tpm = std::max(1, std::min(base + (extra > 0 ? 1 : 0), kMmaTok / sub));
   }
 };
 
 template <int EN, int SUB>
 __global__ void __launch_bounds__(kThreads, 1)
-    router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmX2,
+    router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXs,
                      const __grid_constant__ CUtensorMap tmW,
                      const float* __restrict__ bias, int T, int d, int E, int k,
                      int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                      float* __restrict__ logits_out, float* __restrict__ probs_out,
                      float* __restrict__ aux_partials, int32_t* __restrict__ tile_counts,
                      float* __restrict__ logitsT, int flags, float* __restrict__ z_partials,
-                     int tpc, int tpm, int a_rows, int rem_rows) {
+                     int base, int extra, int tpm) {
   using C = Cfg<EN>;
   using namespace tc;
   constexpr int HC = EN / 2;  // columns per epilogue half (two-warp rows)
   static_assert(SUB == 32 || SUB == 64, "dispatch tile");
   static_assert(!C::SOLO || SUB == 32, "one-warp rows keep 32-token dispatch tiles");
   static_assert(stages_for(stage_bytes_for(kMmaTok, C::B_BYTES)) >= 2, "ring depth");
+  const int a_rows = tpm * SUB;  // tokens of the largest MMA tile
   const int STAGE_BYTES = stage_bytes_for(a_rows, C::B_BYTES);
   const int A_BYTES = a_rows * kBK * 2;
   const int STAGES = stages_for(STAGE_BYTES);
@@ -263,8 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = d / kBK;
   const int ndt = (T + SUB - 1) / SUB;
-  const int dt0 = blockIdx.x * tpc, dt1 = min(ndt, dt0 + tpc);  // this CTA's dispatch tiles
-  const bool last_cta = blockIdx.x == gridDim.x - 1;
+  // this CTA's dispatch tiles [dt0, dt1)
+  const int dt0 = (int)blockIdx.x * base + min((int)blockIdx.x, extra);
+  const int dt1 = min(ndt, dt0 + base + ((int)blockIdx.x < extra ? 1 : 0));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -279,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tensormap(&tmX);
-    if (rem_rows > 0) prefetch_tensormap(&tmX2);
+    prefetch_tensormap(&tmXs);
     prefetch_tensormap(&tmW);
   }
   if (warp == 1) {
@@ -305,11 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0, issued_phase = 0;
       bool ok = true;
       for (int u = dt0; u < dt1 && ok; u += tpm) {
-        const int tok0 = u * SUB;
-        // a short tile of a CTA other than the last: the remainder box
-        const bool rem = dt1 - u < tpm && !last_cta;
-        const CUtensorMap* mapX = rem ? &tmX2 : &tmX;
-        const uint32_t bytes = (uint32_t)((rem ? rem_rows : a_rows) * kBK * 2 + C::B_BYTES);
+        const int nsub = min(tpm, dt1 - u);  // dispatch tiles in this MMA tile
+        const uint32_t bytes = (uint32_t)(nsub * SUB * kBK * 2 + C::B_BYTES);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait<false, true>(&S.empty[stage], phase ^ 1u, abort_flag, kErrProducer)) {
             ok = false;
@@ -317,7 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           unsigned char* sA = ring + (size_t)stage * STAGE_BYTES;
           mbar_arrive_expect_tx(&S.full[stage], bytes);
-          tma_load_2d(sA, mapX, &S.full[stage], kb * kBK, tok0);
+          if (nsub == tpm) {  // a full tile: one box of a_rows rows
+            tma_load_2d(sA, &tmX, &S.full[stage], kb * kBK, u * SUB);
+          } else {
+            for (int j = 0; j < nsub; ++j)
+              tma_load_2d(sA + j * SUB * kBK * 2, &tmXs, &S.full[stage], kb * kBK, (u + j) * SUB);
+          }
           tma_load_2d(sA + A_BYTES, &tmW, &S.full[stage], kb * kBK, 0);
           issued |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -459,7 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane < 16) S.cnt16[ew][lane] = 0;
           __syncwarp();
         }
-        // top-k: repeated arg-max, each pick masked to -inf (ties to the lower index)
+        // top-k: repeated arg-max over the remaining columns (ties to the lower index)
+        RowTopK<EN> tk;
+        tk.init(sr);
         float gk[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) gk[jj] = 0.f;
@@ -467,9 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int j = 0; j < k; ++j) {
           int sel;
-          float best = tree_argmax(sr, sel);
-#pragma unroll
-          for (int i = 0; i < EN; ++i) sr[i] = i == sel ? -INFINITY : sr[i];
+          float best = tk.best(sel);
+          tk.take(sr, sel, true);
           if (!(best > -INFINITY)) {  // only for non-finite logits: stay in range
             sel = j < E ? j : 0;
             best = -INFINITY;
@@ -584,10 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             if (k > 0 && aux_partials) {
-              float g[32];
+              float g[HC];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) g[i] = (live && i < HC) ? ex[i % HC] * inv : 0.f;
-              const float colsum = warp_transpose_sum<32>(g);  // lane l: column col0 + l
+              for (int i = 0; i < HC; ++i) g[i] = live ? ex[i] * inv : 0.f;
+              const float colsum = warp_transpose_sum<HC>(g);  // lane l: column col0 + l % HC
               if (lane < HC && col0 + lane < E) {
                 if (SUB == 32) aux_partials[(size_t)(u + q) * E + col0 + lane] = colsum;
                 else S.gsum[q][col0 + lane] = colsum;
@@ -596,21 +673,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k > 0) {
               // top-k: each pass takes the better of the two halves' best remaining
               // columns (ties to the lower index, which half 0 holds); the winner
-              // masks its pick to -inf
+              // marks its pick taken
+              RowTopK<HC> tk;
+              tk.init(sr);
               float selsum = 0.f;
 #pragma unroll 1
               for (int j = 0; j < k; ++j) {
                 int bi;
-                float bv = tree_argmax(sr, bi);
-                bi += col0;
+                float bv = tk.best(bi);  // bi: column within this half
                 float ov;
                 int oi;
-                pair_xchg(S, bv, bi, ov, oi, h, q, r, xc);
+                pair_xchg(S, bv, col0 + bi, ov, oi, h, q, r, xc);
                 const bool mine = h == 0 ? !(ov > bv) : (bv > ov);
+                tk.take(sr, bi, mine);
                 float best = mine ? bv : ov;
-                int sel = mine ? bi : oi;
-#pragma unroll
-                for (int i = 0; i < HC; ++i) sr[i] = (mine && col0 + i == sel) ? -INFINITY : sr[i];
+                int sel = mine ? col0 + bi : oi;
                 if (!(best > -INFINITY)) {  // only for non-finite logits: stay in range
                   sel = j < E ? j : 0;
                   best = -INFINITY;
@@ -809,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int EN, int SUB>
-cudaError_t launch_en(const RouterPlan& P, const CUtensorMap& mx, const CUtensorMap& mx2,
+cudaError_t launch_en(const RouterPlan& P, const CUtensorMap& mx, const CUtensorMap& mxs,
                       const CUtensorMap& mw, const float* bias, int T, int d, int E, int k,
                       int32_t* idx, float* w, float* logits, float* probs, float* aux,
                       int32_t* tile_counts, float* logitsT, int flags, float* z_partials,
@@ -819,9 +896,9 @@ cudaError_t launch_en(const RouterPlan& P, const CUtensorMap& mx, const CUtensor
   auto kern = router_tc_kernel<EN, SUB>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  return launch_k(kern, dim3(P.grid), dim3(kThreads), sm, st, nullptr, 0, mx, mx2, mw, bias, T, d, E,
-                  k, idx, w, logits, probs, aux, tile_counts, logitsT, flags, z_partials, P.tpc, P.tpm,
-                  P.a_rows, P.rem_rows);
+  return launch_k(kern, dim3(P.grid), dim3(kThreads), sm, st, nullptr, 0, mx, mxs, mw, bias, T, d, E, k,
+                  idx, w, logits, probs, aux, tile_counts, logitsT, flags, z_partials, P.base, P.extra,
+                  P.tpm);
 }
 
 // Which bf16 router runs (measured, CUDA events with the stream held, L2
@@ -859,29 +936,29 @@ inline cudaError_t launch_router(const void* x, const void* wg, const float* bia
   const int nm = en < 16 ? 16 : en;  // the MMA's N: W_g rows per box, past E zero-filled
   // the dispatch tile: router_tokens(E) tokens (32 up to E = 16, 64 above)
   const rtc::RouterPlan P(T, E, tc::sm_count());
-  CUtensorMap mx, mx2, mw;
-  if (!tc::make_map(&mx, x, (uint64_t)T, (uint64_t)d, (uint32_t)P.a_rows) ||
-      !tc::make_map(&mx2, x, (uint64_t)T, (uint64_t)d, (uint32_t)(P.rem_rows > 0 ? P.rem_rows : P.a_rows)) ||
+  CUtensorMap mx, mxs, mw;
+  if (!tc::make_map(&mx, x, (uint64_t)T, (uint64_t)d, (uint32_t)(P.tpm * P.sub)) ||
+      !tc::make_map(&mxs, x, (uint64_t)T, (uint64_t)d, (uint32_t)P.sub) ||
       !tc::make_map(&mw, wg, (uint64_t)E, (uint64_t)d, (uint32_t)nm))
     return cudaErrorInvalidValue;
   switch (en) {
     case 8:
-      return rtc::launch_en<8, 32>(P, mx, mx2, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
+      return rtc::launch_en<8, 32>(P, mx, mxs, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
                                    tile_counts, logitsT, flags, z_partials, st);
     case 16:
-      return rtc::launch_en<16, 32>(P, mx, mx2, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
+      return rtc::launch_en<16, 32>(P, mx, mxs, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
                                     tile_counts, logitsT, flags, z_partials, st);
     case 32:
-      return rtc::launch_en<32, 64>(P, mx, mx2, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
+      return rtc::launch_en<32, 64>(P, mx, mxs, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
                                     tile_counts, logitsT, flags, z_partials, st);
     case 64:
-      return rtc::launch_en<64, 64>(P, mx, mx2, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
+      return rtc::launch_en<64, 64>(P, mx, mxs, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
                                     tile_counts, logitsT, flags, z_partials, st);
     case 128:
-      return rtc::launch_en<128, 64>(P, mx, mx2, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
+      return rtc::launch_en<128, 64>(P, mx, mxs, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
                                      tile_counts, logitsT, flags, z_partials, st);
     default:
-      return rtc::launch_en<256, 64>(P, mx, mx2, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
+      return rtc::launch_en<256, 64>(P, mx, mxs, mw, bias, T, d, E, k, idx, w, logits, probs, aux,
                                      tile_counts, logitsT, flags, z_partials, st);
   }
 }
