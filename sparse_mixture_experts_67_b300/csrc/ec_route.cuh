@@ -193,11 +193,13 @@ __device__ __forceinline__ void ec_slice_phase(int T, int C, int L, int S, int e
 // Stage 2 for (slice sl, expert e): ranks of the slice's candidates among all
 // of the expert's; ranks below C place the token.  Reads other CTAs' lists and
 // pairs through L2 (ld.global.cg), so the fused kernel may run it right after
-// its wait.  stage_smem: the lists are first copied to smem_lists.
+// its wait.  stage_smem: the lists are first copied to s_lists in shared
+// memory; the searches then read shared memory, else the lists in global
+// memory (two separate pointers, so that each path keeps its own address space).
 __device__ __forceinline__ void ec_rank_phase(int T, int C, int L, int S, int e, int sl,
                                               const unsigned long long* __restrict__ cand,
                                               const float2* __restrict__ stats, int stage_smem,
-                                              unsigned long long* smem_lists,
+                                              unsigned long long* s_lists,
                                               int32_t* __restrict__ ec_idx,
                                               float* __restrict__ ec_score,
                                               int32_t* __restrict__ pos, float* s_mi, int* s_cnt) {
@@ -205,7 +207,7 @@ __device__ __forceinline__ void ec_rank_phase(int T, int C, int L, int S, int e,
   if (stage_smem) {  // all S lists of this expert, staged once (16-byte pieces, 4 in flight)
     const int n2 = S * L;  // u64 entries; the lists of one expert start 16-byte aligned
     const uint4* g4 = reinterpret_cast<const uint4*>(lists);
-    uint4* s4 = reinterpret_cast<uint4*>(smem_lists);
+    uint4* s4 = reinterpret_cast<uint4*>(s_lists);
     const int n4 = n2 >> 1;
     const int nt = blockDim.x;
     int i = threadIdx.x;
@@ -220,8 +222,7 @@ __device__ __forceinline__ void ec_rank_phase(int T, int C, int L, int S, int e,
     }
     for (; i < n4; i += nt) s4[i] = __ldcg(g4 + i);
     if (n2 & 1)
-      for (int j = threadIdx.x; j < n2; j += nt) smem_lists[j] = __ldcg(lists + j);
-    lists = smem_lists;
+      for (int j = threadIdx.x; j < n2; j += nt) s_lists[j] = __ldcg(lists + j);
   }
   if (threadIdx.x == 0) {  // the column's softmax denominator, slices in order
     const float2* st = stats + (size_t)e * S;
@@ -237,7 +238,6 @@ __device__ __forceinline__ void ec_rank_phase(int T, int C, int L, int S, int e,
   }
   __syncthreads();
   const float m = s_mi[0], inv = s_mi[1];
-  const unsigned long long* mine = lists + (size_t)sl * L;
   const int P = S - 1;  // the other lists
   // Chunks of B keys, one thread per (key, list slot): slot jj searches the
   // other lists jj, jj + J, ... (one list each unless there are more lists
@@ -253,11 +253,15 @@ __device__ __forceinline__ void ec_rank_phase(int T, int C, int L, int S, int e,
     unsigned long long key = 0ull;
     bool real = false;
     if (c < L && jj < J) {
-      key = stage_smem ? mine[c] : __ldcg(mine + c);
+      const size_t at = (size_t)sl * L + c;
+      key = stage_smem ? s_lists[at] : __ldcg(lists + at);
       real = (key >> 32) != 0xFFFFFFFFull;  // else past the slice end
       int cnt = 0;
       if (real)
-        for (int q = jj; q < P; q += J) cnt += count_below(lists + (size_t)(q < sl ? q : q + 1) * L, L, key);
+        for (int q = jj; q < P; q += J) {
+          const size_t o = (size_t)(q < sl ? q : q + 1) * L;
+          cnt += stage_smem ? count_below(s_lists + o, L, key) : count_below(lists + o, L, key);
+        }
       s_cnt[jj * B + kc] = cnt;
     }
     __syncthreads();
