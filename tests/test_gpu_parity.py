@@ -61,6 +61,12 @@ ROUTER_CASES = [
     # phases
     ("many_bf16_e5", 50000, 64, 5, 2, "bf16", None),
     ("many_bf16_e16", 45000, 128, 16, 4, "bf16", None),
+    # more than 8 picks (the kernels hold the first 8 weights in registers and
+    # rescale the rest in memory): one-warp rows, two-warp rows, wide rows, fp32
+    ("k12_bf16_e16", 300, 64, 16, 12, "bf16", None),
+    ("k10_bf16_e64", 500, 128, 64, 10, "bf16", "zipf"),
+    ("k12_bf16_e256", 300, 64, 256, 12, "bf16", None),
+    ("k9_f32_e12", 200, 32, 12, 9, "f32", None),
 ]
 
 
@@ -289,6 +295,18 @@ def test_layer_tensor_core_router_short_last_tiles(moe, torch, E, k, T, monkeypa
     monkeypatch.setenv("MOE_ROUTER_TC", "1")
     cfg = synth.small_config(f"short_tiles_e{E}", T, 128, 128, E, k, "bf16", seed=70 + E,
                              x_std=1.0, w_std=0.05, wg_std=0.1, bias="zipf" if E > 16 else "none")
+    _check_topk_layer(moe, torch, cfg)
+
+
+@pytest.mark.parametrize("E,k,router", [(256, 8, "auto"), (64, 10, "auto"), (256, 8, "warp_mma")])
+def test_layer_most_experts_and_picks(moe, torch, E, k, router, monkeypatch):
+    """The largest expert count the library takes (E = 256, wide router rows read in
+    32-column chunks, 256 expert segments) and more than 8 picks per token, through
+    the whole layer and the separate combine."""
+    if router != "auto":
+        monkeypatch.setenv("MOE_ROUTER_TC", "0")
+    cfg = synth.small_config(f"most_e{E}_k{k}", 3000, 128, 128, E, k, "bf16", seed=80 + E + k,
+                             x_std=1.0, w_std=0.05, wg_std=0.1)
     _check_topk_layer(moe, torch, cfg)
 
 
