@@ -52,12 +52,13 @@ ROUTER_CASES = [
     ("multi_bf16_e16", 1000, 512, 16, 2, "bf16", None),
     ("multi_bf16_e64", 1000, 512, 64, 4, "bf16", "zipf"),
     ("multi_bf16_e128", 333, 256, 128, 6, "bf16", None),
-    # more dispatch tiles per CTA than one MMA tile holds, not a multiple of it: each
-    # CTA's last, shorter tile goes through the second x map (32 or 64 rows)
+    # more dispatch tiles per CTA than one MMA tile holds (625 tiles over 148 CTAs: 4 or
+    # 5 each), not a multiple of it: a CTA's last, shorter MMA tile is loaded as one box
+    # per dispatch tile (32 or 64 rows)
     ("rem_bf16_e8", 20000, 128, 8, 2, "bf16", None),
     ("rem_bf16_e64", 40000, 128, 64, 4, "bf16", "zipf"),
-    # three MMA tiles per CTA (4 + 4 + 3 dispatch tiles, the last through the second x
-    # map): up to 16 experts both epilogue warp groups run, each over two accumulator
+    # three MMA tiles per CTA (4 + 4 + 2 or 4 + 4 + 3 dispatch tiles, the last one
+    # shorter): up to 16 experts both epilogue warp groups run, each over two accumulator
     # phases
     ("many_bf16_e5", 50000, 64, 5, 2, "bf16", None),
     ("many_bf16_e16", 45000, 128, 16, 4, "bf16", None),
@@ -289,9 +290,9 @@ def test_layer_small_bf16_multi_tile(moe, torch, E, k, router, monkeypatch):
 
 @pytest.mark.parametrize("E,k,T", [(8, 2, 20000), (64, 4, 40000)])
 def test_layer_tensor_core_router_short_last_tiles(moe, torch, E, k, T, monkeypatch):
-    """The tensor-core router with five dispatch tiles per CTA (MMA tiles of four or two,
-    then a shorter one through the second x map), through the dispatch counts, the aux
-    statistics and the whole layer."""
+    """The tensor-core router with four or five dispatch tiles per CTA (MMA tiles of four
+    or two, then a shorter one loaded as one box per dispatch tile), through the dispatch
+    counts, the aux statistics and the whole layer."""
     monkeypatch.setenv("MOE_ROUTER_TC", "1")
     cfg = synth.small_config(f"short_tiles_e{E}", T, 128, 128, E, k, "bf16", seed=70 + E,
                              x_std=1.0, w_std=0.05, wg_std=0.1, bias="zipf" if E > 16 else "none")
