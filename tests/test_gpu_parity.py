@@ -68,6 +68,12 @@ ROUTER_CASES = [
     ("k10_bf16_e64", 500, 128, 64, 10, "bf16", "zipf"),
     ("k12_bf16_e256", 300, 64, 256, 12, "bf16", None),
     ("k9_f32_e12", 200, 32, 12, 9, "f32", None),
+    # one token; one expert; long token ranges (126-127 dispatch tiles per CTA: each
+    # epilogue warp group cycles its accumulator through 16 MMA tiles)
+    ("one_token_bf16_e8", 1, 64, 8, 2, "bf16", None),
+    ("single_bf16_e1", 40, 64, 1, 1, "bf16", None),
+    ("long_bf16_e8", 600000, 64, 8, 2, "bf16", None),
+    ("long_bf16_e64", 300000, 64, 64, 4, "bf16", "zipf"),
 ]
 
 
