@@ -70,6 +70,9 @@ ROUTER_CASES = [
     ("k9_f32_e12", 200, 32, 12, 9, "f32", None),
     # one token; one expert; long token ranges (126-127 dispatch tiles per CTA: each
     # epilogue warp group cycles its accumulator through 16 MMA tiles)
+    # 17-32 experts (8 columns per epilogue warp) and a wide row with padding columns
+    ("e24_bf16", 700, 128, 24, 3, "bf16", "zipf"),
+    ("e100_bf16", 600, 64, 100, 5, "bf16", None),
     ("one_token_bf16_e8", 1, 64, 8, 2, "bf16", None),
     ("single_bf16_e1", 40, 64, 1, 1, "bf16", None),
     ("long_bf16_e8", 600000, 64, 8, 2, "bf16", None),
