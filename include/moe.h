@@ -94,6 +94,23 @@ const char* moe_status_string(moe_status status);
  * synchronises the device; it is a diagnostic, not part of the hot path. */
 moe_status moe_device_error(uint32_t* word, int clear);
 
+/* Self-test of the bounded waits.  Runs the expert-choice selection that
+ * moe_expert_choice_route runs (T tokens, E experts, C picks per expert; pos
+ * holds the logits transposed, [E,T] fp32 bits) as its one cooperative launch,
+ * with every expert's count of arrived slices started far below zero, so that
+ * the wait of each CTA for its expert's other slices is never satisfied.  Each
+ * such wait gives up after its limit (1 s), records code 16 in the device error
+ * word and returns, writing no picks: the launch ends and the context stays
+ * usable.  ec_idx [E,C], ec_score [E,C] and pos are left undefined; ws as for
+ * moe_expert_choice_route (at least moe_expert_choice_workspace_size for the
+ * same T, E and C).  Errors: MOE_ERR_INVALID_ARG for T < 1, E outside 1..256,
+ * C outside 1..T or a NULL array; MOE_ERR_WORKSPACE; MOE_ERR_UNSUPPORTED when the
+ * E * ceil(T / 1024) CTAs cannot all be resident at once (the two-launch form
+ * has no such wait).  A diagnostic that takes about a second, not part of the
+ * hot path. */
+moe_status moe_selftest_wait_expiry(int T, int E, int C, int32_t* ec_idx, float* ec_score,
+                                    int32_t* pos, void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ router
  * Token-choice router ([moe-theory] MoELayer.route; [moe-intro] s = W_g x,
  * g = softmax(s), TopK; [sparse-moe] TopKGating; bias as in [zh-moe]

@@ -24,7 +24,7 @@ __all__ = [
     "moe_grouped_gateup_swiglu_gather",
     "moe_grouped_down", "moe_experts_swiglu", "moe_combine", "moe_ec_combine", "moe_aux_loss",
     "moe_layer_forward", "moe_layer_workspace_size", "moe_route_aux_rows", "moe_device_error",
-    "MoELayer", "HostPipeline",
+    "moe_selftest_wait_expiry", "MoELayer", "HostPipeline",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -68,6 +68,7 @@ _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
     "moe_status_string": ([_I], ctypes.c_char_p),
     "moe_device_error": ([ctypes.POINTER(ctypes.c_uint32), _I], _I),
+    "moe_selftest_wait_expiry": ([_I, _I, _I, _P, _P, _P, _P, _Z, _P], _I),
     "moe_route_aux_rows": ([_I], _Z),
     "moe_route": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P], _I),
     "moe_expert_choice_capacity": ([_I, _I, _F], _I),
@@ -183,6 +184,23 @@ def moe_device_error(clear: bool = True) -> int:
     word = ctypes.c_uint32(0)
     _check("moe_device_error", lib().moe_device_error(ctypes.byref(word), int(clear)))
     return word.value
+
+
+def moe_selftest_wait_expiry(T: int, E: int, capacity_factor: float) -> None:
+    """Runs the expert-choice selection with waits that nothing satisfies (see
+    include/moe.h): each gives up after its bound and sets code 16 in the device
+    error word, which the caller reads with moe_device_error()."""
+    C = moe_expert_choice_capacity(T, E, capacity_factor)
+    dev = torch.device("cuda")
+    pos = torch.zeros((E, T), dtype=torch.int32, device=dev)  # all logits 0.0
+    ec_idx = torch.empty((E, max(C, 1)), dtype=torch.int32, device=dev)
+    ec_score = torch.empty((E, max(C, 1)), dtype=torch.float32, device=dev)
+    nbytes = moe_expert_choice_workspace_size(T, E, capacity_factor)
+    ws = torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=dev)
+    _check("moe_selftest_wait_expiry",
+           lib().moe_selftest_wait_expiry(T, E, C, _ptr(ec_idx), _ptr(ec_score), _ptr(pos), _ptr(ws),
+                                          nbytes, _stream()))
+    torch.cuda.synchronize()
 
 
 def moe_route_aux_rows(T: int) -> int:

@@ -352,8 +352,13 @@ __global__ void __launch_bounds__(kEcSlice)
 // bits).  scratch: ec_scratch_bytes(T, E, C) bytes, 256-byte aligned.  One
 // cooperative launch when the E * S CTAs fit on the GPU at once, else the two
 // stages as two launches.
+// arrive_fill: the byte the arrival counts start from (0; the bounded-wait
+// self-test starts them far below zero, 0x80 bytes, so that no expert's slices
+// ever all arrive).  one_launch_only: return cudaErrorNotSupported instead of
+// taking the two-launch form.
 inline cudaError_t launch_ec_select(int T, int E, int C, int32_t* ec_idx, float* ec_score,
-                                    int32_t* pos, void* scratch, cudaStream_t s) {
+                                    int32_t* pos, void* scratch, cudaStream_t s,
+                                    int arrive_fill = 0, bool one_launch_only = false) {
   const int S = ec_slices(T), L = ec_list_len(C > 0 ? C : 1);
   unsigned long long* cand = static_cast<unsigned long long*>(scratch);
   char* tail = static_cast<char*>(scratch) + ((size_t)E * S * L * 8 + 255) / 256 * 256;
@@ -372,17 +377,18 @@ inline cudaError_t launch_ec_select(int T, int E, int C, int32_t* ec_idx, float*
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ec_select_kernel, kEcSlice, sm) ==
             cudaSuccess &&
         (long long)per_sm * sms >= (long long)S * E) {
-      err = cudaMemsetAsync(arrive, 0, (size_t)E * sizeof(int), s);
+      err = cudaMemsetAsync(arrive, arrive_fill, (size_t)E * sizeof(int), s);
       if (err != cudaSuccess) return err;
       cudaLaunchAttribute coop;
       coop.id = cudaLaunchAttributeCooperative;
       coop.val.cooperative = 1;
       err = launch_k(ec_select_kernel, dim3(S, E), dim3(kEcSlice), sm, s, &coop, 1, T, E, C, L, pos,
                      cand, stats, stage, ec_idx, ec_score, arrive);
-      if (err == cudaSuccess) return err;
+      if (err == cudaSuccess || one_launch_only) return err;
       (void)cudaGetLastError();  // not launched: take the two-launch form
     }
   }
+  if (one_launch_only) return cudaErrorNotSupported;
   cudaError_t err = launch_k(ec_slice_kernel, dim3(S, E), dim3(kEcSlice), 0, s, nullptr, 0, T, E, C,
                              L, pos, cand, stats);
   if (err != cudaSuccess || C <= 0) return err;

@@ -80,6 +80,21 @@ moe_status moe_device_error(uint32_t* word, int clear) {
   return cuda_status(e);
 }
 
+moe_status moe_selftest_wait_expiry(int T, int E, int C, int32_t* ec_idx, float* ec_score,
+                                    int32_t* pos, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (T <= 0 || E < 1 || E > MOE_MAX_EXPERTS || C < 1 || C > T || !ec_idx || !ec_score || !pos)
+    return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < ec_scratch_bytes(T, E, C) + 256) return MOE_ERR_WORKSPACE;
+  char* scratch = static_cast<char*>(ws) + ((256 - (reinterpret_cast<uintptr_t>(ws) & 255)) & 255);
+  const cudaError_t e = launch_ec_select(T, E, C, ec_idx, ec_score, pos, scratch,
+                                         (cudaStream_t)stream, 0x80, true);
+  if (e == cudaErrorNotSupported) {
+    (void)cudaGetLastError();
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return cuda_status(e);
+}
+
 // Rows for the smallest router block (an upper bound for every E).
 size_t moe_route_aux_rows(int T) { return T <= 0 ? 0 : (size_t)ceil_div(T, kRouterTokensMin); }
 

@@ -89,6 +89,20 @@ def test_expert_choice_argument_errors(L):
     assert big >= 16 * 40 * 1024 * 8
 
 
+def test_wait_expiry_selftest_argument_errors(L):
+    z = _nullp()
+    ws = L.moe_expert_choice_workspace_size(8192, 16, 2.0)
+    # T, E or C out of range, or a NULL array: refused before any launch
+    assert L.moe_selftest_wait_expiry(0, 16, 1, _p(), _p(), _p(), _p(), ws, z) == 1
+    assert L.moe_selftest_wait_expiry(8192, 0, 1024, _p(), _p(), _p(), _p(), ws, z) == 1
+    assert L.moe_selftest_wait_expiry(8192, 16, 0, _p(), _p(), _p(), _p(), ws, z) == 1
+    assert L.moe_selftest_wait_expiry(8192, 16, 9000, _p(), _p(), _p(), _p(), ws, z) == 1
+    assert L.moe_selftest_wait_expiry(8192, 16, 1024, _p(), z, _p(), _p(), ws, z) == 1
+    # the selection's scratch: missing or one byte short
+    assert L.moe_selftest_wait_expiry(8192, 16, 1024, _p(), _p(), _p(), z, ws, z) == 3
+    assert L.moe_selftest_wait_expiry(8192, 16, 1024, _p(), _p(), _p(), _p(), ws - 1, z) == 3
+
+
 def test_permute_and_experts_errors(L):
     z = _nullp()
     ws = L.moe_permute_workspace_size(100, 8, 2)

@@ -488,6 +488,26 @@ def test_expert_choice_route_exact_ties(moe, torch):
 
 
 @pytest.mark.slow
+def test_bounded_wait_expiry_reports_and_recovers(moe, torch):
+    """A barrier wait that nothing satisfies gives up after its bound: the expert-choice
+    selection's cooperative launch, with the arrival counts started far below zero, ends
+    within a few seconds with code 16 in the device error word and no picks written, and
+    the next call on the same context is correct."""
+    import time
+    moe.moe_device_error(clear=True)
+    t0 = time.time()
+    moe.moe_selftest_wait_expiry(8192, 16, 2.0)
+    elapsed = time.time() - t0
+    assert moe.moe_device_error(clear=True) == 16
+    assert 0.9 < elapsed < 30.0, elapsed  # the 1 s limit, then every CTA returned
+    # the context is still usable
+    cfg = synth.LayerConfig("after_expiry", T=3000, d=128, F=256, E=8, k=0, dtype="bf16", x_std=1.0,
+                            w_std=0.05, wg_std=0.1, seed=91, routing="expert_choice",
+                            capacity_factor=2.0)
+    _check_ec_layer(moe, torch, cfg)
+    assert moe.moe_device_error(clear=False) == 0
+
+
 def test_layer_ec_e16(moe, torch):
     _check_ec_layer(moe, torch, synth.CONFIGS["ec_e16"])
 
