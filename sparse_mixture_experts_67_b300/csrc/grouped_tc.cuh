@@ -345,6 +345,20 @@ __device__ __forceinline__ TileCoord map_tile(const SmemT& S, int E, int n_tiles
 
 __device__ __forceinline__ float silu_fast(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
+// y[addr..addr+3] += v (a relaxed float4 reduction, as atomicAdd on float4),
+// with an L2 policy: evict_last keeps y's lines in L2 between the additions of
+// a token's two slots, which come from units of different experts.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void red_add_f4_hint(float* addr, float4 v, uint64_t pol) {
+  asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "l"(pol)
+               : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -377,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const float* __restrict__ topk_w = nullptr, int kslots = 1,
                       const __nv_bfloat16* __restrict__ gx = nullptr,
                       const int32_t* __restrict__ gsrc = nullptr, int gdiv = 1,
-                      int frag_store = 0) {
+                      int frag_store = 0, int y_keep = 0) {
   static_assert(PAIRING == 0 || PAIRING == 2, "single CTA or 2-CTA pair");
   constexpr bool PAIR = PAIRING == 2, CL = PAIR;
   static_assert(!(PAIR && (GATHER || BN != 256)), "2-CTA MMA: 256-wide tiles without gather");
@@ -713,6 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float wgt = (COMBINE && valid) ? topk_w[a] : 0.f;
         const int tok = a / kslots;
         float* Y = static_cast<float*>(out);
+        const uint64_t ypol = (COMBINE && y_keep) ? l2_evict_last_policy() : 0ull;
         // plain stores go straight from the fragments, the combine's atomics through
         // the staging (float4 additions covering four rows each measured faster)
         const bool use_frag = frag_store == 2 ? !COMBINE : frag_store == 1;
@@ -772,9 +787,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (COMBINE) {
                 const int rt = __shfl_sync(kFullMask, tok, r);
                 const float rw = __shfl_sync(kFullMask, wgt, r);
-                if (grow < c.row_end)
-                  atomicAdd(reinterpret_cast<float4*>(Y + (size_t)rt * N + n0 + cc + part * 4),
-                            make_float4(rw * val.x, rw * val.y, rw * val.z, rw * val.w));
+                if (grow < c.row_end) {
+                  float* ya = Y + (size_t)rt * N + n0 + cc + part * 4;
+                  const float4 add = make_float4(rw * val.x, rw * val.y, rw * val.z, rw * val.w);
+                  if (y_keep) red_add_f4_hint(ya, add, ypol);
+                  else atomicAdd(reinterpret_cast<float4*>(ya), add);
+                }
               } else if (grow < c.row_end) {
                 *reinterpret_cast<float4*>(Y + (size_t)grow * N + n0 + cc + part * 4) = val;
               }
@@ -886,7 +904,7 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   const int grid = (int)std::min<long long>(sms, max_tiles);
   return launch_k(grouped_tc_kernel<GATEUP, BN, COMBINE, GATHER>, dim3(grid), dim3(kThreads), sm, s,
                   nullptr, 0, a, b0, b1, offsets, R, E, N, K, out, perm, topk_w, kslots, gx, gsrc,
-                  gdiv, down_frag_store());
+                  gdiv, down_frag_store(), 0);
 }
 
 // How 256-wide launches pair CTAs: 2 = 2-CTA MMA (PAIR, the default), 0 =
@@ -906,7 +924,7 @@ template <bool GATEUP, bool COMBINE, int PAIRING>
 cudaError_t launch_cluster(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                            const int32_t* offsets, int R, int E, int N, int K, void* out,
                            cudaStream_t s, const int32_t* perm = nullptr,
-                           const float* topk_w = nullptr, int kslots = 1) {
+                           const float* topk_w = nullptr, int kslots = 1, int y_keep = 0) {
   constexpr int BN = 256;
   constexpr size_t sm = smem_bytes<BN, PAIRING == 2>();
   auto kern = grouped_tc_kernel<GATEUP, BN, COMBINE, false, PAIRING>;
@@ -938,15 +956,16 @@ cudaError_t launch_cluster(const CUtensorMap& a, const CUtensorMap& b0, const CU
   const int clusters = (int)std::min<long long>(max_clusters[dev], units);
   return launch_k(kern, dim3(2 * clusters), dim3(kThreads), sm, s, &attr, 1, a, b0, b1, offsets, R,
                   E, N, K, out, perm, topk_w, kslots, (const __nv_bfloat16*)nullptr,
-                  (const int32_t*)nullptr, 1, down_frag_store());
+                  (const int32_t*)nullptr, 1, down_frag_store(), y_keep);
 }
 
 template <bool GATEUP, bool COMBINE>
 cudaError_t launch_paired(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                           const int32_t* offsets, int R, int E, int N, int K, void* out,
                           cudaStream_t s, const int32_t* perm = nullptr,
-                          const float* topk_w = nullptr, int kslots = 1) {
-  return launch_cluster<GATEUP, COMBINE, 2>(a, b0, b1, offsets, R, E, N, K, out, s, perm, topk_w, kslots);
+                          const float* topk_w = nullptr, int kslots = 1, int y_keep = 0) {
+  return launch_cluster<GATEUP, COMBINE, 2>(a, b0, b1, offsets, R, E, N, K, out, s, perm, topk_w, kslots,
+                                            y_keep);
 }
 
 // MMA width for a launch.  256 everywhere it was measured best (both GEMMs
@@ -1052,9 +1071,13 @@ inline cudaError_t launch_down_combine_tc(const __nv_bfloat16* h, const int32_t*
       !tc::make_map(&m[1], w_down, (uint64_t)E * d, (uint64_t)F, mode == 2 ? 64 : 256) ||
       !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, 128))
     return cudaErrorInvalidValue;
+  // y's lines stay in L2 between a token's two additions when y takes at most a
+  // quarter of L2 (top2_d1024: 33.5 MB); a larger y would push out H and W_down
+  const size_t y_bytes = (size_t)((R + k - 1) / k) * d * sizeof(float);
+  const int y_keep = y_bytes <= (size_t)32 << 20 ? 1 : 0;
   if (mode != 0)
     return tc::launch_paired<false, true>(m[0], m[1], m[2], offsets, R, E, d, F, y, s, perm,
-                                          topk_w, k);
+                                          topk_w, k, y_keep);
   return tc::launch_bn<false, 256, true>(m[0], m[1], m[2], offsets, R, E, d, F, y, sms, s, perm,
                                          topk_w, k);
 }
