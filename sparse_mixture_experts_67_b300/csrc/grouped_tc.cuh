@@ -1072,7 +1072,8 @@ inline cudaError_t launch_down_combine_tc(const __nv_bfloat16* h, const int32_t*
       !tc::make_map(&m[2], w_down, (uint64_t)E * d, (uint64_t)F, 128))
     return cudaErrorInvalidValue;
   // y's lines stay in L2 between a token's two additions when y takes at most a
-  // quarter of L2 (top2_d1024: 33.5 MB); a larger y would push out H and W_down
+  // quarter of L2 (32 MiB: T = 8192, d = 1024 exactly); a larger y would push
+  // out H and W_down
   const size_t y_bytes = (size_t)((R + k - 1) / k) * d * sizeof(float);
   const int y_keep = y_bytes <= (size_t)32 << 20 ? 1 : 0;
   if (mode != 0)
