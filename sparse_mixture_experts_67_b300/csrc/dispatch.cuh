@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(kDispatchThreads)
                             float* __restrict__ f_frac, float* __restrict__ loss_frac,
                             float4* __restrict__ y_zero, int d4, int tokens_per_tile, int cap,
                             float* __restrict__ w_cap, int32_t* __restrict__ dropped,
-                            const float* __restrict__ z_partials, float* __restrict__ z_loss) {
+                            const float* __restrict__ z_partials, float* __restrict__ z_loss,
+                            int split) {
   pdl_begin();
   __shared__ int running[MOE_MAX_EXPERTS];
   __shared__ int s_tot[MOE_MAX_EXPERTS];
@@ -158,7 +159,9 @@ __global__ void __launch_bounds__(kDispatchThreads)
   __shared__ int s_tok[kDispatchThreads];
   __shared__ float s_fp[MOE_MAX_EXPERTS];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int me = blockIdx.x;
+  // split CTAs share tile me: each derives the same ranks, part 0 writes perm,
+  // inv_perm and the statistics, and the row copy and y's zeroing are shared out
+  const int me = blockIdx.x / split, part = blockIdx.x % split;
   const bool fused_scan = tile_base == nullptr;
   for (int e = fused_scan ? E : threadIdx.x; e < E; e += blockDim.x) {
     running[e] = tile_base[(size_t)me * E + e];
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
     int ex = incl - run;
     for (int e = e0; e < min(E, e0 + per); ++e) {
       const int v = s_tot[e];
-      if (me == 0) {
+      if (me == 0 && part == 0) {
         counts[e] = v;
         offsets[e] = ex;
       }
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
       running[e] += ex;
       ex += min(v, cap);
     }
-    if (me == 0 && lane == 31) {
+    if (me == 0 && part == 0 && lane == 31) {
       offsets[E] = ex;  // rows kept
       if (dropped) *dropped = A - ex;
     }
@@ -215,7 +218,9 @@ __global__ void __launch_bounds__(kDispatchThreads)
     const int tk0 = me * tokens_per_tile;
     const int tk1 = min(T, tk0 + tokens_per_tile);
     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (size_t i = (size_t)tk0 * d4 + threadIdx.x; i < (size_t)tk1 * d4; i += blockDim.x) y_zero[i] = z;
+    const size_t n = tk1 > tk0 ? (size_t)(tk1 - tk0) * d4 : 0;
+    const size_t i0 = (size_t)tk0 * d4 + n * part / split, i1 = (size_t)tk0 * d4 + n * (part + 1) / split;
+    for (size_t i = i0 + threadIdx.x; i < i1; i += blockDim.x) y_zero[i] = z;
   }
   __syncthreads();
   const int a0 = me * tile;
@@ -232,11 +237,13 @@ __global__ void __launch_bounds__(kDispatchThreads)
       int row = running[e] + rank;
       for (int w = 0; w < warp; ++w) row += wcnt[w][e];
       if (row - s_seg[e] < cap) {
-        perm[row] = a;
-        inv_perm[a] = row;
+        if (part == 0) {
+          perm[row] = a;
+          inv_perm[a] = row;
+        }
         s_row[threadIdx.x] = row;
       } else {  // past the expert's capacity: dropped
-        inv_perm[a] = -1;
+        if (part == 0) inv_perm[a] = -1;
         s_row[threadIdx.x] = -1;
       }
       s_tok[threadIdx.x] = a / k;
@@ -251,9 +258,9 @@ __global__ void __launch_bounds__(kDispatchThreads)
       }
       running[ee] += sum;
     }
-    if (x != nullptr) {  // copy this round's rows, one warp per row
+    if (x != nullptr) {  // copy this round's rows, one warp per row, rows shared out by part
       const int nvalid = min(kDispatchThreads, a1 - base);
-      for (int i = warp; i < nvalid; i += kDispatchWarps) {
+      for (int i = warp + part * kDispatchWarps; i < nvalid; i += kDispatchWarps * split) {
         if (s_row[i] < 0) continue;  // dropped assignment: no row
         const uint4* src = x + (size_t)s_tok[i] * vec_per_row;
         uint4* dst = x_perm + (size_t)s_row[i] * vec_per_row;
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
     }
     __syncthreads();
   }
-  if (w_cap != nullptr) {  // renormalise the kept weights of this tile's tokens
+  if (w_cap != nullptr && part == 0) {  // renormalise the kept weights of this tile's tokens
     for (int t = a0 / k + threadIdx.x; t < (a1 + k - 1) / k; t += blockDim.x) {
       float sum = 0.f;
       for (int j = 0; j < k; ++j)
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
       }
     }
   }
-  if (me != 0 || aux_partials == nullptr || !fused_scan) return;
+  if (me != 0 || part != 0 || aux_partials == nullptr || !fused_scan) return;
   // CTA 0: aux statistics from the router's per-tile partial sums of g
   for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) s_fp[e] = 0.f;
   __syncthreads();
