@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(kDispatchThreads)
   __shared__ int s_row[kDispatchThreads];
   __shared__ int s_tok[kDispatchThreads];
   __shared__ float s_fp[MOE_MAX_EXPERTS];
+  __shared__ int s_pre[kDispatchWarps][MOE_MAX_EXPERTS];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // split CTAs share tile me: each derives the same ranks, part 0 writes perm,
   // inv_perm and the statistics, and the row copy and y's zeroing are shared out
@@ -167,22 +168,65 @@ __global__ void __launch_bounds__(kDispatchThreads)
     running[e] = tile_base[(size_t)me * E + e];
     s_seg[e] = offsets[e];  // written by dispatch_scan_kernel
   }
-  for (int e = fused_scan ? warp : E; e < E; e += kDispatchWarps) {
-    int tot = 0, pre = 0;
-    for (int t = lane; t < tiles; t += 32) {
-      const int c = tile_counts[(size_t)t * E + e];
-      tot += c;
-      pre += t < me ? c : 0;
+  if (fused_scan && E < 32) {
+    // each expert's total over all tiles and over the tiles before this one: a
+    // warp per expert, lanes over tiles
+    for (int e = warp; e < E; e += kDispatchWarps) {
+      int tot = 0, pre = 0;
+      for (int t = lane; t < tiles; t += 32) {
+        const int c = tile_counts[(size_t)t * E + e];
+        tot += c;
+        pre += t < me ? c : 0;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        tot += __shfl_xor_sync(kFullMask, tot, off);
+        pre += __shfl_xor_sync(kFullMask, pre, off);
+      }
+      if (lane == 0) {
+        s_tot[e] = tot;
+        running[e] = pre;
+      }
+    }
+  } else if (fused_scan) {
+    // the same sums read row by row (a tile's E counts are contiguous, so a
+    // warp's loads are whole lines): lanes over experts, E / 32 per lane, warps
+    // over tiles; per-warp partials are added in shared memory (integers)
+    int tot[MOE_MAX_EXPERTS / 32], pre[MOE_MAX_EXPERTS / 32];
+#pragma unroll
+    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) tot[j] = pre[j] = 0;
+    for (int t = warp; t < tiles; t += kDispatchWarps) {
+      const int32_t* row = tile_counts + (size_t)t * E;
+#pragma unroll
+      for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E) {
+          const int c = row[e];
+          tot[j] += c;
+          pre[j] += t < me ? c : 0;
+        }
+      }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      tot += __shfl_xor_sync(kFullMask, tot, off);
-      pre += __shfl_xor_sync(kFullMask, pre, off);
+    for (int j = 0; j < MOE_MAX_EXPERTS / 32; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E) {
+        wcnt[warp][e] = tot[j];
+        s_pre[warp][e] = pre[j];
+      }
     }
-    if (lane == 0) {
-      s_tot[e] = tot;
-      running[e] = pre;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int tt = 0, pp = 0;
+#pragma unroll
+      for (int w = 0; w < kDispatchWarps; ++w) {
+        tt += wcnt[w][e];
+        pp += s_pre[w][e];
+      }
+      s_tot[e] = tt;
+      running[e] = pp;
     }
+    __syncthreads();  // the partials are read before wcnt is cleared below
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     for (int w = 0; w < kDispatchWarps; ++w) wcnt[w][e] = 0;
@@ -293,11 +337,29 @@ __global__ void __launch_bounds__(kDispatchThreads)
   // CTA 0: aux statistics from the router's per-tile partial sums of g
   for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += blockDim.x) s_fp[e] = 0.f;
   __syncthreads();
+  if (E >= 32) {
+    // column sums of the [tiles, E] partials read row by row: warp w sums rows
+    // w, w + 8, ... of lanes' experts, the warps' sums then added in warp order
+    // (a fixed order: deterministic)
+    for (int j = 0; j * 32 < E; ++j) {
+      const int e = lane + 32 * j;
+      float acc = 0.f;
+      if (e < E)
+        for (int r = warp; r < tiles; r += kDispatchWarps) acc += aux_partials[(size_t)r * E + e];
+      if (e < E) s_pre[warp][e] = __float_as_int(acc);
+    }
+    __syncthreads();
+  }
   for (int e = warp; e < E; e += kDispatchWarps) {
     float acc = 0.f;
-    for (int r = lane; r < tiles; r += 32) acc += aux_partials[(size_t)r * E + e];
+    if (E >= 32) {
+      if (lane == 0)
+        for (int w = 0; w < kDispatchWarps; ++w) acc += __int_as_float(s_pre[w][e]);
+    } else {
+      for (int r = lane; r < tiles; r += 32) acc += aux_partials[(size_t)r * E + e];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+    }
     if (lane == 0) {
       const float pe = acc / (float)T;
       const float fe = (float)s_tot[e] / (float)T;

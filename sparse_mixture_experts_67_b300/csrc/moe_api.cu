@@ -200,13 +200,14 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   const int32_t* base = separate_scan ? tile_base : nullptr;
-  // fewer tiles than two per SM: two CTAs share each tile's row copy (fine_e64:
-  // 256 tiles of 1 MiB of rows; measured faster than one CTA per tile)
+  // fewer tiles than two per SM: two CTAs share each tile's row copy (top2_d1024:
+  // 256 tiles; measured faster than one CTA per tile)
+  const int row_bytes = (int)(d * elt_size(dt));
   const int split = (x != nullptr && tiles < 2 * tc::sm_count()) ? 2 : 1;
   return cuda_status(launch_k(
       dispatch_scatter_kernel, dim3(tiles * split), dim3(kDispatchThreads), 0, s, nullptr, 0, topk_idx,
       (int)A, E, k, tile, tile_counts, base, tiles, perm, inv_perm, counts, offsets,
-      static_cast<const uint4*>(x), (int)(d * elt_size(dt) / 16), static_cast<uint4*>(x_perm),
+      static_cast<const uint4*>(x), row_bytes / 16, static_cast<uint4*>(x_perm),
       aux_partials, T, f, p, loss, f_frac, loss_frac, reinterpret_cast<float4*>(y_zero), d / 4,
       tile / k, cap, w_cap, dropped, z_partials, z_loss, split));
 }
