@@ -138,8 +138,12 @@ __global__ void probs_partials_kernel(const float* __restrict__ probs, int T, in
   }
 }
 
-// One CTA of kAuxThreads.  Warp w reduces experts w, w + 8, ...: each lane sums
-// a fixed strided subset of the partial rows, then a fixed butterfly.
+// One CTA of kAuxThreads.  Below 32 experts warp w reduces experts w, w + 8,
+// ...: each lane sums a fixed strided subset of the partial rows, then a fixed
+// butterfly.  From 32 experts on the rows are read whole (lanes over experts,
+// warp w summing rows w, w + 8, ... in order; coalesced, where the column walk
+// touches a line per lane) and the warps' sums are added in warp order.  Both
+// orders are fixed: deterministic.
 constexpr int kAuxThreads = 256;
 __global__ void __launch_bounds__(kAuxThreads)
     aux_finalize_kernel(const float* __restrict__ partials, int rows, const int32_t* __restrict__ counts,
@@ -149,15 +153,28 @@ __global__ void __launch_bounds__(kAuxThreads)
                         float* __restrict__ z_loss) {
   pdl_begin();
   __shared__ float s[MOE_MAX_EXPERTS];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int nwarps = kAuxThreads / 32;
+  __shared__ float s_w[nwarps][MOE_MAX_EXPERTS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < MOE_MAX_EXPERTS; e += kAuxThreads) s[e] = 0.f;
+  if (E >= 32) {
+    for (int e = lane; e < E; e += 32) {
+      float acc = 0.f;
+      for (int r = warp; r < rows; r += nwarps) acc += partials[(size_t)r * E + e];
+      s_w[warp][e] = acc;
+    }
+  }
   __syncthreads();
   for (int e = warp; e < E; e += nwarps) {
     float acc = 0.f;
-    for (int r = lane; r < rows; r += 32) acc += partials[(size_t)r * E + e];
+    if (E >= 32) {
+      if (lane == 0)
+        for (int w = 0; w < nwarps; ++w) acc += s_w[w][e];
+    } else {
+      for (int r = lane; r < rows; r += 32) acc += partials[(size_t)r * E + e];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
+    }
     if (lane == 0) {
       const float pe = acc / (float)T;
       const float fe = (float)counts[e] / (float)T;
