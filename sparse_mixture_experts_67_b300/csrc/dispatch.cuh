@@ -13,7 +13,8 @@
 //   scatter: each tile derives its per-expert bases from the count matrix,
 //            re-reads its assignments in order and ranks them among equal
 //            experts (warp match_any rank + per-warp counts in shared memory),
-//            giving perm / inv_perm bit-exactly.
+//            giving perm / inv_perm bit-exactly, and copies its rows (with
+//            few tiles, two CTAs share a tile: both rank, one writes).
 #pragma once
 
 #include "common.cuh"
