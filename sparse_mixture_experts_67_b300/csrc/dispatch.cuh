@@ -73,21 +73,75 @@ __global__ void __launch_bounds__(kDispatchThreads)
 // tiles before t, so a row at or past segment start + cap is a dropped one;
 // dropped (nullable) gets the number of dropped assignments.
 constexpr int kScanThreads = 1024;
+// EPL: experts per lane, ceil(E / 32).
+template <int EPL>
 __global__ void __launch_bounds__(kScanThreads)
     dispatch_scan_kernel(const int32_t* __restrict__ tile_counts, int tiles, int E, int A,
                          int32_t* __restrict__ tile_base, int32_t* __restrict__ counts,
                          int32_t* __restrict__ offsets, int cap, int32_t* __restrict__ dropped) {
   pdl_begin();
+  // Rows of the count matrix are read whole (a tile's E counts are contiguous):
+  // warp w owns tiles [w B, (w + 1) B).  With E > 32 lane l takes experts
+  // l, l + 32, ...; with E <= 32 lane l takes expert l % E of row l / E, so a
+  // warp step covers rpw = 32 / E rows (one row from E = 17 on).  Each lane
+  // loads U steps before it uses any, to keep several loads in flight.
+  // Pass 1 sums each block per expert; the block sums are scanned per expert
+  // and the totals across experts; pass 2 walks each block again with a
+  // running base per expert and writes its rows of tile_base.
+  constexpr int nwarps = kScanThreads / 32;
+  constexpr int U = 4;
   __shared__ int s_tot[MOE_MAX_EXPERTS];
   __shared__ int s_off[MOE_MAX_EXPERTS];
+  __shared__ int s_blk[nwarps][MOE_MAX_EXPERTS];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int nwarps = kScanThreads / 32;
-  for (int e = warp; e < E; e += nwarps) {
-    int acc = 0;
-    for (int t = lane; t < tiles; t += 32) acc += tile_counts[(size_t)t * E + e];
+  const int B = (tiles + nwarps - 1) / nwarps;
+  const int t0 = min(tiles, warp * B), t1 = min(tiles, t0 + B);
+  const int rpw = EPL == 1 ? 32 / E : 1;
+  const int r = EPL == 1 ? lane / E : 0;  // row of the step (r >= rpw: idle lane)
+  int ex[EPL];
+  bool on[EPL];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(kFullMask, acc, off);
-    if (lane == 0) s_tot[e] = acc;
+  for (int j = 0; j < EPL; ++j) {
+    ex[j] = EPL == 1 ? lane % E : lane + 32 * j;
+    on[j] = EPL == 1 ? r < rpw : ex[j] < E;
+  }
+  int sum[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) sum[j] = 0;
+  for (int tb = t0; tb < t1; tb += U * rpw) {
+    int v[U][EPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = tb + u * rpw + r;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        v[u][j] = on[j] && t < t1 ? tile_counts[(size_t)t * E + ex[j]] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) sum[j] += v[u][j];
+  }
+  if constexpr (EPL == 1) {  // add the rows of a step: lane (r, e) takes (r + off, e)
+    for (int off = 1; off < rpw; off <<= 1) {
+      const int nb = __shfl_down_sync(kFullMask, sum[0], off * E);
+      if (r + off < rpw) sum[0] += nb;
+    }
+    if (lane < E) s_blk[warp][lane] = sum[0];
+  } else {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j)
+      if (on[j]) s_blk[warp][ex[j]] = sum[j];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kScanThreads) {  // per expert: blocks' exclusive prefix
+    int run = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int v = s_blk[w][e];
+      s_blk[w][e] = run;
+      run += v;
+    }
+    s_tot[e] = run;
   }
   __syncthreads();
   if (warp == 0) {
@@ -101,35 +155,50 @@ __global__ void __launch_bounds__(kScanThreads)
       const int nb = __shfl_up_sync(kFullMask, incl, off);
       if (lane >= off) incl += nb;
     }
-    int ex = incl - run;
+    int exc = incl - run;
     for (int e = e0; e < min(E, e0 + per); ++e) {
-      s_off[e] = ex;
-      ex += min(s_tot[e], cap);
+      s_off[e] = exc;
+      exc += min(s_tot[e], cap);
     }
     if (lane == 31) {
-      offsets[E] = ex;  // rows kept
-      if (dropped) *dropped = A - ex;
+      offsets[E] = exc;  // rows kept
+      if (dropped) *dropped = A - exc;
     }
   }
   __syncthreads();
-  for (int e = warp; e < E; e += nwarps) {
-    int running = s_off[e];
-    for (int t0 = 0; t0 < tiles; t0 += 32) {
-      const int t = t0 + lane;
-      const int v = t < tiles ? tile_counts[(size_t)t * E + e] : 0;
-      int incl = v;
+  int run[EPL];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int nb = __shfl_up_sync(kFullMask, incl, off);
-        if (lane >= off) incl += nb;
+  for (int j = 0; j < EPL; ++j) run[j] = on[j] ? s_off[ex[j]] + s_blk[warp][ex[j]] : 0;
+  for (int tb = t0; tb < t1; tb += U * rpw) {
+    int v[U][EPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = tb + u * rpw + r;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j)
+        v[u][j] = on[j] && t < t1 ? tile_counts[(size_t)t * E + ex[j]] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = tb + u * rpw + r;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        int incl = v[u][j], step = v[u][j];
+        if constexpr (EPL == 1) {  // the step's rows before row r, and the step total
+          for (int off = 1; off < rpw; off <<= 1) {
+            const int nb = __shfl_up_sync(kFullMask, incl, off * E);
+            if (r >= off) incl += nb;
+          }
+          step = __shfl_sync(kFullMask, incl, (rpw - 1) * E + ex[0]);
+        }
+        if (on[j] && t < t1) tile_base[(size_t)t * E + ex[j]] = run[j] + incl - v[u][j];
+        run[j] += step;
       }
-      if (t < tiles) tile_base[(size_t)t * E + e] = running + incl - v;
-      running += __shfl_sync(kFullMask, incl, 31);
     }
-    if (lane == 0) {
-      counts[e] = s_tot[e];
-      offsets[e] = s_off[e];
-    }
+  }
+  for (int e = threadIdx.x; e < E; e += kScanThreads) {
+    counts[e] = s_tot[e];
+    offsets[e] = s_off[e];
   }
 }
 

@@ -192,8 +192,11 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   const bool separate_scan = (long long)tiles * tiles * E > kFusedScanMaxReads;
   if (separate_scan) {
-    e = launch_k(dispatch_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, nullptr, 0, tile_counts,
-                 tiles, E, (int)A, tile_base, counts, offsets, cap, dropped);
+    auto scan = E <= 32 ? dispatch_scan_kernel<1>
+              : E <= 64 ? dispatch_scan_kernel<2>
+              : E <= 128 ? dispatch_scan_kernel<4> : dispatch_scan_kernel<8>;
+    e = launch_k(scan, dim3(1), dim3(kScanThreads), 0, s, nullptr, 0, tile_counts, tiles, E,
+                 (int)A, tile_base, counts, offsets, cap, dropped);
     if (e == cudaSuccess && aux_partials)
       e = launch_k(aux_finalize_kernel, dim3(1), dim3(kAuxThreads), 0, s, nullptr, 0, aux_partials,
                    tiles, counts, T, E, k, f, p, loss, f_frac, loss_frac, z_partials, z_loss);

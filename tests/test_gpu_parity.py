@@ -144,6 +144,15 @@ PERMUTE_CASES = [
     ("all_to_one", 700, 64, 8, 1, "bf16", "one"),
     ("multi_tile_e256", 5000, 64, 256, 2, "bf16", "random"),
     ("fp32_e8", 333, 16, 8, 2, "f32", "random"),
+    # tiles^2 * E above the fused scan's bound (a tile holds 32 tokens for E <= 16, else
+    # 64), so the one-CTA scan writes the per-tile bases: 1, 2, 4 and 8 experts per lane,
+    # packed rows for E <= 16 (5, 8), one row per step for E = 24
+    ("separate_scan_e64", 200000, 64, 64, 4, "bf16", "random"),
+    ("separate_scan_e8", 300000, 64, 8, 2, "bf16", "skewed"),
+    ("separate_scan_e5", 250000, 64, 5, 1, "bf16", "random"),
+    ("separate_scan_e24", 60000, 32, 24, 2, "f32", "random"),
+    ("separate_scan_e100", 30000, 64, 100, 2, "bf16", "skewed"),
+    ("separate_scan_e256", 20000, 64, 256, 2, "bf16", "random"),
 ]
 
 
@@ -367,6 +376,41 @@ def test_layer_capacity_limited(moe, torch, E, k, cf):
         assert np.all(_np(y) == 0)
     else:
         assert_close_output(_np(y), y_ref, "bf16", what=f"y[{cfg.name}]", ref_bf16_h=y_ref_h)
+
+
+def test_layer_capacity_separate_scan(moe, torch):
+    """Capacity-limited top-2 over 64 experts at T = 20000: 313 router tiles of 128
+    assignments, so 313^2 * 64 reads send the counts through the one-CTA scan, which
+    applies the capacity to the segment bases.  Routing outputs are checked whole, y
+    on every 8th token (the oracle's tokens are independent)."""
+    E, k, cf = 64, 2, 0.8
+    cfg = synth.small_config("cap_scan_e64", 20000, 256, 384, E, k, "bf16", seed=77, x_std=1.0,
+                             w_std=0.02, wg_std=0.1, bias="zipf")
+    inp = cached_inputs(cfg)
+    w = dev_weights(inp)
+    x = to_dev(inp.x)
+    T = cfg.T
+    outs = {"topk_idx": torch.empty((T, k), dtype=torch.int32, device="cuda"),
+            "topk_w": torch.empty((T, k), dtype=torch.float32, device="cuda"),
+            "logits": torch.empty((T, E), dtype=torch.float32, device="cuda"),
+            "counts": torch.empty((E,), dtype=torch.int32, device="cuda"),
+            "offsets": torch.empty((E + 1,), dtype=torch.int32, device="cuda"),
+            "dropped": torch.full((1,), -7, dtype=torch.int32, device="cuda")}
+    y = moe.moe_layer_forward(x, w, k=k, capacity_factor=cf, outputs=outs, capacity=True)
+    torch.cuda.synchronize()
+    s_gpu = _np(outs["logits"]).astype(np.float64)
+    idx_g, w_cap, kept, dropped, load, cap = oracle.capacity_route(s_gpu, k, float(np.float32(cf)))
+    np.testing.assert_array_equal(_np(outs["topk_idx"]), idx_g)
+    np.testing.assert_array_equal(_np(outs["counts"]), np.bincount(idx_g.ravel(), minlength=E))
+    np.testing.assert_array_equal(_np(outs["offsets"]), np.concatenate([[0], np.cumsum(load)]))
+    assert int(_np(outs["dropped"])[0]) == dropped and dropped > 0
+    np.testing.assert_allclose(_np(outs["topk_w"]), w_cap, rtol=0, atol=2e-6)
+    sub = np.arange(0, T, 8)
+    x64 = synth.to_f64(inp.x)[sub]
+    experts = synth.ExpertsF64(inp.w_gate, inp.w_up, inp.w_down)
+    y_ref = oracle.moe_forward(x64, idx_g[sub], w_cap[sub], experts)
+    y_ref_h = oracle.moe_forward(x64, idx_g[sub], w_cap[sub], experts, round_h=oracle.bf16_round)
+    assert_close_output(_np(y)[sub], y_ref, "bf16", what="y[cap_scan_e64]", ref_bf16_h=y_ref_h)
 
 
 @pytest.mark.slow
