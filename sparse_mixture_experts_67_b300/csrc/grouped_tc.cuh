@@ -320,12 +320,13 @@ struct TileCoord {
   int e, row0, row_end, nt;
 };
 
-// Tiles are enumerated expert by expert; inside an expert the 128-row block
-// varies fastest and the n-block slowest, so the CTAs of one wave share each
-// weight tile (read from HBM once) while the expert's rows stay in L2.
+// Tiles are enumerated expert by expert.  Inside an expert the row blocks go
+// in groups of `group` (0: one group of all of them); inside a group the row
+// block varies fastest and the n-block slowest, so the CTAs of one wave share
+// each weight tile (read from HBM once) while the group's rows stay in L2.
 template <class SmemT>
 __device__ __forceinline__ TileCoord map_tile(const SmemT& S, int E, int n_tiles, int tile,
-                                              int unit_rows = BM) {
+                                              int unit_rows = BM, int group = 0) {
   TileCoord c;
   int lo = 0, hi = E;  // S.cum[lo] * n_tiles <= tile < S.cum[hi] * n_tiles
   while (hi - lo > 1) {
@@ -335,10 +336,16 @@ __device__ __forceinline__ TileCoord map_tile(const SmemT& S, int E, int n_tiles
   }
   const int m_tiles = S.cum[lo + 1] - S.cum[lo];
   const int local = tile - S.cum[lo] * n_tiles;
-  const int nt = local / m_tiles;
+  int g0 = 0, gs = m_tiles;  // the group's first row block and its row blocks
+  if (group > 0 && m_tiles > group) {
+    g0 = min(local / (group * n_tiles), (m_tiles - 1) / group) * group;
+    gs = min(group, m_tiles - g0);
+  }
+  const int in = local - g0 * n_tiles;
+  const int nt = in / gs;
   c.e = lo;
   c.nt = nt;
-  c.row0 = S.off[lo] + (local - nt * m_tiles) * unit_rows;
+  c.row0 = S.off[lo] + (g0 + in - nt * gs) * unit_rows;
   c.row_end = S.off[lo + 1];
   return c;
 }
@@ -410,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kTileN = GATEUP ? BN / 2 : BN;  // output columns per tile
   constexpr int kUnitRows = CL ? 2 * BM : BM;  // rows of one work unit (a cluster's)
+  constexpr int kGroup = GATEUP ? 0 : 8;  // row blocks per raster group (down: 8)
   const uint32_t crank = CL ? cluster_ctarank() : 0u;
   const int unit0 = CL ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int ustride = CL ? (int)(gridDim.x >> 1) : (int)gridDim.x;
@@ -484,13 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (u < full_units) {
       // down: the last experts first, whose H rows the gate/up kernel wrote last
       // (still in L2 when this kernel starts)
-      c = map_tile(S, E, n_tiles, GATEUP ? u : full_units - 1 - u, kUnitRows);
+      c = map_tile(S, E, n_tiles, GATEUP ? u : full_units - 1 - u, kUnitRows, kGroup);
       c.row0 += (int)crank * BM;  // this CTA's half of the cluster's rows
       col_off = 0;
       width = kTileN;
     } else {
       const int v = u - full_units;
-      c = map_tile(S, E, n_tiles, full_units + (v >> 1), kUnitRows);
+      c = map_tile(S, E, n_tiles, full_units + (v >> 1), kUnitRows, kGroup);
       c.row0 += (int)crank * BM;
       col_off = (v & 1) * (kTileN / 2);
       width = kTileN / 2;
