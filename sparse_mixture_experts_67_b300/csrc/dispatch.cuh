@@ -51,7 +51,9 @@ __global__ void __launch_bounds__(kDispatchThreads)
 // inv_perm.  The tile's first dispatch row per expert comes from tile_base
 // when given (dispatch_scan_kernel), else from the count matrix directly:
 // every CTA reduces the [tiles, E] counts itself (totals, and the sum over
-// the tiles before its own), warp per expert, lanes over tiles; the expert
+// the tiles before its own; below 32 experts a warp per expert with lanes over
+// tiles, from 32 on lanes over experts and warps over tiles, so each load
+// reads a whole row); the expert
 // offsets are the exclusive scan of the totals, and CTA 0 also writes counts /
 // offsets and, given aux_partials, the load-balancing statistics (same
 // reduction order as aux_finalize_kernel).
