@@ -87,13 +87,14 @@ __device__ __forceinline__ float order_key_float(uint32_t k) {
 //     in chunks from the front and the phase stops at the first chunk that
 //     reaches rank C.  Ranks below C place the token: ec_idx / ec_score at the
 //     rank, pos[e, t] = e * C + rank.  The column's max and sum come from the
-//     slices' pairs in slice order.
+//     slices' pairs, merged by one warp in a fixed order.
 constexpr int kEcSlice = 1024;            // tokens per stage-1 CTA (one per thread)
 constexpr int kEcRankThreads = 1024;
 constexpr size_t kEcRankSmemMax = 160 * 1024;  // dynamic shared memory of the rank phase, at most
 // The lists are staged in shared memory up to this many keys in all (80 KB): a
 // larger staging copy costs more than the few search chunks it speeds up
-// (T = 32768, E = 16: 32 lists of 1024, staged 92 us, searched in L2 85 us).
+// (T = 32768, E = 16, 32 lists of 1024: the whole route took 92 us with the
+// lists staged, 80 us with the searches in L2).
 constexpr size_t kEcStageKeysMax = 20480;
 
 inline int ec_slices(int T) { return T <= 0 ? 0 : ceil_div(T, kEcSlice); }
