@@ -67,37 +67,53 @@ __global__ void __launch_bounds__(kDispatchThreads)
 // x != nullptr copies x[a / k] into x_perm[row] (16-byte vectors, warp per
 // row); y_zero != nullptr zeroes the y rows of the tile's tokens
 // (tokens_per_tile of them) for an accumulating combine downstream.
-// Large count matrices: one CTA computes every tile's first dispatch row per
-// expert (tile_base), the counts and the offsets; the scatter CTAs then read
-// their row of tile_base instead of reducing the whole matrix each.
+// Large count matrices: dispatch_scan_kernel computes every tile's first
+// dispatch row per expert (tile_base), the counts and the offsets, over all
+// SMs in two launches (or in one CTA); the scatter CTAs then read their row of
+// tile_base instead of reducing the whole matrix each.
 // cap: per-expert capacity (INT_MAX: none).  Segments hold min(count, cap)
 // rows; tile_base[t, e] is the segment start plus the expert's assignments in
 // tiles before t, so a row at or past segment start + cap is a dropped one;
 // dropped (nullable) gets the number of dropped assignments.
 constexpr int kScanThreads = 1024;
+// The scan over all SMs uses at most this many CTAs (block sums [nb, E]).
+constexpr int kScanBlocks = 160;
+// Modes of dispatch_scan_kernel.  kScanWhole: one CTA over all tiles.  Over
+// nb CTAs, each owning a contiguous range of tiles: kScanBlockSums writes the
+// range's per-expert sums to blk[b, E]; kScanBases (the next launch) takes the
+// sums of the ranges before its own and of all ranges from blk and writes its
+// rows of tile_base (CTA 0 also the counts, offsets and drops).
+enum { kScanWhole = 0, kScanBlockSums = 1, kScanBases = 2 };
 // EPL: experts per lane, ceil(E / 32).
 template <int EPL>
 __global__ void __launch_bounds__(kScanThreads)
     dispatch_scan_kernel(const int32_t* __restrict__ tile_counts, int tiles, int E, int A,
                          int32_t* __restrict__ tile_base, int32_t* __restrict__ counts,
-                         int32_t* __restrict__ offsets, int cap, int32_t* __restrict__ dropped) {
+                         int32_t* __restrict__ offsets, int cap, int32_t* __restrict__ dropped,
+                         int mode, int32_t* __restrict__ blk) {
   pdl_begin();
   // Rows of the count matrix are read whole (a tile's E counts are contiguous):
-  // warp w owns tiles [w B, (w + 1) B).  With E > 32 lane l takes experts
-  // l, l + 32, ...; with E <= 32 lane l takes expert l % E of row l / E, so a
-  // warp step covers rpw = 32 / E rows (one row from E = 17 on).  Each lane
-  // loads U steps before it uses any, to keep several loads in flight.
-  // Pass 1 sums each block per expert; the block sums are scanned per expert
-  // and the totals across experts; pass 2 walks each block again with a
-  // running base per expert and writes its rows of tile_base.
+  // the CTA's range of tiles is cut into nwarps blocks, warp w owning block w.
+  // With E > 32 lane l takes experts l, l + 32, ...; with E <= 32 lane l takes
+  // expert l % E of row l / E, so a warp step covers rpw = 32 / E rows (one
+  // row from E = 17 on).  Each lane loads U steps before it uses any, to keep
+  // several loads in flight.  Pass 1 sums each block per expert; the block
+  // sums are scanned per expert (and, over several CTAs, offset by the ranges
+  // before this one) and the totals across experts; pass 2 walks each block
+  // again with a running base per expert and writes its rows of tile_base.
   constexpr int nwarps = kScanThreads / 32;
   constexpr int U = 4;
   __shared__ int s_tot[MOE_MAX_EXPERTS];
   __shared__ int s_off[MOE_MAX_EXPERTS];
+  __shared__ int s_pre[MOE_MAX_EXPERTS];
   __shared__ int s_blk[nwarps][MOE_MAX_EXPERTS];
+  __shared__ int s_part[2][kScanThreads];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = (tiles + nwarps - 1) / nwarps;
-  const int t0 = min(tiles, warp * B), t1 = min(tiles, t0 + B);
+  const int nb = gridDim.x, bid = blockIdx.x;
+  const int BR = (tiles + nb - 1) / nb;  // tiles per CTA range
+  const int r0 = min(tiles, bid * BR), r1 = min(tiles, r0 + BR);
+  const int B = (r1 - r0 + nwarps - 1) / nwarps;
+  const int t0 = min(r1, r0 + warp * B), t1 = min(r1, t0 + B);
   const int rpw = EPL == 1 ? 32 / E : 1;
   const int r = EPL == 1 ? lane / E : 0;  // row of the step (r >= rpw: idle lane)
   int ex[EPL];
@@ -126,8 +142,8 @@ __global__ void __launch_bounds__(kScanThreads)
   }
   if constexpr (EPL == 1) {  // add the rows of a step: lane (r, e) takes (r + off, e)
     for (int off = 1; off < rpw; off <<= 1) {
-      const int nb = __shfl_down_sync(kFullMask, sum[0], off * E);
-      if (r + off < rpw) sum[0] += nb;
+      const int nb2 = __shfl_down_sync(kFullMask, sum[0], off * E);
+      if (r + off < rpw) sum[0] += nb2;
     }
     if (lane < E) s_blk[warp][lane] = sum[0];
   } else {
@@ -143,7 +159,39 @@ __global__ void __launch_bounds__(kScanThreads)
       s_blk[w][e] = run;
       run += v;
     }
-    s_tot[e] = run;
+    s_tot[e] = run;  // this CTA's range
+    s_pre[e] = 0;
+  }
+  if (mode == kScanBlockSums) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kScanThreads) blk[(size_t)bid * E + e] = s_tot[e];
+    return;
+  }
+  if (mode == kScanBases) {
+    // the ranges before this one and all ranges, from the block sums: G groups
+    // of E threads, group g taking ranges g, g + G, ... (integer sums: exact)
+    const int G = max(1, kScanThreads / E);
+    const int g = (int)threadIdx.x / E, e = (int)threadIdx.x - g * E;
+    if (g < G) {
+      int pre = 0, tot = 0;
+      for (int b2 = g; b2 < nb; b2 += G) {
+        const int v = blk[(size_t)b2 * E + e];
+        tot += v;
+        if (b2 < bid) pre += v;
+      }
+      s_part[0][threadIdx.x] = pre;
+      s_part[1][threadIdx.x] = tot;
+    }
+    __syncthreads();
+    for (int e2 = threadIdx.x; e2 < E; e2 += kScanThreads) {
+      int pre = 0, tot = 0;
+      for (int g2 = 0; g2 < G; ++g2) {
+        pre += s_part[0][g2 * E + e2];
+        tot += s_part[1][g2 * E + e2];
+      }
+      s_pre[e2] = pre;
+      s_tot[e2] = tot;
+    }
   }
   __syncthreads();
   if (warp == 0) {
@@ -154,15 +202,15 @@ __global__ void __launch_bounds__(kScanThreads)
     int incl = run;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-      const int nb = __shfl_up_sync(kFullMask, incl, off);
-      if (lane >= off) incl += nb;
+      const int nb2 = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += nb2;
     }
     int exc = incl - run;
     for (int e = e0; e < min(E, e0 + per); ++e) {
       s_off[e] = exc;
       exc += min(s_tot[e], cap);
     }
-    if (lane == 31) {
+    if (lane == 31 && bid == 0) {
       offsets[E] = exc;  // rows kept
       if (dropped) *dropped = A - exc;
     }
@@ -170,7 +218,8 @@ __global__ void __launch_bounds__(kScanThreads)
   __syncthreads();
   int run[EPL];
 #pragma unroll
-  for (int j = 0; j < EPL; ++j) run[j] = on[j] ? s_off[ex[j]] + s_blk[warp][ex[j]] : 0;
+  for (int j = 0; j < EPL; ++j)
+    run[j] = on[j] ? s_off[ex[j]] + s_pre[ex[j]] + s_blk[warp][ex[j]] : 0;
   for (int tb = t0; tb < t1; tb += U * rpw) {
     int v[U][EPL];
 #pragma unroll
@@ -188,8 +237,8 @@ __global__ void __launch_bounds__(kScanThreads)
         int incl = v[u][j], step = v[u][j];
         if constexpr (EPL == 1) {  // the step's rows before row r, and the step total
           for (int off = 1; off < rpw; off <<= 1) {
-            const int nb = __shfl_up_sync(kFullMask, incl, off * E);
-            if (r >= off) incl += nb;
+            const int nb2 = __shfl_up_sync(kFullMask, incl, off * E);
+            if (r >= off) incl += nb2;
           }
           step = __shfl_sync(kFullMask, incl, (rpw - 1) * E + ex[0]);
         }
@@ -198,10 +247,11 @@ __global__ void __launch_bounds__(kScanThreads)
       }
     }
   }
-  for (int e = threadIdx.x; e < E; e += kScanThreads) {
-    counts[e] = s_tot[e];
-    offsets[e] = s_off[e];
-  }
+  if (bid == 0)
+    for (int e = threadIdx.x; e < E; e += kScanThreads) {
+      counts[e] = s_tot[e];
+      offsets[e] = s_off[e];
+    }
 }
 
 // The in-CTA reduction reads tiles * E counts per CTA; above this many

@@ -150,7 +150,9 @@ moe_status moe_expert_choice_route(const void* x, const void* w_g, const float* 
 size_t moe_permute_workspace_size(int T, int E, int k) {
   if (T < 0 || E < 1 || k < 1) return 0;
   const int tiles = dispatch_tiles((long long)T * k, router_tokens(E) * k);
-  return 2 * align256((size_t)tiles * E * sizeof(int32_t)) + 256;
+  // tile counts | tile bases | the scan's block sums [kScanBlocks, E]
+  return 2 * align256((size_t)tiles * E * sizeof(int32_t)) +
+         align256((size_t)kScanBlocks * E * sizeof(int32_t)) + 256;
 }
 
 moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, int T, int d,
@@ -176,7 +178,8 @@ moe_status moe_gather_rows(const void* x, const int32_t* src, int R, int div, in
 static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T, int d, int E, int k,
                                   moe_dtype dt, void* x_perm, int32_t* counts, int32_t* offsets,
                                   int32_t* perm, int32_t* inv_perm, int32_t* tile_counts,
-                                  int32_t* tile_base, int tile, bool counts_ready, cudaStream_t s,
+                                  int32_t* tile_base, int32_t* scan_blk, int tile,
+                                  bool counts_ready, cudaStream_t s,
                                   const float* aux_partials = nullptr, float* f = nullptr,
                                   float* p = nullptr, float* loss = nullptr,
                                   float* y_zero = nullptr, float* f_frac = nullptr,
@@ -195,8 +198,20 @@ static moe_status dispatch_launch(const void* x, const int32_t* topk_idx, int T,
     auto scan = E <= 32 ? dispatch_scan_kernel<1>
               : E <= 64 ? dispatch_scan_kernel<2>
               : E <= 128 ? dispatch_scan_kernel<4> : dispatch_scan_kernel<8>;
-    e = launch_k(scan, dim3(1), dim3(kScanThreads), 0, s, nullptr, 0, tile_counts, tiles, E,
-                 (int)A, tile_base, counts, offsets, cap, dropped);
+    // over all SMs when the block-sum scratch is given: the ranges' sums, then
+    // the bases; else one CTA
+    const int nb = scan_blk ? std::min(std::min(kScanBlocks, tc::sm_count()), tiles) : 1;
+    if (nb > 1) {
+      e = launch_k(scan, dim3(nb), dim3(kScanThreads), 0, s, nullptr, 0, tile_counts, tiles, E,
+                   (int)A, tile_base, counts, offsets, cap, dropped, (int)kScanBlockSums, scan_blk);
+      if (e == cudaSuccess)
+        e = launch_k(scan, dim3(nb), dim3(kScanThreads), 0, s, nullptr, 0, tile_counts, tiles, E,
+                     (int)A, tile_base, counts, offsets, cap, dropped, (int)kScanBases, scan_blk);
+    } else {
+      e = launch_k(scan, dim3(1), dim3(kScanThreads), 0, s, nullptr, 0, tile_counts, tiles, E,
+                   (int)A, tile_base, counts, offsets, cap, dropped, (int)kScanWhole,
+                   (int32_t*)nullptr);
+    }
     if (e == cudaSuccess && aux_partials)
       e = launch_k(aux_finalize_kernel, dim3(1), dim3(kAuxThreads), 0, s, nullptr, 0, aux_partials,
                    tiles, counts, T, E, k, f, p, loss, f_frac, loss_frac, z_partials, z_loss);
@@ -245,8 +260,9 @@ moe_status moe_permute(const void* x, const int32_t* topk_idx, int T, int d, int
   cv.used = (256 - (reinterpret_cast<uintptr_t>(ws) & 255)) & 255;
   int32_t* tile_counts = cv.take<int32_t>((size_t)tiles * E);
   int32_t* tile_base = cv.take<int32_t>((size_t)tiles * E);
+  int32_t* scan_blk = cv.take<int32_t>((size_t)kScanBlocks * E);
   return dispatch_launch(x, topk_idx, T, d, E, k, dt, x_perm, counts, offsets, perm, inv_perm,
-                         tile_counts, tile_base, tile, false, s);
+                         tile_counts, tile_base, scan_blk, tile, false, s);
 }
 
 static moe_status check_experts(int R, int d, int F, int E, moe_dtype dt) {
@@ -515,6 +531,8 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
   int32_t* tile_counts = static_cast<int32_t*>(pw);
   int32_t* tile_base = reinterpret_cast<int32_t*>(static_cast<char*>(pw) +
                                                   align256((size_t)tiles * D.E * sizeof(int32_t)));
+  int32_t* scan_blk = reinterpret_cast<int32_t*>(static_cast<char*>(pw) +
+                                                 2 * align256((size_t)tiles * D.E * sizeof(int32_t)));
   if (launch_router(x, w->w_g, w->bias, D.T, D.d, D.E, k, D.dtype == MOE_BF16, idx, tw, O.logits,
                     nullptr, aux, s, tile_counts, nullptr, D.flags,
                     O.z_loss ? zpart : nullptr) != cudaSuccess)
@@ -531,7 +549,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const moe_layer_weights
     cap = capd >= (double)A ? (int)A : (int)capd;
   }
   st = dispatch_launch(x, idx, D.T, D.d, D.E, k, D.dtype, x_perm, counts, offsets, perm, inv_perm,
-                       tile_counts, tile_base, tile, true, s, aux, O.f ? O.f : fpl,
+                       tile_counts, tile_base, scan_blk, tile, true, s, aux, O.f ? O.f : fpl,
                        O.p ? O.p : fpl + D.E, O.loss ? O.loss : fpl + 2 * D.E,
                        fused ? y : nullptr, O.f_frac, O.loss_frac, cap,
                        capacity ? tw : nullptr, O.dropped, O.z_loss ? zpart : nullptr, O.z_loss);

@@ -82,5 +82,5 @@ extern "C" moe_status moe_permute_noalloc(const void* x, const int32_t* topk_idx
   // second half of the array holds the tile bases when the separate scan runs
   int32_t* tile_base = scratch + kNoAllocHalf;
   return dispatch_launch(x, topk_idx, T, d, E, k, dt, x_perm, counts, offsets, perm, inv_perm,
-                         tile_counts, tile_base, kTile, false, s);
+                         tile_counts, tile_base, nullptr, kTile, false, s);  // one-CTA scan
 }
