@@ -107,6 +107,11 @@ def test_permute_and_experts_errors(L):
     z = _nullp()
     ws = L.moe_permute_workspace_size(100, 8, 2)
     assert ws > 0
+    # tile counts and tile bases (tiles of 32 tokens' assignments at E <= 16, 64 above),
+    # plus the block sums of the scan over all SMs (up to 160 blocks of E counts)
+    for T, E, k in ((100, 8, 2), (200000, 64, 4), (20000, 256, 2)):
+        tiles = -(-T * k // ((32 if E <= 16 else 64) * k))
+        assert L.moe_permute_workspace_size(T, E, k) >= 4 * (2 * tiles * E + 160 * E)
     assert L.moe_permute(_p(), _p(), 100, 64, 8, 2, 1, _p(), _p(), _p(), _p(), _p(), _p(), ws - 1, z) == 3
     assert L.moe_permute(_p(), _p(), 100, 64, 8, 2, 1, _p(), _p(), _p(), _p(), _p(), z, ws, z) == 3
     assert L.moe_permute(_p(), _p(), 100, 64, 8, 9, 1, _p(), _p(), _p(), _p(), _p(), _p(), ws, z) == 1
